@@ -1,0 +1,144 @@
+/*
+ * sgmv_oracle.c -- the correctness oracle for segmented LoRA apply (SGMV), in plain C, fp64.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may load, link or call this file:
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg use it.  It shares no
+ * code, header, table or constant generator with the CUDA library; the two meet only through
+ * the seeded inputs a test hands to both.
+ *
+ * What is computed, and where it comes from
+ * -----------------------------------------
+ * "Punica Guide: Multi-Tenant LoRA Serving with SGMV", section "The Heterogeneous Batching
+ * Bottleneck: Why Standard Serving Stalls", the per-request equation
+ *       y_i = x_i W0 + (alpha/r) x_i A_{k(i)} B_{k(i)},
+ *   with A_k of shape d_in x r and B_k of shape r x d_out.  The caller supplies y already
+ *   holding x_i W0 (the base output) and scale = alpha/r; the oracle adds the second term.
+ * Same page, section "The SGMV Mathematical Formulation": tokens are grouped into contiguous
+ *   segments [s_i, s_{i+1}), each bound to one adapter through a pointer array.  Segments are
+ *   indexed 0..S-1 with S+1 offsets s_0..s_S (the page's "i in [1, N]" is read as the S
+ *   segments between the S+1 offsets).
+ * Same page, section "Step-by-Step Implementation: Multi-LoRA Batching Dispatcher in PyTorch":
+ *   the reference semantics is a per-row loop x[i] @ A[id] @ B[id]; this file is that loop, in
+ *   fp64, with the alpha/r factor of the equation above.
+ *
+ * Readings where the pages are silent (all stated again in the design notes):
+ *   - y is accumulated into (+=), never overwritten: the equation's first term is the base
+ *     output that already sits in y.
+ *   - weights of adapter k are one contiguous block [L][h_in][r] (A) and [L][r][h_out] (B),
+ *     row-major; layer_idx selects the [h_in][r] / [r][h_out] slice inside the block.
+ *   - a segment whose adapter id is negative carries no adapter: its rows are left unchanged.
+ *   - a segment with s_{i+1} <= s_i is empty.
+ *
+ * Every function here is pinned by the CPU tests (tests/test_oracle_pins.py) against closed
+ * forms, library matmuls, brute force and invariants; none is "parity unpinned".
+ */
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+/* Bits of the table check, as documented in the library header. */
+#define ORACLE_BAD_ORDER    1  /* seg_starts decreases somewhere                     */
+#define ORACLE_BAD_FIRST    2  /* seg_starts[0] < 0                                  */
+#define ORACLE_BAD_LAST     4  /* seg_starts[S] > M                                  */
+#define ORACLE_BAD_ADAPTER  8  /* adapter id >= num_adapters (negative = no adapter) */
+
+/* v[t][c] = sum_j x[t][j] * A_k[layer][j][c]   for every row t of every segment.
+ * "Shrink": the first factor of the equation, x_i A_k (h_in -> r).  v is [M][r]; rows outside
+ * all segments are left as they are. */
+int oracle_sgmv_shrink(double *v, const double *x, const double *const *A,
+                       const int32_t *seg_starts, const int32_t *seg_adapter,
+                       int32_t num_segments, int32_t layer_idx, int32_t h_in, int32_t r)
+{
+    for (int32_t i = 0; i < num_segments; ++i) {
+        const int32_t k = seg_adapter[i];
+        if (k < 0) continue;
+        const double *Ak = A[k] + (size_t)layer_idx * (size_t)h_in * (size_t)r;
+        for (int32_t t = seg_starts[i]; t < seg_starts[i + 1]; ++t) {
+            const double *xt = x + (size_t)t * (size_t)h_in;
+            double *vt = v + (size_t)t * (size_t)r;
+            for (int32_t c = 0; c < r; ++c) {
+                double s = 0.0;
+                for (int32_t j = 0; j < h_in; ++j)
+                    s += xt[j] * Ak[(size_t)j * (size_t)r + (size_t)c];
+                vt[c] = s;
+            }
+        }
+    }
+    return 0;
+}
+
+/* y[t][n] += scale * sum_c v[t][c] * B_k[layer][c][n]   for every row t of every segment.
+ * "Expand": the second factor, (x_i A_k) B_k (r -> h_out), times alpha/r, added into y. */
+int oracle_sgmv_expand(double *y, const double *v, const double *const *B,
+                       const int32_t *seg_starts, const int32_t *seg_adapter,
+                       int32_t num_segments, int32_t layer_idx, int32_t r, int32_t h_out,
+                       double scale)
+{
+    for (int32_t i = 0; i < num_segments; ++i) {
+        const int32_t k = seg_adapter[i];
+        if (k < 0) continue;
+        const double *Bk = B[k] + (size_t)layer_idx * (size_t)r * (size_t)h_out;
+        for (int32_t t = seg_starts[i]; t < seg_starts[i + 1]; ++t) {
+            const double *vt = v + (size_t)t * (size_t)r;
+            double *yt = y + (size_t)t * (size_t)h_out;
+            for (int32_t n = 0; n < h_out; ++n) {
+                double s = 0.0;
+                for (int32_t c = 0; c < r; ++c)
+                    s += vt[c] * Bk[(size_t)c * (size_t)h_out + (size_t)n];
+                yt[n] += scale * s;
+            }
+        }
+    }
+    return 0;
+}
+
+/* y[t] += scale * (x[t] A_k) B_k   -- the whole LoRA term, one token at a time, one segment
+ * after another (the per-row loop of the dispatcher listing, with the alpha/r factor). */
+int oracle_lora_apply(double *y, const double *x, const double *const *A,
+                      const double *const *B, const int32_t *seg_starts,
+                      const int32_t *seg_adapter, int32_t num_segments, int32_t layer_idx,
+                      int32_t h_in, int32_t h_out, int32_t r, double scale)
+{
+    double *v = (double *)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+    if (!v) return -1;
+    for (int32_t i = 0; i < num_segments; ++i) {
+        const int32_t k = seg_adapter[i];
+        if (k < 0) continue;
+        const double *Ak = A[k] + (size_t)layer_idx * (size_t)h_in * (size_t)r;
+        const double *Bk = B[k] + (size_t)layer_idx * (size_t)r * (size_t)h_out;
+        for (int32_t t = seg_starts[i]; t < seg_starts[i + 1]; ++t) {
+            const double *xt = x + (size_t)t * (size_t)h_in;
+            double *yt = y + (size_t)t * (size_t)h_out;
+            for (int32_t c = 0; c < r; ++c) {
+                double s = 0.0;
+                for (int32_t j = 0; j < h_in; ++j)
+                    s += xt[j] * Ak[(size_t)j * (size_t)r + (size_t)c];
+                v[c] = s;
+            }
+            for (int32_t n = 0; n < h_out; ++n) {
+                double s = 0.0;
+                for (int32_t c = 0; c < r; ++c)
+                    s += v[c] * Bk[(size_t)c * (size_t)h_out + (size_t)n];
+                yt[n] += scale * s;
+            }
+        }
+    }
+    free(v);
+    return 0;
+}
+
+/* Checks a segment table the way the library's validation entry point documents it.
+ * Returns an OR of the ORACLE_BAD_* bits (0 = valid). */
+int32_t oracle_validate(const int32_t *seg_starts, const int32_t *seg_adapter,
+                        int32_t num_segments, int32_t num_adapters, int32_t M)
+{
+    int32_t bits = 0;
+    if (num_segments < 0) return ORACLE_BAD_ORDER;
+    if (seg_starts[0] < 0) bits |= ORACLE_BAD_FIRST;
+    if (seg_starts[num_segments] > M) bits |= ORACLE_BAD_LAST;
+    for (int32_t i = 0; i < num_segments; ++i) {
+        if (seg_starts[i + 1] < seg_starts[i]) bits |= ORACLE_BAD_ORDER;
+        if (seg_adapter[i] >= num_adapters) bits |= ORACLE_BAD_ADAPTER;
+    }
+    return bits;
+}
