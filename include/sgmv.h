@@ -1,0 +1,174 @@
+/*
+ * sgmv.h -- C ABI of the GB300 (sm_103a) segmented-gather LoRA library (libsgmv_gb300.so).
+ *
+ * The operation ("Punica Guide: Multi-Tenant LoRA Serving with SGMV", section "The
+ * Heterogeneous Batching Bottleneck: Why Standard Serving Stalls", equation
+ *     y_i = x_i W0 + (alpha/r) x_i A_{k(i)} B_{k(i)};
+ * section "The SGMV Mathematical Formulation": tokens grouped into contiguous segments
+ * [s_i, s_{i+1}), each bound to one adapter through an array of weight pointers; section
+ * "Mathematical Modeling: Throughput Scaling and Kernel Launch Bounds", part 2: one launch for
+ * all A projections ("shrink") and one for all B projections ("expand") per layer):
+ *
+ *   for each segment i in [0, num_segments), k = seg_adapter[i], rows t in
+ *   [seg_starts[i], seg_starts[i+1]):
+ *       v[t]  = x[t] . A_k[layer_idx]                  (shrink, h_in -> r)
+ *       y[t] += scale * v[t] . B_k[layer_idx]          (expand, r -> h_out)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every pointer argument except the host pointer of sgmv_get_error() is DEVICE
+ *   memory owned by the caller, on the current CUDA device: the pointer arrays A_ptrs/B_ptrs
+ *   themselves, the segment table and all tensors.  The library allocates nothing per call
+ *   and keeps no reference after the call is enqueued.
+ * Layout.  Row-major, contiguous.
+ *   x   [M][h_in]            activations (M >= seg_starts[num_segments]).
+ *   y   [M][h_out]           holds the base output x W0 on entry; the LoRA term is added.
+ *   v   [M][r]  fp32         shrink output / expand input.
+ *   A_ptrs[k] -> adapter k's block [L][h_in][r];   layer l starts at element l*h_in*r.
+ *   B_ptrs[k] -> adapter k's block [L][r][h_out];  layer l starts at element l*r*h_out.
+ *   seg_starts [num_segments+1] int32, non-decreasing; seg_adapter [num_segments] int32.
+ *   x, y, A and B share one element type (dtype); accumulation is fp32 throughout and y is
+ *   rounded (to nearest even) once, at the store.
+ * Segments.  Rows outside [seg_starts[0], seg_starts[num_segments]) are never read or
+ *   written.  A segment with seg_starts[i+1] <= seg_starts[i] is empty.  A negative adapter
+ *   id means "no adapter": those rows are left unchanged (shrink leaves their v untouched).
+ *   Several segments may use the same adapter; its weights are then streamed once for all of
+ *   them.  A row must not belong to two segments.
+ * Alignment.  x, y, v, every A_ptrs[k]/B_ptrs[k] block and the pointer arrays must be 16-byte
+ *   aligned; h_in and h_out must be multiples of 8; r must be 8, 16, 32 or 64.
+ * Asynchrony.  Work is enqueued on `stream` and the call returns without synchronising, so it
+ *   can be captured into a CUDA graph (after one uncaptured call with the same dtype/rank on
+ *   the device, which sets the kernels' attributes).  Calls on one stream are ordered; calls
+ *   on different streams that write the same rows race.
+ * Errors.  Host-checkable violations return a negative status and enqueue nothing.  Defects
+ *   that only the device can see (decreasing offsets, an adapter id past the pool) are not
+ *   checked on the fast path: run sgmv_validate() on untrusted tables.  Every device-side wait
+ *   is bounded; a wait that runs out sets the library's device error word, which
+ *   sgmv_get_error() reads (SGMV_ETIMEOUT), and the kernel returns without hanging.
+ */
+#ifndef SGMV_GB300_H
+#define SGMV_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; 0 is the legacy default stream. */
+typedef struct CUstream_st *sgmv_stream_t;
+
+typedef enum {
+    SGMV_F32 = 0,   /* float32                     */
+    SGMV_F16 = 1,   /* IEEE binary16               */
+    SGMV_BF16 = 2   /* bfloat16                    */
+} sgmv_dtype_t;
+
+typedef enum {
+    SGMV_OK = 0,
+    SGMV_EINVAL = -1,        /* null pointer, negative size, bad enum                       */
+    SGMV_EALIGN = -2,        /* pointer not 16-byte aligned, h_in/h_out not multiples of 8  */
+    SGMV_EUNSUPPORTED = -3,  /* rank not in {8,16,32,64}, sizes past the documented limits  */
+    SGMV_ECUDA = -4,         /* a CUDA runtime call or launch failed                        */
+    SGMV_ETIMEOUT = -5       /* a bounded device-side wait ran out (see sgmv_get_error)     */
+} sgmv_status_t;
+
+/* Largest num_segments one call accepts (the segment table is staged on chip). */
+#define SGMV_MAX_SEGMENTS 4096
+/* Largest h_in and h_out one call accepts. */
+#define SGMV_MAX_HIDDEN 65536
+
+/*
+ * lora_apply -- the fused path: y[t] += scale * (x[t] . A_k) . B_k for every segment row.
+ * Source: the y_i equation above (with scale = alpha/r) and the SGMV segment formulation; the
+ * fusion keeps the r-wide intermediate on chip, so one launch replaces the two per layer of
+ * section "Mathematical Modeling ...", part 2.
+ *   y            in/out  [M][h_out], dtype
+ *   x            in      [M][h_in],  dtype
+ *   A_ptrs       in      [num_adapters] device pointers to [L][h_in][r] blocks, dtype
+ *   B_ptrs       in      [num_adapters] device pointers to [L][r][h_out] blocks, dtype
+ *   seg_starts   in      [num_segments+1] int32
+ *   seg_adapter  in      [num_segments] int32 (negative: no adapter)
+ *   num_segments         0 <= num_segments <= SGMV_MAX_SEGMENTS (0: returns SGMV_OK, no-op)
+ *   layer_idx            >= 0, selects the layer inside each adapter block
+ *   h_in, h_out          multiples of 8, <= SGMV_MAX_HIDDEN
+ *   r                    8, 16, 32 or 64
+ *   scale                alpha / r, applied in fp32 to the intermediate before the expand
+ *   dtype                element type of x, y, A and B
+ *   stream               CUDA stream the work is enqueued on
+ * Returns SGMV_OK or a negative sgmv_status_t (nothing enqueued on a negative status other
+ * than SGMV_ECUDA from the launch itself).
+ */
+int lora_apply(void *y, const void *x, const void *const *A_ptrs, const void *const *B_ptrs,
+               const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,
+               int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
+               sgmv_dtype_t dtype, sgmv_stream_t stream);
+
+/*
+ * sgmv_shrink -- v[t] = x[t] . A_k for every segment row (overwrites those rows of v; other
+ * rows of v are not written).  Source: the first factor x_i A_{k(i)} of the y_i equation and
+ * the "one launch for all A projections" of section "Mathematical Modeling ...", part 2.
+ *   v      out  [M][r] float32
+ *   x      in   [M][h_in] dtype;  A_ptrs, seg_starts, seg_adapter, num_segments, layer_idx,
+ *   h_in, r, dtype, stream: as for lora_apply.
+ */
+int sgmv_shrink(float *v, const void *x, const void *const *A_ptrs, const int32_t *seg_starts,
+                const int32_t *seg_adapter, int32_t num_segments, int32_t layer_idx,
+                int32_t h_in, int32_t r, sgmv_dtype_t dtype, sgmv_stream_t stream);
+
+/*
+ * sgmv_expand -- y[t] += scale * v[t] . B_k for every segment row.  Source: the second factor
+ * (x_i A_k) B_k of the y_i equation, times alpha/r, and the "one launch for all B projections"
+ * of section "Mathematical Modeling ...", part 2.
+ *   y      in/out [M][h_out] dtype
+ *   v      in     [M][r] float32 (as written by sgmv_shrink)
+ *   B_ptrs, seg_starts, seg_adapter, num_segments, layer_idx, r, h_out, scale, dtype, stream:
+ *   as for lora_apply.
+ */
+int sgmv_expand(void *y, const float *v, const void *const *B_ptrs, const int32_t *seg_starts,
+                const int32_t *seg_adapter, int32_t num_segments, int32_t layer_idx, int32_t r,
+                int32_t h_out, float scale, sgmv_dtype_t dtype, sgmv_stream_t stream);
+
+/*
+ * sgmv_validate -- checks a segment table on the device and writes an OR of these bits to
+ * *d_err (device int32, overwritten; 0 = valid):
+ *   1  seg_starts decreases somewhere          2  seg_starts[0] < 0
+ *   4  seg_starts[num_segments] > M            8  an adapter id >= num_adapters
+ * Negative adapter ids are valid (no adapter).  The pages describe no such check; it is the
+ * debugging counterpart of the fast path, which trusts the table.
+ *   seg_starts, seg_adapter  in   device table as for lora_apply
+ *   num_segments             >= 0 (any size)
+ *   num_adapters             size of the pointer arrays the table will be used with
+ *   M                        rows of x and y
+ *   d_err                    out  device int32
+ */
+int sgmv_validate(const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,
+                  int32_t num_adapters, int32_t M, int32_t *d_err, sgmv_stream_t stream);
+
+/*
+ * sgmv_get_error -- synchronises `stream`, copies the current device's library error word to
+ * *host_err (a host int32: 0 or a negative sgmv_status_t such as SGMV_ETIMEOUT) and, when
+ * clear != 0, resets it to 0.  Returns SGMV_OK or SGMV_ECUDA.
+ */
+int sgmv_get_error(int32_t *host_err, int32_t clear, sgmv_stream_t stream);
+
+/*
+ * sgmv_set_wait_limit -- sets the bound, in nanoseconds, of every device-side wait of later
+ * launches on the current device (default 2e9 = 2 s; 0 restores the default).  With
+ * inject_stall != 0 the next launches also wait once on a barrier that nothing completes, so
+ * that the bound runs out: a fault-free way to exercise the timeout path.  Test hook; the
+ * pages describe no counterpart.  Returns SGMV_OK or SGMV_ECUDA.
+ */
+int sgmv_set_wait_limit(uint64_t limit_ns, int32_t inject_stall);
+
+/* Human-readable name of a status code (static string). */
+const char *sgmv_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int sgmv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGMV_GB300_H */

@@ -1,0 +1,188 @@
+"""ctypes binding of libsgmv_gb300.so -- argument marshalling only.
+
+Every function here has the name of a C entry point in include/sgmv.h, takes torch CUDA tensors
+(PyTorch provides device memory and streams, nothing else), extracts pointers and sizes and
+calls the library.  No step of the computation runs in Python, and there is no fallback: a
+missing library, a CPU tensor or a failing status raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+SGMV_OK, SGMV_EINVAL, SGMV_EALIGN, SGMV_EUNSUPPORTED, SGMV_ECUDA, SGMV_ETIMEOUT = 0, -1, -2, -3, -4, -5
+SGMV_MAX_SEGMENTS = 4096
+SGMV_MAX_HIDDEN = 65536
+SYMBOLS = ("lora_apply", "sgmv_shrink", "sgmv_expand", "sgmv_validate", "sgmv_get_error",
+           "sgmv_set_wait_limit", "sgmv_status_string", "sgmv_version")
+
+
+class SgmvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def lib(build_if_stale: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the shared library and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if build_if_stale and _build.is_stale():
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing; build it with "
+                               "`python -m segmented_gather_gemm_sgmv_gb300.build`")
+        L = ctypes.CDLL(path)
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+        L.lora_apply.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, ctypes.c_int,
+                                 vp]
+        L.sgmv_shrink.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp]
+        L.sgmv_expand.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, ctypes.c_int, vp]
+        L.sgmv_validate.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+        L.sgmv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
+        L.sgmv_set_wait_limit.argtypes = [ctypes.c_uint64, i32]
+        L.sgmv_status_string.argtypes = [ctypes.c_int]
+        L.sgmv_status_string.restype = ctypes.c_char_p
+        L.sgmv_version.argtypes = []
+        for name in ("lora_apply", "sgmv_shrink", "sgmv_expand", "sgmv_validate",
+                     "sgmv_get_error", "sgmv_set_wait_limit", "sgmv_version"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().sgmv_status_string(int(status)).decode()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def _cuda(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _table(seg_starts, seg_adapter):
+    import torch
+    _cuda(seg_starts, "seg_starts")
+    _cuda(seg_adapter, "seg_adapter")
+    if seg_starts.dtype != torch.int32 or seg_adapter.dtype != torch.int32:
+        raise TypeError("seg_starts and seg_adapter must be int32")
+    S = seg_adapter.numel()
+    if seg_starts.numel() != S + 1:
+        raise ValueError("seg_starts must hold num_segments + 1 offsets")
+    return S
+
+
+def _ptrs(t, name):
+    import torch
+    _cuda(t, name)
+    if t.dtype != torch.int64:
+        raise TypeError(f"{name} must be an int64 tensor of device addresses")
+    return t.data_ptr()
+
+
+def _check(rc: int, where: str):
+    if rc != SGMV_OK:
+        raise SgmvError(rc, where)
+
+
+def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None):
+    """y[t] += scale * (x[t] A_k) B_k for every segment row (in place on y)."""
+    _cuda(y, "y"), _cuda(x, "x")
+    if x.dtype != y.dtype or x.dim() != 2 or y.dim() != 2 or x.shape[0] != y.shape[0]:
+        raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
+    S = _table(seg_starts, seg_adapter)
+    rc = lib().lora_apply(y.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"),
+                          _ptrs(B_ptrs, "B_ptrs"), seg_starts.data_ptr(), seg_adapter.data_ptr(),
+                          S, int(layer_idx), x.shape[1], y.shape[1], int(r), float(scale),
+                          _dtype_code(x), _stream(stream, x.device))
+    _check(rc, "lora_apply")
+    return y
+
+
+def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None):
+    """v[t] = x[t] A_k (fp32) for every segment row."""
+    import torch
+    _cuda(v, "v"), _cuda(x, "x")
+    if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != x.shape[0]:
+        raise ValueError("v must be float32 [M, r]")
+    S = _table(seg_starts, seg_adapter)
+    rc = lib().sgmv_shrink(v.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"),
+                           seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx),
+                           x.shape[1], int(r), _dtype_code(x), _stream(stream, x.device))
+    _check(rc, "sgmv_shrink")
+    return v
+
+
+def sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None):
+    """y[t] += scale * v[t] B_k for every segment row (in place on y)."""
+    import torch
+    _cuda(y, "y"), _cuda(v, "v")
+    if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != y.shape[0]:
+        raise ValueError("v must be float32 [M, r]")
+    S = _table(seg_starts, seg_adapter)
+    rc = lib().sgmv_expand(y.data_ptr(), v.data_ptr(), _ptrs(B_ptrs, "B_ptrs"),
+                           seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx),
+                           int(r), y.shape[1], float(scale), _dtype_code(y),
+                           _stream(stream, y.device))
+    _check(rc, "sgmv_expand")
+    return y
+
+
+def sgmv_validate(seg_starts, seg_adapter, num_adapters, M, d_err, stream=None):
+    """Writes the table-check bits into the device int32 tensor d_err (see include/sgmv.h)."""
+    import torch
+    S = _table(seg_starts, seg_adapter)
+    _cuda(d_err, "d_err")
+    if d_err.dtype != torch.int32 or d_err.numel() < 1:
+        raise TypeError("d_err must be a device int32 tensor")
+    rc = lib().sgmv_validate(seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(num_adapters),
+                             int(M), d_err.data_ptr(), _stream(stream, seg_starts.device))
+    _check(rc, "sgmv_validate")
+    return d_err
+
+
+def sgmv_get_error(clear: bool = True, stream=None, device=None) -> int:
+    """Synchronises and returns the library's device error word (0 or SGMV_ETIMEOUT)."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    out = ctypes.c_int32(0)
+    _check(lib().sgmv_get_error(ctypes.byref(out), 1 if clear else 0, _stream(stream, dev)),
+           "sgmv_get_error")
+    return int(out.value)
+
+
+def sgmv_set_wait_limit(limit_ns: int, inject_stall: bool = False):
+    """Bound of every device-side wait (0: default 2 s); inject_stall forces one to run out."""
+    _check(lib().sgmv_set_wait_limit(int(limit_ns), 1 if inject_stall else 0),
+           "sgmv_set_wait_limit")
+
+
+def sgmv_version() -> int:
+    return int(lib().sgmv_version())

@@ -1,0 +1,414 @@
+// sgmv_abi.cu -- the C ABI declared in include/sgmv.h: argument checks, launch geometry,
+// kernel attributes, the table-validation kernel and the library's device error word.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "sgmv.h"
+#include "sgmv_core.cuh"
+#include "sgmv_launch.h"
+
+namespace {
+
+// Written by kernels whose bounded wait ran out (SGMV_ETIMEOUT); read by sgmv_get_error.
+__device__ int g_sgmv_error = 0;
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kMaxSmem = 232448;  // 227 KB per CTA on sm_103a
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+struct KernelCache {
+  const void* fn = nullptr;
+  size_t smem_set = 0;
+  int cluster = 0;
+  size_t smem_q = 0;
+  int max_clusters = 0;
+};
+
+struct DeviceState {
+  bool init = false;
+  int sms = 0;
+  int* err = nullptr;
+  uint64_t wait_ns = kDefaultWaitNs;
+  int inject = 0;
+  KernelCache cache[3][3][4];  // dtype, mode, rank index
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+struct Tuning {
+  int cluster = 0;  // 0: automatic
+  int stages = 4;
+  int stage_kb = 16;
+};
+
+Tuning read_tuning() {
+  Tuning t;
+  if (const char* s = std::getenv("SGMV_CLUSTER")) t.cluster = std::atoi(s);
+  if (const char* s = std::getenv("SGMV_STAGES")) t.stages = std::max(2, std::atoi(s));
+  if (const char* s = std::getenv("SGMV_STAGE_KB")) t.stage_kb = std::max(4, std::atoi(s));
+  return t;
+}
+const Tuning& tuning() {
+  static const Tuning t = read_tuning();
+  return t;
+}
+
+int rank_index(int r) {
+  switch (r) {
+    case 8: return 0;
+    case 16: return 1;
+    case 32: return 2;
+    case 64: return 3;
+    default: return -1;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SGMV_ECUDA;
+  DeviceState& st = g_dev[dev];
+  if (!st.init) {
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SGMV_ECUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sgmv_error) != cudaSuccess) return SGMV_ECUDA;
+    st.err = static_cast<int*>(p);
+    st.init = true;
+  }
+  *out = &st;
+  return SGMV_OK;
+}
+
+const void* kernel_for(int dtype, int mode, int r) {
+  switch (dtype) {
+    case SGMV_F32: return sgmv::kernel_f32(mode, r);
+    case SGMV_F16: return sgmv::kernel_f16(mode, r);
+    case SGMV_BF16: return sgmv::kernel_bf16(mode, r);
+    default: return nullptr;
+  }
+}
+
+struct Problem {
+  int mode;
+  int dtype;
+  int r;
+  int S;
+  int layer;
+  int h_in;
+  int h_out;
+  float scale;
+};
+
+// Lays out shared memory and fills the geometry part of the kernel parameters.
+int plan_geometry(const Problem& pb, sgmv::Params& p, size_t* smem_out) {
+  const Tuning& tu = tuning();
+  const int eb = pb.dtype == SGMV_F32 ? 4 : 2;
+  const int vec = 16 / eb;
+  int C = tu.cluster > 0 ? tu.cluster : 4;
+  C = std::min(std::max(C, 1), 16);
+  const int rmax = 8;
+  const int stage_bytes = tu.stage_kb * 1024;
+  const int nst = tu.stages;
+  const int units_in = pb.h_in / 8, units_out = pb.h_out / 8;
+  const int kc_max = (pb.mode == sgmv::kExpand) ? 0 : ((units_in + C - 1) / C) * 8;
+  const int nc_max = (pb.mode == sgmv::kShrink) ? 0 : ((units_out + C - 1) / C) * 8;
+  const int wmax = sgmv::kConsumers * vec;
+  if (stage_bytes < pb.r * eb) return SGMV_EUNSUPPORTED;
+  if (nc_max > 0 && stage_bytes < std::min(wmax, nc_max) * eb + 16) return SGMV_EUNSUPPORTED;
+  int hs = 64;  // hash slots: power of two, load factor <= 2/3
+  while (hs < pb.S + pb.S / 2 + 2) hs <<= 1;
+
+  size_t off = 0;
+  p.off_bars = static_cast<uint32_t>(off);
+  off += up(8 * (2 * nst + sgmv::kNumFixedBars), 16);
+  p.off_ctl = static_cast<uint32_t>(off);
+  off += 64;
+  p.desc_ints = static_cast<int32_t>(up(2 + rmax, 4));
+  p.off_desc = static_cast<uint32_t>(off);
+  off += 2 * 4 * p.desc_ints;
+  p.off_tab = static_cast<uint32_t>(off);
+  off += up(4 * (3 * static_cast<size_t>(pb.S) + 2), 16);
+  p.off_vpart = static_cast<uint32_t>(off);
+  off += 2 * 4 * rmax * pb.r;
+  p.off_vfull = static_cast<uint32_t>(off);
+  off += 4 * rmax * pb.r;
+  p.off_red = static_cast<uint32_t>(off);
+  off += 4 * sgmv::kConsumerWarps * rmax * pb.r;
+  const size_t xs_row = up(std::max<size_t>(static_cast<size_t>(kc_max) * eb,
+                                            pb.mode == sgmv::kExpand ? 4u * pb.r : 0u),
+                           16);
+  const size_t ys_row = up(static_cast<size_t>(nc_max) * eb, 16);
+  p.off_xs = static_cast<uint32_t>(up(off, 128));
+  off = p.off_xs + rmax * xs_row;
+  p.off_ys = static_cast<uint32_t>(up(off, 128));
+  off = p.off_ys + rmax * ys_row;
+  p.off_ring = static_cast<uint32_t>(up(off, 1024));
+  const size_t ring = std::max<size_t>(static_cast<size_t>(nst) * stage_bytes,
+                                       4 * (static_cast<size_t>(pb.S) + 3 * hs));
+  off = p.off_ring + ring;
+  if (off > kMaxSmem) return SGMV_EUNSUPPORTED;
+
+  p.C = C;
+  p.nstages = nst;
+  p.stage_bytes = stage_bytes;
+  p.rmax = rmax;
+  p.kc_max = kc_max;
+  p.nc_max = nc_max;
+  p.wmax = wmax;
+  p.hash_slots = hs;
+  p.xs_row_bytes = static_cast<uint32_t>(xs_row);
+  p.ys_row_bytes = static_cast<uint32_t>(ys_row);
+  *smem_out = off;
+  return SGMV_OK;
+}
+
+int launch(const Problem& pb, sgmv::Params& p, cudaStream_t stream) {
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != SGMV_OK) return rc;
+  size_t smem = 0;
+  rc = plan_geometry(pb, p, &smem);
+  if (rc != SGMV_OK) return rc;
+  p.err = st->err;
+  p.S = pb.S;
+  p.layer = pb.layer;
+  p.h_in = pb.h_in;
+  p.h_out = pb.h_out;
+  p.scale = pb.scale;
+  p.wait_limit_ns = st->wait_ns;
+  p.inject_stall = st->inject;
+
+  const void* fn = kernel_for(pb.dtype, pb.mode, pb.r);
+  if (!fn) return SGMV_EUNSUPPORTED;
+  const bool clustered = pb.mode != sgmv::kExpand;
+  int grid = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    KernelCache& kc = st->cache[pb.dtype][pb.mode][rank_index(pb.r)];
+    if (kc.smem_set < smem) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem)) != cudaSuccess)
+        return SGMV_ECUDA;
+      if (clustered && p.C > 8 &&
+          cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+              cudaSuccess)
+        return SGMV_ECUDA;
+      kc.smem_set = smem;
+    }
+    if (kc.cluster != p.C || kc.smem_q != smem) {
+      int n = 0;
+      if (clustered) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(static_cast<unsigned>(p.C * st->sms), 1, 1);
+        cfg.blockDim = dim3(sgmv::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) return SGMV_ECUDA;
+      } else {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, sgmv::kThreads, smem) !=
+            cudaSuccess)
+          return SGMV_ECUDA;
+        n = per_sm * st->sms / p.C;
+      }
+      if (n <= 0) return SGMV_EUNSUPPORTED;
+      kc.cluster = p.C;
+      kc.smem_q = smem;
+      kc.max_clusters = n;
+    }
+    grid = kc.max_clusters * p.C;
+  }
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(sgmv::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  if (clustered) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[] = {&p};
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SGMV_ECUDA;
+  return SGMV_OK;
+}
+
+int check_common(int num_segments, const void* seg_starts, const void* seg_adapter,
+                 int layer_idx, int r, int dtype) {
+  if (num_segments < 0 || layer_idx < 0) return SGMV_EINVAL;
+  if (dtype != SGMV_F32 && dtype != SGMV_F16 && dtype != SGMV_BF16) return SGMV_EINVAL;
+  if (!seg_starts || !seg_adapter) return SGMV_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(seg_starts) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seg_adapter) & 3u))
+    return SGMV_EALIGN;
+  if (rank_index(r) < 0) return SGMV_EUNSUPPORTED;
+  if (num_segments > SGMV_MAX_SEGMENTS) return SGMV_EUNSUPPORTED;
+  return SGMV_OK;
+}
+
+int check_hidden(int h) {
+  if (h <= 0) return SGMV_EINVAL;
+  if (h > SGMV_MAX_HIDDEN) return SGMV_EUNSUPPORTED;
+  if (h % 8) return SGMV_EALIGN;
+  return SGMV_OK;
+}
+
+// Checks table entries on the device; see sgmv_validate in include/sgmv.h.
+__global__ void validate_kernel(const int32_t* ss, const int32_t* sa, int S, int num_adapters,
+                                int M, int32_t* err) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  int bits = 0;
+  if (i == 0) {
+    if (ss[0] < 0) bits |= 2;
+    if (ss[S] > M) bits |= 4;
+  }
+  if (i < S) {
+    if (ss[i + 1] < ss[i]) bits |= 1;
+    if (sa[i] >= num_adapters) bits |= 8;
+  }
+  if (bits) atomicOr(err, bits);
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_apply(void* y, const void* x, const void* const* A_ptrs, const void* const* B_ptrs,
+               const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
+               int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
+               sgmv_dtype_t dtype, sgmv_stream_t stream) {
+  int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
+  if (rc != SGMV_OK) return rc;
+  if (!y || !x || !A_ptrs || !B_ptrs) return SGMV_EINVAL;
+  if ((rc = check_hidden(h_in)) != SGMV_OK || (rc = check_hidden(h_out)) != SGMV_OK) return rc;
+  if (!aligned16(y) || !aligned16(x) || (reinterpret_cast<uintptr_t>(A_ptrs) & 7u) ||
+      (reinterpret_cast<uintptr_t>(B_ptrs) & 7u))
+    return SGMV_EALIGN;
+  if (num_segments == 0) return SGMV_OK;
+  sgmv::Params p = {};
+  p.y = y;
+  p.x = x;
+  p.A_ptrs = A_ptrs;
+  p.B_ptrs = B_ptrs;
+  p.seg_starts = seg_starts;
+  p.seg_adapter = seg_adapter;
+  const Problem pb{sgmv::kFused, dtype, r, num_segments, layer_idx, h_in, h_out, scale};
+  return launch(pb, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgmv_shrink(float* v, const void* x, const void* const* A_ptrs, const int32_t* seg_starts,
+                const int32_t* seg_adapter, int32_t num_segments, int32_t layer_idx,
+                int32_t h_in, int32_t r, sgmv_dtype_t dtype, sgmv_stream_t stream) {
+  int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
+  if (rc != SGMV_OK) return rc;
+  if (!v || !x || !A_ptrs) return SGMV_EINVAL;
+  if ((rc = check_hidden(h_in)) != SGMV_OK) return rc;
+  if (!aligned16(v) || !aligned16(x) || (reinterpret_cast<uintptr_t>(A_ptrs) & 7u))
+    return SGMV_EALIGN;
+  if (num_segments == 0) return SGMV_OK;
+  sgmv::Params p = {};
+  p.x = x;
+  p.v_out = v;
+  p.A_ptrs = A_ptrs;
+  p.seg_starts = seg_starts;
+  p.seg_adapter = seg_adapter;
+  const Problem pb{sgmv::kShrink, dtype, r, num_segments, layer_idx, h_in, 8, 1.0f};
+  return launch(pb, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgmv_expand(void* y, const float* v, const void* const* B_ptrs, const int32_t* seg_starts,
+                const int32_t* seg_adapter, int32_t num_segments, int32_t layer_idx, int32_t r,
+                int32_t h_out, float scale, sgmv_dtype_t dtype, sgmv_stream_t stream) {
+  int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
+  if (rc != SGMV_OK) return rc;
+  if (!y || !v || !B_ptrs) return SGMV_EINVAL;
+  if ((rc = check_hidden(h_out)) != SGMV_OK) return rc;
+  if (!aligned16(y) || !aligned16(v) || (reinterpret_cast<uintptr_t>(B_ptrs) & 7u))
+    return SGMV_EALIGN;
+  if (num_segments == 0) return SGMV_OK;
+  sgmv::Params p = {};
+  p.y = y;
+  p.v_in = v;
+  p.B_ptrs = B_ptrs;
+  p.seg_starts = seg_starts;
+  p.seg_adapter = seg_adapter;
+  const Problem pb{sgmv::kExpand, dtype, r, num_segments, layer_idx, 8, h_out, scale};
+  return launch(pb, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgmv_validate(const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
+                  int32_t num_adapters, int32_t M, int32_t* d_err, sgmv_stream_t stream) {
+  if (num_segments < 0 || !seg_starts || !d_err || (num_segments > 0 && !seg_adapter))
+    return SGMV_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(d_err, 0, sizeof(int32_t), s) != cudaSuccess) return SGMV_ECUDA;
+  const int threads = 256;
+  const int blocks = std::max(1, (num_segments + threads - 1) / threads);
+  validate_kernel<<<blocks, threads, 0, s>>>(seg_starts, seg_adapter, num_segments, num_adapters,
+                                             M, d_err);
+  return cudaGetLastError() == cudaSuccess ? SGMV_OK : SGMV_ECUDA;
+}
+
+int sgmv_get_error(int32_t* host_err, int32_t clear, sgmv_stream_t stream) {
+  if (!host_err) return SGMV_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_sgmv_error, sizeof(int), 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return SGMV_ECUDA;
+  *host_err = v;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_sgmv_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return SGMV_ECUDA;
+  }
+  return SGMV_OK;
+}
+
+int sgmv_set_wait_limit(uint64_t limit_ns, int32_t inject_stall) {
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != SGMV_OK) return rc;
+  st->wait_ns = limit_ns ? limit_ns : kDefaultWaitNs;
+  st->inject = inject_stall ? 1 : 0;
+  return SGMV_OK;
+}
+
+const char* sgmv_status_string(int status) {
+  switch (status) {
+    case SGMV_OK: return "SGMV_OK";
+    case SGMV_EINVAL: return "SGMV_EINVAL: invalid argument";
+    case SGMV_EALIGN: return "SGMV_EALIGN: misaligned pointer or size";
+    case SGMV_EUNSUPPORTED: return "SGMV_EUNSUPPORTED: rank or size outside the supported range";
+    case SGMV_ECUDA: return "SGMV_ECUDA: CUDA runtime error";
+    case SGMV_ETIMEOUT: return "SGMV_ETIMEOUT: a device-side wait ran out";
+    default: return "unknown status";
+  }
+}
+
+int sgmv_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,14 @@
+// sgmv_launch.h -- host-side glue between the C ABI (sgmv_abi.cu) and the per-dtype kernel
+// instantiations (sgmv_inst_*.cu).
+#pragma once
+#include <cstdint>
+
+namespace sgmv {
+
+// Returns the __global__ function for (mode, rank) of one element type, or nullptr when the
+// rank is not instantiated.  mode: 0 fused, 1 shrink, 2 expand.
+const void* kernel_f32(int mode, int r);
+const void* kernel_f16(int mode, int r);
+const void* kernel_bf16(int mode, int r);
+
+}  // namespace sgmv

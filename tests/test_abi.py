@@ -1,0 +1,94 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every entry point that
+include/sgmv.h declares, and its host-side argument checks return the documented statuses
+before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from segmented_gather_gemm_sgmv_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sgmv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char \*)\s*\**\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    return binding.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert set(binding.SYMBOLS) <= set(names), names
+    for name in names:
+        assert hasattr(L, name), f"{name} declared in sgmv.h but not exported"
+
+
+def test_header_constants_match_binding():
+    text = open(HEADER).read()
+    assert f"#define SGMV_MAX_SEGMENTS {binding.SGMV_MAX_SEGMENTS}" in text
+    assert f"#define SGMV_MAX_HIDDEN {binding.SGMV_MAX_HIDDEN}" in text
+    for name, val in [("SGMV_EINVAL", -1), ("SGMV_EALIGN", -2), ("SGMV_EUNSUPPORTED", -3),
+                      ("SGMV_ECUDA", -4), ("SGMV_ETIMEOUT", -5)]:
+        assert re.search(rf"{name}\s*=\s*{val}\b", text), name
+
+
+def test_version_and_strings(L):
+    assert L.sgmv_version() == 100
+    for s in (0, -1, -2, -3, -4, -5):
+        assert binding.status_string(s).startswith("SGMV_")
+
+
+# Fake but aligned device addresses: the host checks never dereference them.
+P = 0x7F0000000000
+OK_ARGS = dict(y=P, x=P + 0x10000, A=P + 0x20000, B=P + 0x30000, ss=P + 0x40000, sa=P + 0x50000,
+               S=4, layer=0, h_in=4096, h_out=4096, r=16, scale=1.0, dt=1)
+
+
+def apply(L, **kw):
+    a = dict(OK_ARGS, **kw)
+    return L.lora_apply(a["y"], a["x"], a["A"], a["B"], a["ss"], a["sa"], a["S"], a["layer"],
+                        a["h_in"], a["h_out"], a["r"], a["scale"], a["dt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(y=None), -1), (dict(x=None), -1), (dict(A=None), -1), (dict(ss=None), -1),
+    (dict(S=-1), -1), (dict(layer=-2), -1), (dict(dt=7), -1), (dict(h_in=0), -1),
+    (dict(y=P + 8), -2), (dict(x=P + 0x10004), -2), (dict(h_in=4100), -2), (dict(h_out=12), -2),
+    (dict(ss=P + 0x40002), -2),
+    (dict(r=12), -3), (dict(r=128), -3), (dict(S=4097), -3), (dict(h_out=65544), -3),
+    (dict(S=0), 0),
+])
+def test_lora_apply_host_checks(L, kw, status):
+    assert apply(L, **kw) == status
+
+
+def test_shrink_expand_validate_host_checks(L):
+    a = OK_ARGS
+    assert L.sgmv_shrink(None, a["x"], a["A"], a["ss"], a["sa"], 4, 0, 4096, 16, 1, None) == -1
+    assert L.sgmv_shrink(a["y"], a["x"], a["A"], a["ss"], a["sa"], 4, 0, 4096, 24, 1, None) == -3
+    assert L.sgmv_shrink(a["y"], a["x"], a["A"], a["ss"], a["sa"], 0, 0, 4096, 16, 1, None) == 0
+    assert L.sgmv_expand(a["y"], None, a["B"], a["ss"], a["sa"], 4, 0, 16, 4096, 1.0, 1,
+                         None) == -1
+    assert L.sgmv_expand(a["y"], a["x"], a["B"], a["ss"], a["sa"], 4, 0, 16, 4090, 1.0, 1,
+                         None) == -2
+    assert L.sgmv_validate(None, a["sa"], 4, 8, 10, a["y"], None) == -1
+    assert L.sgmv_validate(a["ss"], a["sa"], -1, 8, 10, a["y"], None) == -1
+    assert L.sgmv_get_error(None, 0, None) == -1
+
+
+def test_python_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    from segmented_gather_gemm_sgmv_gb300 import lora_apply
+    y = torch.zeros(2, 8, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA"):
+        lora_apply(y, y, torch.zeros(1, dtype=torch.int64), torch.zeros(1, dtype=torch.int64),
+                   torch.zeros(2, dtype=torch.int32), torch.zeros(1, dtype=torch.int32), 0, 16,
+                   1.0)
