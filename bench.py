@@ -217,12 +217,14 @@ def time_graph_steps(torch, setup, K, W, stream, world):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
     e0.record(stream)
     for _ in range(K // per):
         g_full.replay()
     if g_rem is not None:
         g_rem.replay()
     e1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(world)
     return e0.elapsed_time(e1)

@@ -88,7 +88,8 @@ typedef enum {
  *   A_ptrs       in      [num_adapters] device pointers to [L][h_in][r] blocks, dtype
  *   B_ptrs       in      [num_adapters] device pointers to [L][r][h_out] blocks, dtype
  *   seg_starts   in      [num_segments+1] int32
- *   seg_adapter  in      [num_segments] int32 (negative: no adapter)
+ *   seg_adapter  in      [num_segments] int32 (negative: no adapter; may be null when
+ *                        num_segments == 0)
  *   num_segments         0 <= num_segments <= SGMV_MAX_SEGMENTS (0: returns SGMV_OK, no-op)
  *   layer_idx            >= 0, selects the layer inside each adapter block
  *   h_in, h_out          multiples of 8, <= SGMV_MAX_HIDDEN

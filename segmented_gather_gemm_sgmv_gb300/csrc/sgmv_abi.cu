@@ -257,7 +257,7 @@ int check_common(int num_segments, const void* seg_starts, const void* seg_adapt
                  int layer_idx, int r, int dtype) {
   if (num_segments < 0 || layer_idx < 0) return SGMV_EINVAL;
   if (dtype != SGMV_F32 && dtype != SGMV_F16 && dtype != SGMV_BF16) return SGMV_EINVAL;
-  if (!seg_starts || !seg_adapter) return SGMV_EINVAL;
+  if (!seg_starts || (num_segments > 0 && !seg_adapter)) return SGMV_EINVAL;
   if ((reinterpret_cast<uintptr_t>(seg_starts) & 3u) ||
       (reinterpret_cast<uintptr_t>(seg_adapter) & 3u))
     return SGMV_EALIGN;

@@ -64,7 +64,7 @@ def apply(L, **kw):
     (dict(y=P + 8), -2), (dict(x=P + 0x10004), -2), (dict(h_in=4100), -2), (dict(h_out=12), -2),
     (dict(ss=P + 0x40002), -2),
     (dict(r=12), -3), (dict(r=128), -3), (dict(S=4097), -3), (dict(h_out=65544), -3),
-    (dict(S=0), 0),
+    (dict(S=0), 0), (dict(S=0, sa=None), 0), (dict(S=1, sa=None), -1),
 ])
 def test_lora_apply_host_checks(L, kw, status):
     assert apply(L, **kw) == status
