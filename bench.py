@@ -167,9 +167,10 @@ def barrier(world):
 class Setup:
     """Device-resident inputs of the workload: pool, NB rotating x/y sets, segment table."""
 
-    def __init__(self, w, device, nbuf=32, seed=0):
+    def __init__(self, w, device, nbuf=32, seed=0, overlap=True):
         import torch
         self.w = w
+        self.overlap = overlap
         self.ss, self.sa = workloads.make_segments(w.name, seed)
         self.M = int(self.ss[-1])
         self.A, self.B = workloads.make_pool(w, device, seed=seed + 1)
@@ -188,7 +189,8 @@ class Setup:
         from segmented_gather_gemm_sgmv_gb300 import lora_apply
         i = step % self.nbuf
         lora_apply(self.y[i], self.x[i], self.A_ptrs, self.B_ptrs, self.d_ss, self.d_sa,
-                   step % self.w.layers, self.w.r, self.w.scale, stream=stream)
+                   step % self.w.layers, self.w.r, self.w.scale, stream=stream,
+                   overlap_prior=self.overlap)
 
 
 def capture(torch, fn, n, stream):
@@ -210,20 +212,22 @@ def time_graph_steps(torch, setup, K, W, stream, world):
     g_full = capture(torch, lambda s: setup.call(s, stream), per, stream)
     rem = K % per
     g_rem = capture(torch, lambda s: setup.call(s, stream), rem, stream) if rem else None
-    for _ in range(max(1, (W + per - 1) // per)):
-        g_full.replay()
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        for _ in range(max(1, (W + per - 1) // per)):
+            g_full.replay()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.nvtx.range_push("timed")
-    e0.record(stream)
-    for _ in range(K // per):
-        g_full.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K // per):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(world)
@@ -250,7 +254,7 @@ def time_e2e(torch, setup, K, stream):
         ssd.copy_(ssh, non_blocking=True)
         sad.copy_(sah, non_blocking=True)
         lora_apply(yd, xd, setup.A_ptrs, setup.B_ptrs, ssd, sad, s % w.layers, w.r, w.scale,
-                   stream=stream)
+                   stream=stream, overlap_prior=setup.overlap)
         yout.copy_(yd, non_blocking=True)
 
     per = w.layers
@@ -259,14 +263,16 @@ def time_e2e(torch, setup, K, stream):
             step(s)
     torch.cuda.synchronize()
     g = capture(torch, step, per, stream)
-    g.replay()
+    with torch.cuda.stream(stream):
+        g.replay()
     torch.cuda.synchronize()
     reps = max(1, n // per)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        g.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     h2d = xh.numel() * xh.element_size() + yh.numel() * yh.element_size() + 4 * (
@@ -320,6 +326,11 @@ def run_ours(args):
     nbytes, M = algorithmic_bytes(w, setup.ss, setup.sa)
     K, W = args.steps, args.warmup
 
+    # isolated calls (each kernel waits for the previous one to finish): context figure
+    setup.overlap = False
+    ms_iso = time_graph_steps(torch, setup, min(K, 6400), W, stream, world)
+    us_iso = ms_iso * 1e3 / min(K, 6400)
+    setup.overlap = not args.no_overlap
     clocks = ClockSampler(torch.cuda.current_device()).start()
     time.sleep(0.3)
     ms = time_graph_steps(torch, setup, K, W, stream, world)
@@ -351,6 +362,10 @@ def run_ours(args):
         "impl": "ours",
         "tokens_per_s": round(world * M / per, 1),
         "us_per_call": round(per * 1e6, 3),
+        "us_per_call_isolated": round(us_iso, 3),
+        "launch": "lora_apply_ex(SGMV_OVERLAP_PRIOR): each call's weight prefetch overlaps the "
+                  "previous call (programmatic dependent launch)" if setup.overlap else
+                  "lora_apply: each call starts after the previous one completes",
         "config": {"workload": w.name, "h_in": w.h_in, "h_out": w.h_out, "r": w.r,
                    "tokens": M, "segments": int(len(setup.sa)),
                    "distinct_adapters": int(len({int(k) for k in setup.sa})),
@@ -443,6 +458,8 @@ def main():
     ap.add_argument("--workload", default="decode_distinct", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="plain lora_apply launches (no programmatic dependent launch)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

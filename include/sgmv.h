@@ -105,6 +105,28 @@ int lora_apply(void *y, const void *x, const void *const *A_ptrs, const void *co
                int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
                sgmv_dtype_t dtype, sgmv_stream_t stream);
 
+/* Flags of lora_apply_ex. */
+#define SGMV_OVERLAP_PRIOR 1u
+
+/*
+ * lora_apply_ex -- lora_apply with launch flags.
+ *   flags = 0: identical to lora_apply.
+ *   flags = SGMV_OVERLAP_PRIOR: the kernel is launched as a programmatic dependent of the
+ *     kernel enqueued before it on `stream` (CUDA programmatic dependent launch).  It may start,
+ *     read the segment table and the pointer arrays and stream adapter weights while that
+ *     previous kernel is still running; it waits for the previous kernel to complete before it
+ *     reads x or y and before it writes y.  Use it for back-to-back layer calls (for example a
+ *     CUDA graph of a layer sweep): the weight streaming of one call then overlaps the tail of
+ *     the previous one.  Precondition: the immediately preceding kernel on the stream does not
+ *     write the segment table, A_ptrs/B_ptrs or any adapter weights.  The pages describe no
+ *     counterpart; it is launch mechanics for the same operation.
+ * Other arguments, layout and errors: as for lora_apply (SGMV_EINVAL for unknown flags).
+ */
+int lora_apply_ex(void *y, const void *x, const void *const *A_ptrs, const void *const *B_ptrs,
+                  const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,
+                  int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
+                  sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream);
+
 /*
  * sgmv_shrink -- v[t] = x[t] . A_k for every segment row (overwrites those rows of v; other
  * rows of v are not written).  Source: the first factor x_i A_{k(i)} of the y_i equation and

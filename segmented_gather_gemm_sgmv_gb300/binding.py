@@ -19,7 +19,8 @@ _lib = None
 SGMV_OK, SGMV_EINVAL, SGMV_EALIGN, SGMV_EUNSUPPORTED, SGMV_ECUDA, SGMV_ETIMEOUT = 0, -1, -2, -3, -4, -5
 SGMV_MAX_SEGMENTS = 4096
 SGMV_MAX_HIDDEN = 65536
-SYMBOLS = ("lora_apply", "sgmv_shrink", "sgmv_expand", "sgmv_validate", "sgmv_get_error",
+SGMV_OVERLAP_PRIOR = 1
+SYMBOLS = ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_expand", "sgmv_validate", "sgmv_get_error",
            "sgmv_set_wait_limit", "sgmv_status_string", "sgmv_version")
 
 
@@ -45,6 +46,8 @@ def lib(build_if_stale: bool = True) -> ctypes.CDLL:
         vp, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
         L.lora_apply.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, ctypes.c_int,
                                  vp]
+        L.lora_apply_ex.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
+                                    ctypes.c_int, ctypes.c_uint32, vp]
         L.sgmv_shrink.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp]
         L.sgmv_expand.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, ctypes.c_int, vp]
         L.sgmv_validate.argtypes = [vp, vp, i32, i32, i32, vp, vp]
@@ -53,7 +56,7 @@ def lib(build_if_stale: bool = True) -> ctypes.CDLL:
         L.sgmv_status_string.argtypes = [ctypes.c_int]
         L.sgmv_status_string.restype = ctypes.c_char_p
         L.sgmv_version.argtypes = []
-        for name in ("lora_apply", "sgmv_shrink", "sgmv_expand", "sgmv_validate",
+        for name in ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_expand", "sgmv_validate",
                      "sgmv_get_error", "sgmv_set_wait_limit", "sgmv_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -112,17 +115,26 @@ def _check(rc: int, where: str):
         raise SgmvError(rc, where)
 
 
-def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None):
-    """y[t] += scale * (x[t] A_k) B_k for every segment row (in place on y)."""
+def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None,
+               overlap_prior=False):
+    """y[t] += scale * (x[t] A_k) B_k for every segment row (in place on y).
+
+    overlap_prior=True calls lora_apply_ex with SGMV_OVERLAP_PRIOR: the kernel may stream
+    weights while the previous kernel on the stream is still running (see include/sgmv.h).
+    """
     _cuda(y, "y"), _cuda(x, "x")
     if x.dtype != y.dtype or x.dim() != 2 or y.dim() != 2 or x.shape[0] != y.shape[0]:
         raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
     S = _table(seg_starts, seg_adapter)
-    rc = lib().lora_apply(y.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"),
-                          _ptrs(B_ptrs, "B_ptrs"), seg_starts.data_ptr(), seg_adapter.data_ptr(),
-                          S, int(layer_idx), x.shape[1], y.shape[1], int(r), float(scale),
-                          _dtype_code(x), _stream(stream, x.device))
-    _check(rc, "lora_apply")
+    args = (y.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
+            seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1],
+            y.shape[1], int(r), float(scale), _dtype_code(x))
+    if overlap_prior:
+        rc = lib().lora_apply_ex(*args, SGMV_OVERLAP_PRIOR, _stream(stream, x.device))
+        _check(rc, "lora_apply_ex")
+    else:
+        rc = lib().lora_apply(*args, _stream(stream, x.device))
+        _check(rc, "lora_apply")
     return y
 
 

@@ -18,7 +18,9 @@ namespace {
 __device__ int g_sgmv_error = 0;
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kMaxSmem = 232448;  // 227 KB per CTA on sm_103a
+constexpr size_t kPairSmem = 114688;  // 112 KB: two CTAs fit on an SM (228 KB), so the next
+                                      // kernel of the stream can start beside this one
+constexpr size_t kMaxSmem = 232448;   // 227 KB: large segment tables (one CTA per SM)
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 struct KernelCache {
@@ -41,16 +43,18 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
+constexpr int kMaxStages = 16;
+
 struct Tuning {
-  int cluster = 0;  // 0: automatic
-  int stages = 4;
-  int stage_kb = 16;
+  int stages = 0;     // 0: as many as shared memory holds
+  int stage_kb = 16;  // ring stage size
+  int budget_kb = 0;  // 0: 112 KB (two CTAs per SM), else the per-CTA shared-memory budget
 };
 
 Tuning read_tuning() {
   Tuning t;
-  if (const char* s = std::getenv("SGMV_CLUSTER")) t.cluster = std::atoi(s);
-  if (const char* s = std::getenv("SGMV_STAGES")) t.stages = std::max(2, std::atoi(s));
+  if (const char* s = std::getenv("SGMV_SMEM_KB")) t.budget_kb = std::max(0, std::atoi(s));
+  if (const char* s = std::getenv("SGMV_STAGES")) t.stages = std::max(0, std::atoi(s));
   if (const char* s = std::getenv("SGMV_STAGE_KB")) t.stage_kb = std::max(4, std::atoi(s));
   return t;
 }
@@ -108,28 +112,27 @@ struct Problem {
   float scale;
 };
 
-// Lays out shared memory and fills the geometry part of the kernel parameters.
-int plan_geometry(const Problem& pb, sgmv::Params& p, size_t* smem_out) {
+// Lays out shared memory and fills the geometry part of the kernel parameters.  The launch
+// cluster is kMaxGroup CTAs; the kernel itself picks how many of them share an item.
+int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* smem_out) {
   const Tuning& tu = tuning();
   const int eb = pb.dtype == SGMV_F32 ? 4 : 2;
   const int vec = 16 / eb;
-  int C = tu.cluster > 0 ? tu.cluster : 4;
-  C = std::min(std::max(C, 1), 16);
-  const int rmax = 8;
+  const int C = sgmv::kMaxGroup;
+  const int rmax = sgmv::kRowsMax;
   const int stage_bytes = tu.stage_kb * 1024;
-  const int nst = tu.stages;
-  const int units_in = pb.h_in / 8, units_out = pb.h_out / 8;
-  const int kc_max = (pb.mode == sgmv::kExpand) ? 0 : ((units_in + C - 1) / C) * 8;
-  const int nc_max = (pb.mode == sgmv::kShrink) ? 0 : ((units_out + C - 1) / C) * 8;
-  const int wmax = sgmv::kConsumers * vec;
-  if (stage_bytes < pb.r * eb) return SGMV_EUNSUPPORTED;
-  if (nc_max > 0 && stage_bytes < std::min(wmax, nc_max) * eb + 16) return SGMV_EUNSUPPORTED;
+  // A rows per stage, followed by the same rows' columns of up to rmax x rows.
+  const int kb = (stage_bytes / ((pb.r + rmax) * eb)) / 8 * 8;
+  // Expand pass width: one thread per 16 bytes of a B row, and rmax y rows must fit a stage.
+  const int wmax = std::min(sgmv::kConsumers * vec, stage_bytes / (rmax * eb)) / 8 * 8;
+  if (kb < 8 || wmax < 8 || stage_bytes < wmax * eb + 16 || stage_bytes < rmax * pb.r * 4)
+    return SGMV_EUNSUPPORTED;
   int hs = 64;  // hash slots: power of two, load factor <= 2/3
   while (hs < pb.S + pb.S / 2 + 2) hs <<= 1;
 
   size_t off = 0;
   p.off_bars = static_cast<uint32_t>(off);
-  off += up(8 * (2 * nst + sgmv::kNumFixedBars), 16);
+  off += up(8 * (2 * kMaxStages + sgmv::kNumFixedBars), 16);
   p.off_ctl = static_cast<uint32_t>(off);
   off += 64;
   p.desc_ints = static_cast<int32_t>(up(2 + rmax, 4));
@@ -143,40 +146,39 @@ int plan_geometry(const Problem& pb, sgmv::Params& p, size_t* smem_out) {
   off += 4 * rmax * pb.r;
   p.off_red = static_cast<uint32_t>(off);
   off += 4 * sgmv::kConsumerWarps * rmax * pb.r;
-  const size_t xs_row = up(std::max<size_t>(static_cast<size_t>(kc_max) * eb,
-                                            pb.mode == sgmv::kExpand ? 4u * pb.r : 0u),
-                           16);
-  const size_t ys_row = up(static_cast<size_t>(nc_max) * eb, 16);
-  p.off_xs = static_cast<uint32_t>(up(off, 128));
-  off = p.off_xs + rmax * xs_row;
-  p.off_ys = static_cast<uint32_t>(up(off, 128));
-  off = p.off_ys + rmax * ys_row;
   p.off_ring = static_cast<uint32_t>(up(off, 1024));
-  const size_t ring = std::max<size_t>(static_cast<size_t>(nst) * stage_bytes,
-                                       4 * (static_cast<size_t>(pb.S) + 3 * hs));
+  // As many ring stages as the budget holds (the ring also hosts the transient hash table).
+  const size_t scratch = 4 * (static_cast<size_t>(pb.S) + 3 * hs);
+  if (p.off_ring + std::max<size_t>(scratch, 2 * static_cast<size_t>(stage_bytes)) > budget)
+    return SGMV_EUNSUPPORTED;
+  int nst = static_cast<int>((budget - p.off_ring) / stage_bytes);
+  nst = std::min(nst, tu.stages > 0 ? tu.stages : kMaxStages);
+  nst = std::min(std::max(nst, 2), kMaxStages);
+  const size_t ring = std::max<size_t>(static_cast<size_t>(nst) * stage_bytes, scratch);
   off = p.off_ring + ring;
-  if (off > kMaxSmem) return SGMV_EUNSUPPORTED;
+  if (off > budget) return SGMV_EUNSUPPORTED;
 
   p.C = C;
   p.nstages = nst;
   p.stage_bytes = stage_bytes;
   p.rmax = rmax;
-  p.kc_max = kc_max;
-  p.nc_max = nc_max;
+  p.kb = kb;
   p.wmax = wmax;
   p.hash_slots = hs;
-  p.xs_row_bytes = static_cast<uint32_t>(xs_row);
-  p.ys_row_bytes = static_cast<uint32_t>(ys_row);
   *smem_out = off;
   return SGMV_OK;
 }
 
-int launch(const Problem& pb, sgmv::Params& p, cudaStream_t stream) {
+int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stream) {
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc != SGMV_OK) return rc;
   size_t smem = 0;
-  rc = plan_geometry(pb, p, &smem);
+  const size_t budget = tuning().budget_kb > 0
+                            ? std::min<size_t>(kMaxSmem, static_cast<size_t>(tuning().budget_kb) * 1024)
+                            : kPairSmem;
+  rc = plan_geometry(pb, budget, p, &smem);
+  if (rc == SGMV_EUNSUPPORTED) rc = plan_geometry(pb, kMaxSmem, p, &smem);
   if (rc != SGMV_OK) return rc;
   p.err = st->err;
   p.S = pb.S;
@@ -226,6 +228,7 @@ int launch(const Problem& pb, sgmv::Params& p, cudaStream_t stream) {
           return SGMV_ECUDA;
         n = per_sm * st->sms / p.C;
       }
+      n = std::min(n, std::max(1, st->sms / p.C));  // one CTA per SM per kernel
       if (n <= 0) return SGMV_EUNSUPPORTED;
       kc.cluster = p.C;
       kc.smem_q = smem;
@@ -235,19 +238,26 @@ int launch(const Problem& pb, sgmv::Params& p, cudaStream_t stream) {
   }
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(sgmv::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  unsigned na = 0;
   if (clustered) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(p.C);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  if (flags & SGMV_OVERLAP_PRIOR) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   void* args[] = {&p};
   if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SGMV_ECUDA;
   return SGMV_OK;
@@ -297,6 +307,15 @@ int lora_apply(void* y, const void* x, const void* const* A_ptrs, const void* co
                const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
                int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
                sgmv_dtype_t dtype, sgmv_stream_t stream) {
+  return lora_apply_ex(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, num_segments, layer_idx,
+                       h_in, h_out, r, scale, dtype, 0u, stream);
+}
+
+int lora_apply_ex(void* y, const void* x, const void* const* A_ptrs, const void* const* B_ptrs,
+                  const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
+                  int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
+                  sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream) {
+  if (flags & ~static_cast<uint32_t>(SGMV_OVERLAP_PRIOR)) return SGMV_EINVAL;
   int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
   if (rc != SGMV_OK) return rc;
   if (!y || !x || !A_ptrs || !B_ptrs) return SGMV_EINVAL;
@@ -313,7 +332,7 @@ int lora_apply(void* y, const void* x, const void* const* A_ptrs, const void* co
   p.seg_starts = seg_starts;
   p.seg_adapter = seg_adapter;
   const Problem pb{sgmv::kFused, dtype, r, num_segments, layer_idx, h_in, h_out, scale};
-  return launch(pb, p, reinterpret_cast<cudaStream_t>(stream));
+  return launch(pb, p, flags, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int sgmv_shrink(float* v, const void* x, const void* const* A_ptrs, const int32_t* seg_starts,
@@ -333,7 +352,7 @@ int sgmv_shrink(float* v, const void* x, const void* const* A_ptrs, const int32_
   p.seg_starts = seg_starts;
   p.seg_adapter = seg_adapter;
   const Problem pb{sgmv::kShrink, dtype, r, num_segments, layer_idx, h_in, 8, 1.0f};
-  return launch(pb, p, reinterpret_cast<cudaStream_t>(stream));
+  return launch(pb, p, 0u, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int sgmv_expand(void* y, const float* v, const void* const* B_ptrs, const int32_t* seg_starts,
@@ -353,7 +372,7 @@ int sgmv_expand(void* y, const float* v, const void* const* B_ptrs, const int32_
   p.seg_starts = seg_starts;
   p.seg_adapter = seg_adapter;
   const Problem pb{sgmv::kExpand, dtype, r, num_segments, layer_idx, 8, h_out, scale};
-  return launch(pb, p, reinterpret_cast<cudaStream_t>(stream));
+  return launch(pb, p, 0u, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int sgmv_validate(const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,

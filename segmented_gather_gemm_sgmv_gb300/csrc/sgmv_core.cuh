@@ -10,16 +10,22 @@
 //  * Scheduler, in every CTA: the segment table is staged in shared memory and every segment
 //    with an adapter is hashed by adapter id, so that all rows of one adapter -- even rows of
 //    non-adjacent segments -- form one group whose weights are streamed once per call.  A
-//    group is cut into work items of at most `rmax` rows.  All CTAs derive the same item list;
-//    cluster q runs items q, q+G, q+2G, ...  (The pages' "pre-sorted segment descriptors" and
-//    "one threadblock per segment", section "Hardware-Level Optimizations in SGMV".)
-//  * One item runs on one thread-block cluster of C CTAs.  CTA c owns the c-th slice of h_in
-//    (shrink, split-K) and of h_out (expand).  Its weight slices stream through a ring of
-//    shared-memory stages filled by 1-D bulk copies (TMA) that one producer warp issues; the
-//    eight consumer warps compute on the CUDA cores in fp32.
-//  * The r-wide partial products of the C CTAs are summed through distributed shared memory
-//    in a fixed order (deterministic), so the intermediate v never leaves the cluster in the
-//    fused path.
+//    group is cut into work items of at most kRowsMax rows.  All CTAs derive the same item
+//    list.  (The pages' "pre-sorted segment descriptors" and "one threadblock per segment",
+//    section "Hardware-Level Optimizations in SGMV".)
+//  * One item runs on a group of E CTAs (E = 1, 2 or 4, picked in the kernel from the item
+//    count so that every SM has work; a group never spans two clusters).  Member m owns the
+//    m-th slice of h_in (shrink, split-K) and of h_out (expand).
+//  * Everything an item reads streams through one ring of shared-memory stages filled by 1-D
+//    bulk copies (TMA) that one producer warp issues, in the order the consumers use it:
+//    A-row chunks (each carrying the matching columns of the item's x rows), then per expand
+//    pass the B-row chunks and one stage with the item's y rows.  Eight consumer warps compute
+//    in fp32 on the CUDA cores.
+//  * With E > 1 the r-wide partial products are summed through distributed shared memory in a
+//    fixed member order (deterministic), so the intermediate v never leaves the cluster.
+//  * Programmatic dependent launch: a kernel lets the next one start at once; the producer
+//    fills the ring with weights, then waits for the previous kernel before any activation
+//    copy (x, y, v).
 //  * Every wait is bounded (globaltimer); a wait that runs out flags the CTA, sets the
 //    library's device error word and lets the kernel run to its end without touching global
 //    memory again.
@@ -36,12 +42,15 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kStatusTimeout = -5;         // SGMV_ETIMEOUT
+constexpr int kRowsMax = 4;                // rows per CUDA-core work item
 
 enum Mode : int { kFused = 0, kShrink = 1, kExpand = 2 };
 
 // Barrier slots after the 2*nstages ring barriers.
-enum Bar : int { kXFull = 0, kXFree, kYFull, kYFree, kDesc0, kDesc1, kVReady0, kVReady1, kNever,
+enum Bar : int { kDescFull0 = 0, kDescFull1, kDescFree0, kDescFree1, kVReady0, kVReady1, kNever,
                  kNumFixedBars };
+
+constexpr int kMaxGroup = 4;  // largest number of CTAs that share one item (launch cluster size)
 
 struct Params {
   void* y;
@@ -55,16 +64,14 @@ struct Params {
   int* err;  // library device error word
   int32_t S, layer, h_in, h_out;
   float scale;
-  int32_t C;            // CTAs per item (cluster size for shrink / fused)
+  int32_t C;            // launch cluster size (a multiple of every group size used)
   int32_t nstages;      // ring stages
   int32_t stage_bytes;  // bytes per ring stage
   int32_t rmax;         // rows per work item
-  int32_t kc_max, nc_max;  // widest h_in / h_out slice of one CTA (elements)
-  int32_t wmax;            // widest B row segment one expand pass covers (elements)
-  int32_t hash_slots;      // power of two > 1.5*S
-  uint32_t off_bars, off_ctl, off_desc, off_tab, off_vpart, off_vfull, off_red, off_xs, off_ys,
-      off_ring;
-  uint32_t xs_row_bytes, ys_row_bytes;
+  int32_t kb;           // A rows per chunk (the chunk's x columns follow them in the stage)
+  int32_t wmax;         // widest window of B columns one expand pass covers (elements)
+  int32_t hash_slots;   // power of two > 1.5*S
+  uint32_t off_bars, off_ctl, off_desc, off_tab, off_vpart, off_vfull, off_red, off_ring;
   int32_t desc_ints;
   uint64_t wait_limit_ns;
   int32_t inject_stall;
@@ -167,39 +174,93 @@ struct Waiter {
 };
 
 // ---- slices and chunking (identical arithmetic on the producer and consumer sides) -------
-static __device__ __forceinline__ void slice_of(int n, int C, int c, int& lo, int& hi) {
+static __device__ __forceinline__ void slice_of(int n, int parts, int m, int& lo, int& hi) {
   const int units = n >> 3;  // slices start on multiples of 8 elements (16-byte aligned)
-  lo = (units * c / C) << 3;
-  hi = (units * (c + 1) / C) << 3;
+  lo = (units * m / parts) << 3;
+  hi = (units * (m + 1) / parts) << 3;
 }
 
-template <typename T, int R>
+// The stages of one item: [A chunks][pass 0: B chunks, y][pass 1: ...] (fused);
+// [A chunks] (shrink); [v][pass 0: B chunks, y]... (expand).
+enum ChunkKind : int { kChunkA = 0, kChunkB = 1, kChunkY = 2, kChunkV = 3 };
+
+template <typename T, int R, int MODE>
 struct Chunking {
   int kc, nc;     // this CTA's h_in / h_out slice width
-  int kb, nA;     // A rows per chunk, number of A chunks
+  int nA;         // A chunks
+  int kbe;        // A rows per chunk (balanced, <= p.kb, a multiple of 8)
   int passes;     // expand passes
-  __device__ __forceinline__ void init(const Params& p, int kc_, int nc_) {
-    kc = kc_;
-    nc = nc_;
-    kb = p.stage_bytes / (R * (int)sizeof(T));
-    nA = (kc + kb - 1) / kb;
-    passes = (nc + p.wmax - 1) / p.wmax;
+  int total;      // stages per item
+  __device__ __forceinline__ static int row_stride(int w) {  // padded B row in a stage
+    return w * static_cast<int>(sizeof(T)) + 16;
   }
   __device__ __forceinline__ int pass_width(const Params& p, int pass) const {
     return min(p.wmax, nc - pass * p.wmax);
   }
-  __device__ __forceinline__ static int row_stride(int w) {  // padded B row in a stage
-    return w * (int)sizeof(T) + 16;
+  __device__ __forceinline__ int pass_rows(const Params& p, int w) const {
+    const int cap = min(R, p.stage_bytes / row_stride(w));
+    const int n = (R + cap - 1) / cap;
+    return (R + n - 1) / n;  // balanced chunks
   }
-  __device__ __forceinline__ int pass_rows(const Params& p, int w) const {  // B rows / chunk
-    return min(R, p.stage_bytes / row_stride(w));
+  __device__ __forceinline__ void init(const Params& p, int kc_, int nc_) {
+    kc = (MODE == kExpand) ? 0 : kc_;
+    nc = (MODE == kShrink) ? 0 : nc_;
+    nA = (kc + p.kb - 1) / p.kb;
+    kbe = nA > 0 ? ((kc + nA - 1) / nA + 7) / 8 * 8 : p.kb;
+    nA = kbe > 0 ? (kc + kbe - 1) / kbe : 0;
+    passes = (nc + p.wmax - 1) / p.wmax;
+    total = nA + (MODE == kExpand ? 1 : 0);
+    for (int ps = 0; ps < passes; ++ps) {
+      const int cb = pass_rows(p, pass_width(p, ps));
+      total += (R + cb - 1) / cb + 1;
+    }
+  }
+  struct Loc {
+    int kind, a, pass, c0, rows, wdt;
+  };
+  // Stage idx of an item -> what it holds.
+  __device__ __forceinline__ Loc locate(const Params& p, int idx) const {
+    Loc l{kChunkA, 0, 0, 0, 0, 0};
+    if (MODE == kExpand) {
+      if (idx == 0) {
+        l.kind = kChunkV;
+        return l;
+      }
+      --idx;
+    }
+    if (idx < nA) {
+      l.kind = kChunkA;
+      l.a = idx;
+      l.rows = min(kbe, kc - idx * kbe);
+      return l;
+    }
+    idx -= nA;
+    for (int ps = 0; ps < passes; ++ps) {
+      const int wdt = pass_width(p, ps);
+      const int cb = pass_rows(p, wdt);
+      const int nb = (R + cb - 1) / cb;
+      if (idx <= nb) {
+        l.pass = ps;
+        l.wdt = wdt;
+        if (idx == nb) {
+          l.kind = kChunkY;
+        } else {
+          l.kind = kChunkB;
+          l.c0 = idx * cb;
+          l.rows = min(cb, R - l.c0);
+        }
+        return l;
+      }
+      idx -= nb + 1;
+    }
+    return l;
   }
 };
 
 // ---- scheduler ------------------------------------------------------------------------
 // Exclusive scan of `cnt(i)` over i in [0, n) into out[0..n] (out[n] = total), all threads.
 template <typename F>
-__device__ void block_exclusive_scan(int n, int* out, int* wsum, F cnt) {
+__device__ __forceinline__ void block_exclusive_scan(int n, int* out, int* wsum, F cnt) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kWarps = kThreads / 32;
   const int per = (n + kThreads - 1) / kThreads;
@@ -241,7 +302,7 @@ static __device__ __forceinline__ uint32_t hash_slot(int k, int mask) {
 // exclusive prefix of "work items led by segment i".  Segment i leads its group when it is the
 // first non-empty segment of its adapter; its group gets ceil(rows / rmax) items.
 // `scratch` (transient) holds slot[S] and the hash table (3 * hash_slots ints).
-static __device__ void build_schedule(const Params& p, int* starts, int* adapters, int* base,
+static __device__ __forceinline__ void build_schedule(const Params& p, int* starts, int* adapters, int* base,
                                int* scratch, int* wsum) {
   const int tid = threadIdx.x;
   const int S = p.S, HS = p.hash_slots;
@@ -249,12 +310,29 @@ static __device__ void build_schedule(const Params& p, int* starts, int* adapter
   int* hkey = slot + S;
   int* hlead = hkey + HS;
   int* hcnt = hlead + HS;
-  for (int i = tid; i <= S; i += kThreads) starts[i] = __ldg(p.seg_starts + i);
-  for (int i = tid; i < S; i += kThreads) adapters[i] = __ldg(p.seg_adapter + i);
+  // Table loads go out first (registers), the hash is cleared while they are in flight.
+  constexpr int kPer = 4;
+  int st_v[kPer], ad_v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = tid + u * kThreads;
+    st_v[u] = (i <= S) ? __ldg(p.seg_starts + i) : 0;
+    ad_v[u] = (i < S) ? __ldg(p.seg_adapter + i) : 0;
+  }
   for (int h = tid; h < HS; h += kThreads) {
     hkey[h] = -1;
     hlead[h] = 0x7fffffff;
     hcnt[h] = 0;
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = tid + u * kThreads;
+    if (i <= S) starts[i] = st_v[u];
+    if (i < S) adapters[i] = ad_v[u];
+  }
+  for (int i = tid + kPer * kThreads; i <= S; i += kThreads) {
+    starts[i] = __ldg(p.seg_starts + i);
+    if (i < S) adapters[i] = __ldg(p.seg_adapter + i);
   }
   __syncthreads();
   for (int i = tid; i < S; i += kThreads) {
@@ -282,7 +360,7 @@ static __device__ void build_schedule(const Params& p, int* starts, int* adapter
 }
 
 // One warp: turns item t into {adapter, rows, row ids...} in d (d[0]=k, d[1]=R, d[2..]=rows).
-static __device__ void decode_item(const Params& p, int t, const int* starts, const int* adapters,
+static __device__ __forceinline__ void decode_item(const Params& p, int t, const int* starts, const int* adapters,
                             const int* base, int* d) {
   const int lane = threadIdx.x & 31;
   const int S = p.S;
@@ -322,173 +400,220 @@ static __device__ void decode_item(const Params& p, int t, const int* starts, co
 template <typename T, int R, int MODE>
 struct Kernel {
   using E = Elem<T>;
+  using Ch = Chunking<T, R, MODE>;
   static constexpr int kVec = E::kVec;
-  static constexpr int kCpr = R / kVec;          // 16-byte chunks per A row
+  static constexpr int kCpr = R / kVec;  // 16-byte chunks per A row
   static constexpr int kKLanes = kConsumers / kCpr;
   static constexpr int kEb = sizeof(T);
   static_assert(kCpr >= 1 && kCpr <= 32, "rank / vector width");
 
+  // Shared-memory map with every address precomputed once per CTA (values, not a pointer to
+  // the parameter block: the device functions are inlined and keep these in registers).
   struct Smem {
-    uint8_t* base;
-    const Params* p;
-    __device__ uint32_t bar(int i) const {
-      return smem_addr(base + p->off_bars) + 8u * static_cast<uint32_t>(i);
+    uint32_t bars_u32;  // barrier 0
+    uint8_t* ring;      // stage 0
+    uint32_t ring_u32;
+    int nst, stage_bytes, desc_ints, vpart_floats;
+    int* desc_p;
+    float *vpart_p, *vfull_p, *red_p;
+    __device__ __forceinline__ void init(uint8_t* smem, const Params& p) {
+      bars_u32 = smem_addr(smem + p.off_bars);
+      ring = smem + p.off_ring;
+      ring_u32 = smem_addr(ring);
+      nst = p.nstages;
+      stage_bytes = p.stage_bytes;
+      desc_ints = p.desc_ints;
+      vpart_floats = p.rmax * R;
+      desc_p = reinterpret_cast<int*>(smem + p.off_desc);
+      vpart_p = reinterpret_cast<float*>(smem + p.off_vpart);
+      vfull_p = reinterpret_cast<float*>(smem + p.off_vfull);
+      red_p = reinterpret_cast<float*>(smem + p.off_red);
     }
-    __device__ uint32_t full(int s) const { return bar(s); }
-    __device__ uint32_t empty(int s) const { return bar(p->nstages + s); }
-    __device__ uint32_t fixed(int b) const { return bar(2 * p->nstages + b); }
-    __device__ uint8_t* stage(int s) const {
-      return base + p->off_ring + static_cast<uint32_t>(s) * p->stage_bytes;
+    __device__ __forceinline__ uint32_t bar(int i) const {
+      return bars_u32 + 8u * static_cast<uint32_t>(i);
     }
-    __device__ int* desc(int b) const {
-      return reinterpret_cast<int*>(base + p->off_desc) + b * p->desc_ints;
+    __device__ __forceinline__ uint32_t full(int s) const { return bar(s); }
+    __device__ __forceinline__ uint32_t empty(int s) const { return bar(nst + s); }
+    __device__ __forceinline__ uint32_t fixed(int b) const { return bar(2 * nst + b); }
+    __device__ __forceinline__ uint8_t* stage(int s) const {
+      return ring + static_cast<uint32_t>(s) * static_cast<uint32_t>(stage_bytes);
     }
-    __device__ float* vpart(int b) const {
-      return reinterpret_cast<float*>(base + p->off_vpart) + b * p->rmax * R;
+    __device__ __forceinline__ uint32_t stage_u32(int s) const {
+      return ring_u32 + static_cast<uint32_t>(s) * static_cast<uint32_t>(stage_bytes);
     }
-    __device__ float* vfull() const { return reinterpret_cast<float*>(base + p->off_vfull); }
-    __device__ float* red() const { return reinterpret_cast<float*>(base + p->off_red); }
-    __device__ uint8_t* xs() const { return base + p->off_xs; }
-    __device__ uint8_t* ys() const { return base + p->off_ys; }
+    __device__ __forceinline__ int* desc(int b) const { return desc_p + b * desc_ints; }
+    __device__ __forceinline__ float* vpart(int b) const { return vpart_p + b * vpart_floats; }
+  };
+
+  // The CTAs that share one item.
+  struct Group {
+    int size;       // E
+    int m;          // this CTA's member index
+    int gid, ng;    // group index, number of groups
+    int rank0;      // cluster rank of member 0
   };
 
   // ------------------------------------------------------------------ producer warp ----
-  __device__ static void producer(const Params& p, const Smem& sm, const Waiter& w,
-                                  const int* starts, const int* adapters, const int* base,
-                                  int q, int G, int n_my, int crank, int k0, int n0,
-                                  const Chunking<T, R>& ch) {
+  // Activation part of stage `idx` of the item (x columns of an A chunk, the y rows of an
+  // expand pass, the v rows), onto the stage's full barrier.
+  __device__ __forceinline__ static void issue_acts(const Params& p, const Smem& sm,
+                                                    const Waiter& w, const Ch& ch, int idx, int s,
+                                                    const int* d, int nrow, int k0, int n0,
+                                                    uint64_t pol) {
+    const int lane = threadIdx.x & 31;
+    const typename Ch::Loc l = ch.locate(p, idx);
+    if (l.kind == kChunkA) {
+      const uint32_t xo = static_cast<uint32_t>(p.kb * R * kEb);
+      for (int i = lane; i < nrow && w.ok(); i += 32)
+        bulk_g2s(sm.stage_u32(s) + xo + static_cast<uint32_t>(i * p.kb * kEb),
+                 static_cast<const T*>(p.x) + static_cast<size_t>(d[2 + i]) * p.h_in + k0 +
+                     l.a * ch.kbe,
+                 l.rows * kEb, sm.full(s), pol);
+    } else if (l.kind == kChunkY) {
+      for (int i = lane; i < nrow && w.ok(); i += 32)
+        bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(i * l.wdt * kEb),
+                 static_cast<const T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.h_out + n0 +
+                     l.pass * p.wmax,
+                 l.wdt * kEb, sm.full(s), pol);
+    } else if (l.kind == kChunkV) {
+      for (int i = lane; i < nrow && w.ok(); i += 32)
+        bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(i * R * 4),
+                 p.v_in + static_cast<size_t>(d[2 + i]) * R, R * 4, sm.full(s), pol);
+    }
+  }
+
+  // Stage `idx` of the item into ring slot g % nst: wait for the slot, announce the bytes
+  // (weights and activations), copy the weights, and the activations when `acts`.
+  __device__ __forceinline__ static void issue_stage(const Params& p, const Smem& sm,
+                                                     const Waiter& w, const Ch& ch, int idx,
+                                                     uint32_t g, const T* Ak, const T* Bk,
+                                                     const int* d, int nrow, int k0, int n0,
+                                                     bool acts, uint64_t pol_w, uint64_t pol_a) {
+    const int lane = threadIdx.x & 31;
+    const int NST = sm.nst;
+    const int s = static_cast<int>(g % static_cast<uint32_t>(NST));
+    const typename Ch::Loc l = ch.locate(p, idx);
+    uint32_t bytes;
+    if (l.kind == kChunkA)
+      bytes = static_cast<uint32_t>((R + nrow) * l.rows * kEb);
+    else if (l.kind == kChunkB)
+      bytes = static_cast<uint32_t>(l.rows * l.wdt * kEb);
+    else if (l.kind == kChunkY)
+      bytes = static_cast<uint32_t>(nrow * l.wdt * kEb);
+    else
+      bytes = static_cast<uint32_t>(nrow * R * 4);
+    if (lane == 0) {
+      if (g >= static_cast<uint32_t>(NST)) w.wait<false>(sm.empty(s), ((g / NST) - 1) & 1);
+      mbar_arrive_expect_tx(sm.full(s), w.ok() ? bytes : 0u);
+      if (l.kind == kChunkA && w.ok())
+        bulk_g2s(sm.stage_u32(s), Ak + static_cast<size_t>(k0 + l.a * ch.kbe) * R,
+                 static_cast<uint32_t>(l.rows * R * kEb), sm.full(s), pol_w);
+    }
+    __syncwarp();
+    if (l.kind == kChunkB) {
+      const int stride = Ch::row_stride(l.wdt);
+      for (int rr = lane; rr < l.rows && w.ok(); rr += 32)
+        bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(rr * stride),
+                 Bk + static_cast<size_t>(l.c0 + rr) * p.h_out + n0 + l.pass * p.wmax,
+                 static_cast<uint32_t>(l.wdt * kEb), sm.full(s), pol_w);
+    }
+    if (acts) issue_acts(p, sm, w, ch, idx, s, d, nrow, k0, n0, pol_a);
+    __syncwarp();
+  }
+
+  __device__ __forceinline__ static void producer(const Params& p, const Smem& sm,
+                                                  const Waiter& w, const Group& grp,
+                                                  const int* starts, const int* adapters,
+                                                  const int* base, int n_my, int k0, int n0,
+                                                  const Ch& ch) {
     const int lane = threadIdx.x & 31;
     const uint64_t pol_w = policy_evict_first();  // weights: streamed once per call
-    const uint64_t pol_a = policy_evict_last();   // activations: reused by the C CTAs
-    const int NST = p.nstages;
-    uint32_t g = 0;  // ring chunk counter
+    const uint64_t pol_a = policy_evict_last();   // activations: reused by the group
+    const int NST = sm.nst;
+    uint32_t g = 0;  // ring stage counter
+    bool prior_done = false;
     for (int li = 0; li < n_my; ++li) {
-      const int t = q + li * G;
-      int* d = sm.desc(li & 1);
-      decode_item(p, t, starts, adapters, base, d);
-      if (lane == 0) mbar_arrive(sm.fixed(kDesc0 + (li & 1)));
+      const int b = li & 1;
+      if (li >= 2 && lane == 0) w.wait<false>(sm.fixed(kDescFree0 + b), ((li >> 1) - 1) & 1);
+      __syncwarp();
+      int* d = sm.desc(b);
+      decode_item(p, grp.gid + li * grp.ng, starts, adapters, base, d);
+      if (lane == 0) mbar_arrive(sm.fixed(kDescFull0 + b));
       const int k = d[0];
       const int nrow = min(max(d[1], 0), p.rmax);
       const T* Ak = nullptr;
       const T* Bk = nullptr;
-      if (MODE != kExpand) {
+      if (MODE != kExpand)
         Ak = static_cast<const T*>(p.A_ptrs[k]) + static_cast<size_t>(p.layer) * p.h_in * R;
-      }
-      if (MODE != kShrink) {
+      if (MODE != kShrink)
         Bk = static_cast<const T*>(p.B_ptrs[k]) + static_cast<size_t>(p.layer) * R * p.h_out;
+      for (int idx = 0; idx < ch.total; ++idx, ++g) {
+        if (!prior_done && g >= static_cast<uint32_t>(NST)) {
+          // The ring is full of weights that do not depend on the previous kernel of the
+          // stream; before any slot is reused, wait for that kernel and add the activations
+          // of the stages already issued (item 0 started at slot 0).
+          pdl_wait_prior();
+          prior_done = true;
+          for (int j = 0; j < idx; ++j) issue_acts(p, sm, w, ch, j, j, d, nrow, k0, n0, pol_a);
+        }
+        issue_stage(p, sm, w, ch, idx, g, Ak, Bk, d, nrow, k0, n0, prior_done, pol_w, pol_a);
       }
-      // ---- x rows (shrink, fused) or v rows (expand) into xs
-      if (li > 0 && lane == 0) w.wait<false>(sm.fixed(kXFree), (li - 1) & 1);
-      __syncwarp();
-      {
-        const uint32_t row_bytes = (MODE == kExpand) ? R * 4u : ch.kc * kEb;
-        if (lane == 0) mbar_arrive_expect_tx(sm.fixed(kXFull), w.ok() ? nrow * row_bytes : 0u);
-        __syncwarp();
-        for (int i = lane; i < nrow && row_bytes > 0 && w.ok(); i += 32) {
-          const int row = d[2 + i];
-          const void* src = (MODE == kExpand)
-                                ? static_cast<const void*>(p.v_in + static_cast<size_t>(row) * R)
-                                : static_cast<const void*>(static_cast<const T*>(p.x) +
-                                                           static_cast<size_t>(row) * p.h_in + k0);
-          bulk_g2s(smem_addr(sm.xs() + i * p.xs_row_bytes), src, row_bytes, sm.fixed(kXFull),
-                   pol_a);
-        }
-      }
-      // ---- A chunks
-      if (MODE != kExpand) {
-        for (int j = 0; j < ch.nA; ++j, ++g) {
-          const int s = g % NST;
-          if (lane == 0) {
-            if (g >= (uint32_t)NST) w.wait<false>(sm.empty(s), ((g / NST) - 1) & 1);
-            const int rows = min(ch.kb, ch.kc - j * ch.kb);
-            const uint32_t bytes = rows * R * kEb;
-            mbar_arrive_expect_tx(sm.full(s), w.ok() ? bytes : 0u);
-            if (w.ok())
-              bulk_g2s(smem_addr(sm.stage(s)), Ak + static_cast<size_t>(k0 + j * ch.kb) * R,
-                       bytes, sm.full(s), pol_w);
-          }
-        }
-      }
-      // ---- y rows
-      if (MODE != kShrink) {
-        if (li > 0 && lane == 0) w.wait<false>(sm.fixed(kYFree), (li - 1) & 1);
-        __syncwarp();
-        const uint32_t row_bytes = ch.nc * kEb;
-        if (lane == 0) mbar_arrive_expect_tx(sm.fixed(kYFull), w.ok() ? nrow * row_bytes : 0u);
-        __syncwarp();
-        for (int i = lane; i < nrow && row_bytes > 0 && w.ok(); i += 32) {
-          const int row = d[2 + i];
-          bulk_g2s(smem_addr(sm.ys() + i * p.ys_row_bytes),
-                   static_cast<const T*>(p.y) + static_cast<size_t>(row) * p.h_out + n0,
-                   row_bytes, sm.fixed(kYFull), pol_a);
-        }
-        // ---- B chunks: pass by pass, `cb` rows of the pass's column window per chunk
-        for (int pass = 0; pass < ch.passes; ++pass) {
-          const int wdt = ch.pass_width(p, pass);
-          const int cb = ch.pass_rows(p, wdt);
-          const int stride = Chunking<T, R>::row_stride(wdt);
-          for (int c0 = 0; c0 < R; c0 += cb, ++g) {
-            const int s = g % NST;
-            const int rows = min(cb, R - c0);
-            if (lane == 0) {
-              if (g >= (uint32_t)NST) w.wait<false>(sm.empty(s), ((g / NST) - 1) & 1);
-              mbar_arrive_expect_tx(sm.full(s), w.ok() ? rows * wdt * kEb : 0u);
-            }
-            __syncwarp();
-            for (int rr = lane; rr < rows && w.ok(); rr += 32) {
-              bulk_g2s(smem_addr(sm.stage(s) + rr * stride),
-                       Bk + static_cast<size_t>(c0 + rr) * p.h_out + n0 + pass * p.wmax,
-                       wdt * kEb, sm.full(s), pol_w);
-            }
-            __syncwarp();
-          }
-        }
+      if (!prior_done) {
+        pdl_wait_prior();
+        prior_done = true;
+        for (int j = 0; j < ch.total; ++j) issue_acts(p, sm, w, ch, j, j, d, nrow, k0, n0, pol_a);
       }
     }
+    if (!prior_done) pdl_wait_prior();
   }
 
   // --------------------------------------------------------------- consumer warps ----
   template <int RB>
-  __device__ static void consume_item(const Params& p, const Smem& sm, const Waiter& w,
-                                      int li, uint32_t& g, const int* d, int nrow, int crank,
-                                      int k0, int n0, const Chunking<T, R>& ch) {
+  __device__ __forceinline__ static void consume_item(const Params& p, const Smem& sm,
+                                                      const Waiter& w, const Group& grp, int li,
+                                                      bool last, uint32_t& g, const int* d,
+                                                      int nrow, int n0, const Ch& ch) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int NST = p.nstages;
+    const int NST = sm.nst;
     float acc[RB][kVec];
-    float* vfull = sm.vfull();
+    float* vfull = sm.vfull_p;
 
-    if (MODE != kExpand) {
+    if (MODE == kExpand) {
+      // ------------------------------------------------------------- v rows of the item
+      const int s = static_cast<int>(g % static_cast<uint32_t>(NST));
+      w.wait<false>(sm.full(s), (g / NST) & 1);
+      const float* vs = reinterpret_cast<const float*>(sm.stage(s));
+      for (int t = tid; t < nrow * R; t += kConsumers) vfull[t] = p.scale * vs[t];
+      named_bar(1, kConsumers);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.empty(s));
+      ++g;
+    } else {
       // ----------------------------------------------------------- shrink (split-K)
 #pragma unroll
       for (int i = 0; i < RB; ++i)
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) acc[i][j] = 0.f;
-      w.wait<false>(sm.fixed(kXFull), li & 1);
+        for (int e = 0; e < kVec; ++e) acc[i][e] = 0.f;
       const int cc = tid % kCpr, kl = tid / kCpr;
-      const uint8_t* xs = sm.xs();
-      const int xs_row = p.xs_row_bytes;
+      const int xrow = p.kb * kEb;
       for (int j = 0; j < ch.nA; ++j, ++g) {
-        const int s = g % NST;
+        const int s = static_cast<int>(g % static_cast<uint32_t>(NST));
         w.wait<false>(sm.full(s), (g / NST) & 1);
-        const int kr0 = j * ch.kb;
-        const int rows = min(ch.kb, ch.kc - kr0);
+        const int rows = min(ch.kbe, ch.kc - j * ch.kbe);
         const uint8_t* st = sm.stage(s);
+        const uint8_t* xs = st + p.kb * R * kEb;
         for (int kk = kl; kk < rows; kk += kKLanes) {
           float a[kVec];
           E::load16(st + (kk * R + cc * kVec) * kEb, a);
 #pragma unroll
           for (int i = 0; i < RB; ++i) {
-            const float xv = E::load1(xs + i * xs_row + (kr0 + kk) * kEb);
+            const float xv = E::load1(xs + i * xrow + kk * kEb);
 #pragma unroll
             for (int e = 0; e < kVec; ++e) acc[i][e] = fmaf(xv, a[e], acc[i][e]);
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty(s));
-      }
-      if (MODE == kFused) {  // xs is no longer read (shrink-only releases it after writing v,
-        __syncwarp();        // since the producer may rewrite this descriptor after that)
-        if (lane == 0) mbar_arrive(sm.fixed(kXFree));
       }
       // reduce over the k-lanes of the warp (lanes with equal cc), then over warps
 #pragma unroll
@@ -497,7 +622,7 @@ struct Kernel {
         for (int i = 0; i < RB; ++i)
 #pragma unroll
           for (int e = 0; e < kVec; ++e) acc[i][e] += __shfl_xor_sync(0xffffffffu, acc[i][e], o);
-      float* red = sm.red();
+      float* red = sm.red_p;
       if (lane < kCpr) {
 #pragma unroll
         for (int i = 0; i < RB; ++i)
@@ -506,58 +631,55 @@ struct Kernel {
             red[(warp * p.rmax + i) * R + lane * kVec + e] = acc[i][e];
       }
       named_bar(1, kConsumers);
-      float* vp = sm.vpart(li & 1);
-      for (int t = tid; t < RB * R; t += kConsumers) {
-        const int i = t / R, c = t % R;
-        float s = 0.f;
+      if (grp.size == 1) {
+        for (int t = tid; t < nrow * R; t += kConsumers) {
+          float s = 0.f;
 #pragma unroll
-        for (int ww = 0; ww < kConsumerWarps; ++ww) s += red[(ww * p.rmax + i) * R + c];
-        vp[i * R + c] = s;
-      }
-      named_bar(1, kConsumers);
-      // ----------------------------------------------------- cluster all-reduce of v
-      const uint32_t vready = sm.fixed(kVReady0 + (li & 1));
-      if (tid == 0) {
-        fence_acq_rel_cluster();
-        for (int c = 0; c < p.C; ++c) mbar_arrive_remote(vready, c);
-      }
-      w.wait<true>(vready, (li >> 1) & 1);
-      const uint32_t vp_addr = smem_addr(vp);
-      for (int t = tid; t < nrow * R; t += kConsumers) {
-        float s = 0.f;
-        for (int c = 0; c < p.C; ++c) s += ld_cluster_f32(cluster_map(vp_addr + 4u * t, c));
-        if (MODE == kFused) {
-          vfull[t] = s * p.scale;
-        } else {  // shrink: CTA (row mod C) writes the row
-          const int i = t / R;
-          if ((i % p.C) == crank && w.ok())
-            p.v_out[static_cast<size_t>(d[2 + i]) * R + (t % R)] = s;
+          for (int ww = 0; ww < kConsumerWarps; ++ww) s += red[ww * p.rmax * R + t];
+          if (MODE == kFused) {
+            vfull[t] = s * p.scale;
+          } else if (w.ok()) {
+            p.v_out[static_cast<size_t>(d[2 + t / R]) * R + (t % R)] = s;
+          }
         }
+        named_bar(1, kConsumers);
+      } else {
+        float* vp = sm.vpart(li & 1);
+        for (int t = tid; t < nrow * R; t += kConsumers) {
+          float s = 0.f;
+#pragma unroll
+          for (int ww = 0; ww < kConsumerWarps; ++ww) s += red[ww * p.rmax * R + t];
+          vp[t] = s;
+        }
+        named_bar(1, kConsumers);
+        // ------------------------------------------------- group all-reduce of v (DSMEM)
+        const uint32_t vready = sm.fixed(kVReady0 + (li & 1));
+        if (li == 0) cluster_wait();  // peers' barriers are initialised (arrive #1)
+        if (tid == 0)
+          for (int j = 0; j < grp.size; ++j) mbar_arrive_remote(vready, grp.rank0 + j);
+        w.wait<true>(vready, (li >> 1) & 1);
+        const uint32_t vp_addr = smem_addr(vp);
+        for (int t = tid; t < nrow * R; t += kConsumers) {
+          float s = 0.f;
+          for (int j = 0; j < grp.size; ++j)
+            s += ld_cluster_f32(cluster_map(vp_addr + 4u * t, grp.rank0 + j));
+          if (MODE == kFused) {
+            vfull[t] = s * p.scale;
+          } else if ((t / R) % grp.size == grp.m && w.ok()) {
+            p.v_out[static_cast<size_t>(d[2 + t / R]) * R + (t % R)] = s;
+          }
+        }
+        named_bar(1, kConsumers);
+        if (last) cluster_arrive();  // no more reads of peer shared memory (arrive #2)
       }
-      named_bar(1, kConsumers);
-      if (MODE == kShrink) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sm.fixed(kXFree));
-      }
-    } else {
-      // ------------------------------------------------------------- expand only
-      w.wait<false>(sm.fixed(kXFull), li & 1);
-      for (int t = tid; t < nrow * R; t += kConsumers) {
-        const int i = t / R, c = t % R;
-        vfull[t] = p.scale * reinterpret_cast<const float*>(sm.xs() + i * p.xs_row_bytes)[c];
-      }
-      named_bar(1, kConsumers);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.fixed(kXFree));
     }
 
     if (MODE != kShrink) {
       // ------------------------------------------------------- expand over the N slice
-      bool y_ready = false;
       for (int pass = 0; pass < ch.passes; ++pass) {
         const int wdt = ch.pass_width(p, pass);
         const int cb = ch.pass_rows(p, wdt);
-        const int stride = Chunking<T, R>::row_stride(wdt);
+        const int stride = Ch::row_stride(wdt);
         const int nch = wdt / kVec;
         int cl_n = 1;
         while (cl_n < 32 && nch * cl_n * 2 <= kConsumers) cl_n <<= 1;
@@ -568,19 +690,19 @@ struct Kernel {
 #pragma unroll
           for (int e = 0; e < kVec; ++e) acc[i][e] = 0.f;
         for (int c0 = 0; c0 < R; c0 += cb, ++g) {
-          const int s = g % NST;
+          const int s = static_cast<int>(g % static_cast<uint32_t>(NST));
           const int rows = min(cb, R - c0);
           w.wait<false>(sm.full(s), (g / NST) & 1);
           if (active) {
             const uint8_t* st = sm.stage(s) + my_ch * 16;
             for (int c = cl; c < rows; c += cl_n) {
-              float b[kVec];
-              E::load16(st + c * stride, b);
+              float bv[kVec];
+              E::load16(st + c * stride, bv);
 #pragma unroll
               for (int i = 0; i < RB; ++i) {
                 const float vv = vfull[i * R + c0 + c];
 #pragma unroll
-                for (int e = 0; e < kVec; ++e) acc[i][e] = fmaf(vv, b[e], acc[i][e]);
+                for (int e = 0; e < kVec; ++e) acc[i][e] = fmaf(vv, bv[e], acc[i][e]);
               }
             }
           }
@@ -592,57 +714,64 @@ struct Kernel {
           for (int i = 0; i < RB; ++i)
 #pragma unroll
             for (int e = 0; e < kVec; ++e) acc[i][e] += __shfl_xor_sync(0xffffffffu, acc[i][e], o);
-        if (!y_ready) {
-          w.wait<false>(sm.fixed(kYFull), li & 1);
-          y_ready = true;
-        }
+        // the pass's y rows: add, round once, store
+        const int s = static_cast<int>(g % static_cast<uint32_t>(NST));
+        w.wait<false>(sm.full(s), (g / NST) & 1);
         if (active && cl == 0 && w.ok()) {
-          const int col = pass * p.wmax + my_ch * kVec;
+          const int col = my_ch * kVec;
+          const uint8_t* ys = sm.stage(s);
 #pragma unroll
           for (int i = 0; i < RB; ++i) {
             if (i < nrow) {
               float yo[kVec];
-              E::load16(sm.ys() + i * p.ys_row_bytes + col * kEb, yo);
+              E::load16(ys + (i * wdt + col) * kEb, yo);
 #pragma unroll
               for (int e = 0; e < kVec; ++e) yo[e] += acc[i][e];
-              E::store16(static_cast<T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.h_out + n0 + col,
+              E::store16(static_cast<T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.h_out +
+                             n0 + pass * p.wmax + col,
                          yo);
             }
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty(s));
+        ++g;
       }
-      if (!y_ready) w.wait<false>(sm.fixed(kYFull), li & 1);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.fixed(kYFree));
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.fixed(kDescFree0 + (li & 1)));
   }
 
-  __device__ static void consumer(const Params& p, const Smem& sm, const Waiter& w, int n_my,
-                                  int crank, int k0, int n0, const Chunking<T, R>& ch) {
+  __device__ __forceinline__ static void consumer(const Params& p, const Smem& sm,
+                                                  const Waiter& w, const Group& grp, int n_my,
+                                                  int n0, const Ch& ch) {
     uint32_t g = 0;
     for (int li = 0; li < n_my; ++li) {
-      w.wait<false>(sm.fixed(kDesc0 + (li & 1)), (li >> 1) & 1);
+      w.wait<false>(sm.fixed(kDescFull0 + (li & 1)), (li >> 1) & 1);
       const int* d = sm.desc(li & 1);
       const int nrow = min(max(d[1], 0), p.rmax);
+      const bool last = li == n_my - 1;
       if (nrow <= 1)
-        consume_item<1>(p, sm, w, li, g, d, nrow, crank, k0, n0, ch);
+        consume_item<1>(p, sm, w, grp, li, last, g, d, nrow, n0, ch);
       else if (nrow <= 2)
-        consume_item<2>(p, sm, w, li, g, d, nrow, crank, k0, n0, ch);
-      else if (nrow <= 4)
-        consume_item<4>(p, sm, w, li, g, d, nrow, crank, k0, n0, ch);
+        consume_item<2>(p, sm, w, grp, li, last, g, d, nrow, n0, ch);
       else
-        consume_item<8>(p, sm, w, li, g, d, nrow, crank, k0, n0, ch);
+        consume_item<kRowsMax>(p, sm, w, grp, li, last, g, d, nrow, n0, ch);
+    }
+    // keep every thread's cluster barrier sequence: wait #1, arrive #2 (done per item above
+    // when the group exchanges partial products)
+    if (MODE != kExpand && !(grp.size > 1 && n_my > 0)) {
+      cluster_wait();
+      cluster_arrive();
     }
   }
 
-  __device__ static void run(const Params& p) {
+  __device__ __forceinline__ static void run(const Params& p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    Smem sm{smem, &p};
+    pdl_launch_dependents();  // the next kernel of the stream may start its weight prefetch
+    Smem sm;
+    sm.init(smem, p);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int C = p.C;
-    const int crank = static_cast<int>(blockIdx.x) % C;
-    const int q = static_cast<int>(blockIdx.x) / C;
-    const int G = static_cast<int>(gridDim.x) / C;
     int* ctl = reinterpret_cast<int*>(smem + p.off_ctl);
     int* starts = reinterpret_cast<int*>(smem + p.off_tab);
     int* adapters = starts + (p.S + 1);
@@ -653,46 +782,63 @@ struct Kernel {
         mbar_init(sm.full(s), 1);
         mbar_init(sm.empty(s), kConsumerWarps);
       }
-      mbar_init(sm.fixed(kXFull), 1);
-      mbar_init(sm.fixed(kXFree), kConsumerWarps);
-      mbar_init(sm.fixed(kYFull), 1);
-      mbar_init(sm.fixed(kYFree), kConsumerWarps);
-      mbar_init(sm.fixed(kDesc0), 1);
-      mbar_init(sm.fixed(kDesc1), 1);
-      mbar_init(sm.fixed(kVReady0), C);
-      mbar_init(sm.fixed(kVReady1), C);
+      mbar_init(sm.fixed(kDescFull0), 1);
+      mbar_init(sm.fixed(kDescFull1), 1);
+      mbar_init(sm.fixed(kDescFree0), kConsumerWarps);
+      mbar_init(sm.fixed(kDescFree1), kConsumerWarps);
       mbar_init(sm.fixed(kNever), 1);
       ctl[0] = 0;
-      fence_mbar_init();
     }
     build_schedule(p, starts, adapters, base, reinterpret_cast<int*>(smem + p.off_ring),
                    ctl + 4);
+    // Group size E: as large as the launch cluster allows while every item still gets its own
+    // group of CTAs (few items: split each across CTAs; many items: one CTA each, no exchange).
+    const int n_items = base[p.S];
+    const int N = static_cast<int>(gridDim.x);
+    Group grp;
+    grp.size = 1;
+    while (grp.size * 2 <= p.C && n_items * grp.size * 2 <= N) grp.size *= 2;
+    grp.m = static_cast<int>(blockIdx.x) % grp.size;
+    grp.gid = static_cast<int>(blockIdx.x) / grp.size;
+    grp.ng = N / grp.size;
+    grp.rank0 = (static_cast<int>(blockIdx.x) % p.C) / grp.size * grp.size;
+    if (tid == 0) {
+      mbar_init(sm.fixed(kVReady0), grp.size);
+      mbar_init(sm.fixed(kVReady1), grp.size);
+      fence_mbar_init();
+    }
     fence_proxy_async();  // the ring held the hash table: order before bulk copies land
     __syncthreads();
-    if (MODE != kExpand) cluster_sync_all();  // peers' barriers are initialised
+    // Cluster barrier protocol (fused / shrink), per thread: arrive #1 here (barriers are
+    // initialised) -> wait #1 before the first remote arrive -> arrive #2 after the last read of
+    // peer shared memory -> wait #2 at exit (no CTA leaves while a peer may still read it).
+    if (MODE != kExpand) cluster_arrive();
 
     const Waiter w{reinterpret_cast<volatile int*>(ctl), p.err, p.wait_limit_ns};
     if (p.inject_stall) w.wait<false>(sm.fixed(kNever), 0);  // nothing completes it
 
-    const int n_items = base[p.S];
-    const int n_my = (q < n_items) ? (n_items - q + G - 1) / G : 0;
+    const int n_my = (grp.gid < n_items) ? (n_items - grp.gid + grp.ng - 1) / grp.ng : 0;
     int k0 = 0, k1 = 0, n0 = 0, n1 = 0;
-    slice_of(p.h_in, C, crank, k0, k1);
-    slice_of(p.h_out, C, crank, n0, n1);
-    Chunking<T, R> ch;
-    ch.init(p, MODE == kExpand ? 0 : k1 - k0, MODE == kShrink ? 0 : n1 - n0);
+    slice_of(p.h_in, grp.size, grp.m, k0, k1);
+    slice_of(p.h_out, grp.size, grp.m, n0, n1);
+    Ch ch;
+    ch.init(p, k1 - k0, n1 - n0);
 
     if (warp == kConsumerWarps) {
-      producer(p, sm, w, starts, adapters, base, q, G, n_my, crank, k0, n0, ch);
+      producer(p, sm, w, grp, starts, adapters, base, n_my, k0, n0, ch);
+      if (MODE != kExpand) {
+        cluster_wait();
+        cluster_arrive();
+      }
     } else {
-      consumer(p, sm, w, n_my, crank, k0, n0, ch);
+      consumer(p, sm, w, grp, n_my, n0, ch);
     }
     __syncthreads();
     if (!w.ok()) {  // gave up: let every bulk copy already issued land before the CTA exits
       const uint64_t t0 = now_ns();
       while (now_ns() - t0 < 200000ull) __nanosleep(1000);
     }
-    if (MODE != kExpand) cluster_sync_all();  // no CTA leaves while peers read its smem
+    if (MODE != kExpand) cluster_wait();
   }
 };
 

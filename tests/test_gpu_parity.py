@@ -295,3 +295,78 @@ def test_wait_timeout_reports_and_recovers():
     y = harness.run_apply(c, 0)
     harness.assert_close(y.float().cpu().numpy(), harness.oracle_apply(c, 0), "after timeout")
     assert sgmv_get_error(clear=True) == 0
+
+
+# ------------------------------------------------------------- overlapped launches ----
+@pytest.mark.parametrize("use_graph", [False, True])
+def test_overlap_prior_chain(use_graph):
+    """Back-to-back lora_apply_ex(SGMV_OVERLAP_PRIOR) calls where each call reads, as x, the y
+    the previous call wrote: the prefetch may overlap the previous kernel, the activations may
+    not.  Checked against the oracle applied in sequence."""
+    import oracle
+    from segmented_gather_gemm_sgmv_gb300 import lora_apply
+    w = workloads.Workload("chain", 1024, 1024, 16, "f16", 24, 6)
+    rng = np.random.default_rng(21)
+    ss, sa = workloads.random_segments(rng, 40, 3, 24)
+    c = harness.make_case(w, ss, sa)
+    n = 6
+    ys = [c.y0.clone() * 0.5 for _ in range(n)]
+    x0 = c.x.clone()
+    stream = torch.cuda.Stream()
+
+    def chain():
+        x = x0
+        for i in range(n):
+            lora_apply(ys[i], x, c.A_ptrs, c.B_ptrs, c.d_ss, c.d_sa, i, w.r, w.scale,
+                       stream=stream, overlap_prior=True)
+            x = ys[i]
+
+    if use_graph:
+        with torch.cuda.stream(stream):
+            chain()  # uncaptured first calls set kernel attributes
+        torch.cuda.synchronize()
+        for i in range(n):
+            ys[i].copy_(c.y0 * 0.5)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            chain()
+        for i in range(n):
+            ys[i].copy_(c.y0 * 0.5)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            g.replay()
+    else:
+        with torch.cuda.stream(stream):
+            chain()
+    torch.cuda.synchronize()
+    keys = harness.touched(sa, ss)
+    x = x0.double().cpu().numpy()
+    for i in range(n):
+        A = harness.oracle_blocks(c.A, keys, i)
+        B = harness.oracle_blocks(c.B, keys, i)
+        y_in = (c.y0 * 0.5).double().cpu().numpy()
+        ref = oracle.lora_apply(y_in, x, A, B, ss, sa, 0, w.scale)
+        harness.assert_close(ys[i].float().cpu().numpy(), ref, f"chain step {i}")
+        x = ys[i].double().cpu().numpy()  # the next call reads what this one wrote
+
+
+def test_max_segments():
+    """num_segments = SGMV_MAX_SEGMENTS (4096 one-token segments; the large-table geometry)."""
+    from segmented_gather_gemm_sgmv_gb300 import SgmvError, binding
+    w = workloads.Workload("maxseg", 512, 256, 16, "bf16", 64, 1)
+    rng = np.random.default_rng(9)
+    S = binding.SGMV_MAX_SEGMENTS
+    ss = np.arange(S + 1, dtype=np.int32)
+    sa = rng.integers(-1, 64, size=S).astype(np.int32)
+    c = harness.make_case(w, ss, sa)
+    y = harness.run_apply(c, 0)
+    harness.assert_close(y.float().cpu().numpy(), harness.oracle_apply(c, 0), "max segments")
+    _check_untouched(c, y)
+    ss2 = np.arange(S + 2, dtype=np.int32)
+    sa2 = np.zeros(S + 1, np.int32)
+    with pytest.raises(SgmvError) as e:
+        from segmented_gather_gemm_sgmv_gb300 import lora_apply
+        lora_apply(c.y0.clone(), c.x, c.A_ptrs, c.B_ptrs,
+                   torch.as_tensor(ss2, device="cuda"), torch.as_tensor(sa2, device="cuda"), 0,
+                   w.r, w.scale)
+    assert e.value.status == -3
