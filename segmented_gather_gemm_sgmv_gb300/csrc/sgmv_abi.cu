@@ -112,6 +112,46 @@ struct Problem {
   float scale;
 };
 
+void slice(int n, int parts, int m, int* lo, int* hi) {
+  const int units = n / 8;  // slices start on multiples of 8 elements (16-byte aligned)
+  *lo = units * m / parts * 8;
+  *hi = units * (m + 1) / parts * 8;
+}
+
+// B rows per chunk of an expand pass of width w: as many as a stage holds, balanced.
+int pass_rows(int r, int stage_bytes, int w, int eb) {
+  const int cap = std::min(r, stage_bytes / (w * eb + 16));
+  const int n = (r + cap - 1) / cap;
+  return (r + n - 1) / n;
+}
+
+// Chunk plan of member m of a group of E CTAs (the kernel indexes these, so it does no
+// division by runtime values).
+sgmv::MemberPlan member_plan(const Problem& pb, int E, int m, int kb, int wmax, int stage_bytes,
+                             int eb) {
+  sgmv::MemberPlan mp = {};
+  int k1 = 0, n1 = 0;
+  slice(pb.h_in, E, m, &mp.k0, &k1);
+  slice(pb.h_out, E, m, &mp.n0, &n1);
+  mp.kc = pb.mode == sgmv::kExpand ? 0 : k1 - mp.k0;
+  mp.nc = pb.mode == sgmv::kShrink ? 0 : n1 - mp.n0;
+  mp.nA = (mp.kc + kb - 1) / kb;
+  mp.kbe = mp.nA > 0 ? ((mp.kc + mp.nA - 1) / mp.nA + 7) / 8 * 8 : kb;
+  mp.nA = (mp.kc + mp.kbe - 1) / mp.kbe;
+  mp.passes = (mp.nc + wmax - 1) / wmax;
+  mp.total = mp.nA + (pb.mode == sgmv::kExpand ? 1 : 0);
+  if (mp.passes > 0) {
+    mp.w_full = wmax;
+    mp.cb_full = pass_rows(pb.r, stage_bytes, wmax, eb);
+    mp.nb_full = (pb.r + mp.cb_full - 1) / mp.cb_full;
+    mp.w_last = mp.nc - (mp.passes - 1) * wmax;
+    mp.cb_last = pass_rows(pb.r, stage_bytes, mp.w_last, eb);
+    mp.nb_last = (pb.r + mp.cb_last - 1) / mp.cb_last;
+    mp.total += (mp.passes - 1) * (mp.nb_full + 1) + mp.nb_last + 1;
+  }
+  return mp;
+}
+
 // Lays out shared memory and fills the geometry part of the kernel parameters.  The launch
 // cluster is kMaxGroup CTAs; the kernel itself picks how many of them share an item.
 int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* smem_out) {
@@ -138,8 +178,8 @@ int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* sme
   p.desc_ints = static_cast<int32_t>(up(2 + rmax, 4));
   p.off_desc = static_cast<uint32_t>(off);
   off += 2 * 4 * p.desc_ints;
-  p.off_tab = static_cast<uint32_t>(off);
-  off += up(4 * (3 * static_cast<size_t>(pb.S) + 2), 16);
+  p.off_tab = static_cast<uint32_t>(off);  // starts[S+1], adapters[S], base[S+1], gcnt[S]
+  off += up(4 * (4 * static_cast<size_t>(pb.S) + 2), 16);
   p.off_vpart = static_cast<uint32_t>(off);
   off += 2 * 4 * rmax * pb.r;
   p.off_vfull = static_cast<uint32_t>(off);
@@ -161,10 +201,11 @@ int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* sme
   p.C = C;
   p.nstages = nst;
   p.stage_bytes = stage_bytes;
-  p.rmax = rmax;
   p.kb = kb;
-  p.wmax = wmax;
   p.hash_slots = hs;
+  int slot = 0;
+  for (int E = 1; E <= C; E <<= 1)
+    for (int m = 0; m < E; ++m) p.plan[slot++] = member_plan(pb, E, m, kb, wmax, stage_bytes, eb);
   *smem_out = off;
   return SGMV_OK;
 }

@@ -50,7 +50,22 @@ enum Mode : int { kFused = 0, kShrink = 1, kExpand = 2 };
 enum Bar : int { kDescFull0 = 0, kDescFull1, kDescFree0, kDescFree1, kVReady0, kVReady1, kNever,
                  kNumFixedBars };
 
-constexpr int kMaxGroup = 4;  // largest number of CTAs that share one item (launch cluster size)
+constexpr int kMaxGroup = 4;   // largest number of CTAs that share one item (launch cluster size)
+constexpr int kPlanSlots = 7;  // member plans: E = 1 (slot 0), E = 2 (slots 1-2), E = 4 (3-6)
+
+// What one member of a group of E CTAs streams for an item (computed on the host, so that the
+// kernel does no division by runtime values).  Expand passes: all but the last cover w_full
+// columns of the member's h_out slice, the last covers w_last; each pass is nb B chunks of cb
+// B rows (the last chunk may be shorter) and one stage of y rows.
+struct MemberPlan {
+  int32_t k0, kc;        // h_in slice [k0, k0 + kc)
+  int32_t nA, kbe;       // A chunks, A rows per chunk (a multiple of 8)
+  int32_t n0, nc;        // h_out slice [n0, n0 + nc)
+  int32_t passes;        // expand passes
+  int32_t w_full, cb_full, nb_full;
+  int32_t w_last, cb_last, nb_last;
+  int32_t total;         // ring stages per item
+};
 
 struct Params {
   void* y;
@@ -67,14 +82,13 @@ struct Params {
   int32_t C;            // launch cluster size (a multiple of every group size used)
   int32_t nstages;      // ring stages
   int32_t stage_bytes;  // bytes per ring stage
-  int32_t rmax;         // rows per work item
-  int32_t kb;           // A rows per chunk (the chunk's x columns follow them in the stage)
-  int32_t wmax;         // widest window of B columns one expand pass covers (elements)
+  int32_t kb;           // x-row stride (elements) inside an A stage (>= every kbe)
   int32_t hash_slots;   // power of two > 1.5*S
   uint32_t off_bars, off_ctl, off_desc, off_tab, off_vpart, off_vfull, off_red, off_ring;
   int32_t desc_ints;
   uint64_t wait_limit_ns;
   int32_t inject_stall;
+  MemberPlan plan[kPlanSlots];
 };
 
 // ---- element types ---------------------------------------------------------------------
@@ -173,87 +187,74 @@ struct Waiter {
   __device__ __forceinline__ bool ok() const { return *abort == 0; }
 };
 
-// ---- slices and chunking (identical arithmetic on the producer and consumer sides) -------
-static __device__ __forceinline__ void slice_of(int n, int parts, int m, int& lo, int& hi) {
-  const int units = n >> 3;  // slices start on multiples of 8 elements (16-byte aligned)
-  lo = (units * m / parts) << 3;
-  hi = (units * (m + 1) / parts) << 3;
-}
-
-// The stages of one item: [A chunks][pass 0: B chunks, y][pass 1: ...] (fused);
+// ---- stage layout ---------------------------------------------------------------------
+// The stages of one item, in ring order: [A chunks][pass 0: B chunks, y][pass 1: ...] (fused);
 // [A chunks] (shrink); [v][pass 0: B chunks, y]... (expand).
-enum ChunkKind : int { kChunkA = 0, kChunkB = 1, kChunkY = 2, kChunkV = 3 };
+enum ChunkKind : int { kChunkA = 0, kChunkB = 1, kChunkY = 2, kChunkV = 3, kChunkEnd = 4 };
 
-template <typename T, int R, int MODE>
-struct Chunking {
-  int kc, nc;     // this CTA's h_in / h_out slice width
-  int nA;         // A chunks
-  int kbe;        // A rows per chunk (balanced, <= p.kb, a multiple of 8)
-  int passes;     // expand passes
-  int total;      // stages per item
-  __device__ __forceinline__ static int row_stride(int w) {  // padded B row in a stage
-    return w * static_cast<int>(sizeof(T)) + 16;
+static __device__ __forceinline__ int b_row_stride(int w, int eb) { return w * eb + 16; }
+
+// Walks the stages of an item in ring order (increments only, no division).
+template <int R, int MODE>
+struct StageWalk {
+  int kind, a, pass, c0, rows, wdt, cb;
+  __device__ __forceinline__ void set_pass(const MemberPlan& mp, int ps) {
+    pass = ps;
+    const bool lastp = ps == mp.passes - 1;
+    wdt = lastp ? mp.w_last : mp.w_full;
+    cb = lastp ? mp.cb_last : mp.cb_full;
+    kind = kChunkB;
+    c0 = 0;
+    rows = min(cb, R);
   }
-  __device__ __forceinline__ int pass_width(const Params& p, int pass) const {
-    return min(p.wmax, nc - pass * p.wmax);
+  __device__ __forceinline__ void after_a(const MemberPlan& mp) {
+    if (MODE != kShrink && mp.passes > 0) set_pass(mp, 0); else kind = kChunkEnd;
   }
-  __device__ __forceinline__ int pass_rows(const Params& p, int w) const {
-    const int cap = min(R, p.stage_bytes / row_stride(w));
-    const int n = (R + cap - 1) / cap;
-    return (R + n - 1) / n;  // balanced chunks
-  }
-  __device__ __forceinline__ void init(const Params& p, int kc_, int nc_) {
-    kc = (MODE == kExpand) ? 0 : kc_;
-    nc = (MODE == kShrink) ? 0 : nc_;
-    nA = (kc + p.kb - 1) / p.kb;
-    kbe = nA > 0 ? ((kc + nA - 1) / nA + 7) / 8 * 8 : p.kb;
-    nA = kbe > 0 ? (kc + kbe - 1) / kbe : 0;
-    passes = (nc + p.wmax - 1) / p.wmax;
-    total = nA + (MODE == kExpand ? 1 : 0);
-    for (int ps = 0; ps < passes; ++ps) {
-      const int cb = pass_rows(p, pass_width(p, ps));
-      total += (R + cb - 1) / cb + 1;
-    }
-  }
-  struct Loc {
-    int kind, a, pass, c0, rows, wdt;
-  };
-  // Stage idx of an item -> what it holds.
-  __device__ __forceinline__ Loc locate(const Params& p, int idx) const {
-    Loc l{kChunkA, 0, 0, 0, 0, 0};
+  __device__ __forceinline__ void first(const MemberPlan& mp) {
+    a = 0;
+    pass = 0;
+    c0 = 0;
+    wdt = 0;
+    cb = 0;
     if (MODE == kExpand) {
-      if (idx == 0) {
-        l.kind = kChunkV;
-        return l;
-      }
-      --idx;
+      kind = kChunkV;
+    } else if (mp.nA > 0) {
+      kind = kChunkA;
+      rows = min(mp.kbe, mp.kc);
+    } else {
+      after_a(mp);
     }
-    if (idx < nA) {
-      l.kind = kChunkA;
-      l.a = idx;
-      l.rows = min(kbe, kc - idx * kbe);
-      return l;
+  }
+  __device__ __forceinline__ void next(const MemberPlan& mp) {
+    if (kind == kChunkV) {
+      after_a(mp);
+    } else if (kind == kChunkA) {
+      if (++a < mp.nA) rows = min(mp.kbe, mp.kc - a * mp.kbe); else after_a(mp);
+    } else if (kind == kChunkB) {
+      c0 += cb;
+      if (c0 < R) rows = min(cb, R - c0); else kind = kChunkY;
+    } else if (kind == kChunkY) {
+      if (pass + 1 < mp.passes) set_pass(mp, pass + 1); else kind = kChunkEnd;
     }
-    idx -= nA;
-    for (int ps = 0; ps < passes; ++ps) {
-      const int wdt = pass_width(p, ps);
-      const int cb = pass_rows(p, wdt);
-      const int nb = (R + cb - 1) / cb;
-      if (idx <= nb) {
-        l.pass = ps;
-        l.wdt = wdt;
-        if (idx == nb) {
-          l.kind = kChunkY;
-        } else {
-          l.kind = kChunkB;
-          l.c0 = idx * cb;
-          l.rows = min(cb, R - l.c0);
-        }
-        return l;
-      }
-      idx -= nb + 1;
+  }
+};
+
+// Ring slot iterator: slot s, phase parity of the current round, whether a round completed.
+struct RingPos {
+  int s;
+  uint32_t par;
+  bool wrapped;
+  __device__ __forceinline__ void init() {
+    s = 0;
+    par = 0;
+    wrapped = false;
+  }
+  __device__ __forceinline__ void next(int nst) {
+    if (++s == nst) {
+      s = 0;
+      par ^= 1u;
+      wrapped = true;
     }
-    return l;
   }
 };
 
@@ -300,10 +301,12 @@ static __device__ __forceinline__ uint32_t hash_slot(int k, int mask) {
 
 // Builds, in shared memory: starts[0..S], adapters[0..S-1], base[0..S] where base is the
 // exclusive prefix of "work items led by segment i".  Segment i leads its group when it is the
-// first non-empty segment of its adapter; its group gets ceil(rows / rmax) items.
+// first non-empty segment of its adapter; its group gets ceil(rows / kRowsMax) items, and
+// gcnt[lead] holds the group's row count.
 // `scratch` (transient) holds slot[S] and the hash table (3 * hash_slots ints).
-static __device__ __forceinline__ void build_schedule(const Params& p, int* starts, int* adapters, int* base,
-                               int* scratch, int* wsum) {
+static __device__ __forceinline__ void build_schedule(const Params& p, int* starts, int* adapters,
+                                                      int* base, int* gcnt, int* scratch,
+                                                      int* wsum) {
   const int tid = threadIdx.x;
   const int S = p.S, HS = p.hash_slots;
   int* slot = scratch;
@@ -352,16 +355,19 @@ static __device__ __forceinline__ void build_schedule(const Params& p, int* star
     slot[i] = h;
   }
   __syncthreads();
-  const int rmax = p.rmax;
   block_exclusive_scan(S, base, wsum, [&](int i) {
     const int h = slot[i];
-    return (h >= 0 && hlead[h] == i) ? (hcnt[h] + rmax - 1) / rmax : 0;
+    const bool lead = h >= 0 && hlead[h] == i;
+    const int rows = lead ? hcnt[h] : 0;
+    gcnt[i] = rows;
+    return (rows + kRowsMax - 1) / kRowsMax;
   });
 }
 
 // One warp: turns item t into {adapter, rows, row ids...} in d (d[0]=k, d[1]=R, d[2..]=rows).
-static __device__ __forceinline__ void decode_item(const Params& p, int t, const int* starts, const int* adapters,
-                            const int* base, int* d) {
+static __device__ __forceinline__ void decode_item(const Params& p, int t, const int* starts,
+                                                   const int* adapters, const int* base,
+                                                   const int* gcnt, int* d) {
   const int lane = threadIdx.x & 31;
   const int S = p.S;
   int lo = 0, hi = S - 1;  // largest i with base[i] <= t
@@ -371,8 +377,8 @@ static __device__ __forceinline__ void decode_item(const Params& p, int t, const
   }
   const int lead = lo;
   const int k = adapters[lead];
-  const int p_lo = (t - base[lead]) * p.rmax;
-  const int p_hi = p_lo + p.rmax;
+  const int p_lo = (t - base[lead]) * kRowsMax;
+  const int p_hi = min(p_lo + kRowsMax, gcnt[lead]);  // stop once the chunk's rows are found
   int pos = 0;
   for (int jb = lead; jb < S && pos < p_hi; jb += 32) {
     const int j = jb + lane;
@@ -400,20 +406,19 @@ static __device__ __forceinline__ void decode_item(const Params& p, int t, const
 template <typename T, int R, int MODE>
 struct Kernel {
   using E = Elem<T>;
-  using Ch = Chunking<T, R, MODE>;
+  using Walk = StageWalk<R, MODE>;
   static constexpr int kVec = E::kVec;
   static constexpr int kCpr = R / kVec;  // 16-byte chunks per A row
   static constexpr int kKLanes = kConsumers / kCpr;
   static constexpr int kEb = sizeof(T);
   static_assert(kCpr >= 1 && kCpr <= 32, "rank / vector width");
 
-  // Shared-memory map with every address precomputed once per CTA (values, not a pointer to
-  // the parameter block: the device functions are inlined and keep these in registers).
+  // Shared-memory map with every address precomputed once per CTA.
   struct Smem {
     uint32_t bars_u32;  // barrier 0
     uint8_t* ring;      // stage 0
     uint32_t ring_u32;
-    int nst, stage_bytes, desc_ints, vpart_floats;
+    int nst, stage_bytes, desc_ints;
     int* desc_p;
     float *vpart_p, *vfull_p, *red_p;
     __device__ __forceinline__ void init(uint8_t* smem, const Params& p) {
@@ -423,7 +428,6 @@ struct Kernel {
       nst = p.nstages;
       stage_bytes = p.stage_bytes;
       desc_ints = p.desc_ints;
-      vpart_floats = p.rmax * R;
       desc_p = reinterpret_cast<int*>(smem + p.off_desc);
       vpart_p = reinterpret_cast<float*>(smem + p.off_vpart);
       vfull_p = reinterpret_cast<float*>(smem + p.off_vfull);
@@ -442,126 +446,133 @@ struct Kernel {
       return ring_u32 + static_cast<uint32_t>(s) * static_cast<uint32_t>(stage_bytes);
     }
     __device__ __forceinline__ int* desc(int b) const { return desc_p + b * desc_ints; }
-    __device__ __forceinline__ float* vpart(int b) const { return vpart_p + b * vpart_floats; }
+    __device__ __forceinline__ float* vpart(int b) const { return vpart_p + b * kRowsMax * R; }
   };
 
   // The CTAs that share one item.
   struct Group {
-    int size;       // E
-    int m;          // this CTA's member index
-    int gid, ng;    // group index, number of groups
-    int rank0;      // cluster rank of member 0
+    int size;     // E
+    int m;        // this CTA's member index
+    int gid, ng;  // group index, number of groups
+    int rank0;    // cluster rank of member 0
   };
 
   // ------------------------------------------------------------------ producer warp ----
-  // Activation part of stage `idx` of the item (x columns of an A chunk, the y rows of an
-  // expand pass, the v rows), onto the stage's full barrier.
+  // Activation part of a stage (x columns of an A chunk, y rows of a pass, v rows) into slot s.
   __device__ __forceinline__ static void issue_acts(const Params& p, const Smem& sm,
-                                                    const Waiter& w, const Ch& ch, int idx, int s,
-                                                    const int* d, int nrow, int k0, int n0,
+                                                    const Waiter& w, const MemberPlan& mp,
+                                                    const Walk& st, int s, const int* d, int nrow,
                                                     uint64_t pol) {
     const int lane = threadIdx.x & 31;
-    const typename Ch::Loc l = ch.locate(p, idx);
-    if (l.kind == kChunkA) {
+    if (st.kind == kChunkA) {
       const uint32_t xo = static_cast<uint32_t>(p.kb * R * kEb);
       for (int i = lane; i < nrow && w.ok(); i += 32)
         bulk_g2s(sm.stage_u32(s) + xo + static_cast<uint32_t>(i * p.kb * kEb),
-                 static_cast<const T*>(p.x) + static_cast<size_t>(d[2 + i]) * p.h_in + k0 +
-                     l.a * ch.kbe,
-                 l.rows * kEb, sm.full(s), pol);
-    } else if (l.kind == kChunkY) {
+                 static_cast<const T*>(p.x) + static_cast<size_t>(d[2 + i]) * p.h_in + mp.k0 +
+                     st.a * mp.kbe,
+                 static_cast<uint32_t>(st.rows * kEb), sm.full(s), pol);
+    } else if (st.kind == kChunkY) {
       for (int i = lane; i < nrow && w.ok(); i += 32)
-        bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(i * l.wdt * kEb),
-                 static_cast<const T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.h_out + n0 +
-                     l.pass * p.wmax,
-                 l.wdt * kEb, sm.full(s), pol);
-    } else if (l.kind == kChunkV) {
+        bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(i * st.wdt * kEb),
+                 static_cast<const T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.h_out + mp.n0 +
+                     st.pass * mp.w_full,
+                 static_cast<uint32_t>(st.wdt * kEb), sm.full(s), pol);
+    } else if (st.kind == kChunkV) {
       for (int i = lane; i < nrow && w.ok(); i += 32)
         bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(i * R * 4),
                  p.v_in + static_cast<size_t>(d[2 + i]) * R, R * 4, sm.full(s), pol);
     }
   }
 
-  // Stage `idx` of the item into ring slot g % nst: wait for the slot, announce the bytes
-  // (weights and activations), copy the weights, and the activations when `acts`.
+  // One stage into the current ring slot: wait for the slot (after the first round), announce
+  // the stage's bytes (weights and activations), copy the weights, and the activations when
+  // `acts`.
   __device__ __forceinline__ static void issue_stage(const Params& p, const Smem& sm,
-                                                     const Waiter& w, const Ch& ch, int idx,
-                                                     uint32_t g, const T* Ak, const T* Bk,
-                                                     const int* d, int nrow, int k0, int n0,
-                                                     bool acts, uint64_t pol_w, uint64_t pol_a) {
+                                                     const Waiter& w, const MemberPlan& mp,
+                                                     const Walk& st, const RingPos& rp,
+                                                     const T* Ak, const T* Bk, const int* d,
+                                                     int nrow, bool acts, uint64_t pol_w,
+                                                     uint64_t pol_a) {
     const int lane = threadIdx.x & 31;
-    const int NST = sm.nst;
-    const int s = static_cast<int>(g % static_cast<uint32_t>(NST));
-    const typename Ch::Loc l = ch.locate(p, idx);
+    const int s = rp.s;
     uint32_t bytes;
-    if (l.kind == kChunkA)
-      bytes = static_cast<uint32_t>((R + nrow) * l.rows * kEb);
-    else if (l.kind == kChunkB)
-      bytes = static_cast<uint32_t>(l.rows * l.wdt * kEb);
-    else if (l.kind == kChunkY)
-      bytes = static_cast<uint32_t>(nrow * l.wdt * kEb);
+    if (st.kind == kChunkA)
+      bytes = static_cast<uint32_t>((R + nrow) * st.rows * kEb);
+    else if (st.kind == kChunkB)
+      bytes = static_cast<uint32_t>(st.rows * st.wdt * kEb);
+    else if (st.kind == kChunkY)
+      bytes = static_cast<uint32_t>(nrow * st.wdt * kEb);
     else
       bytes = static_cast<uint32_t>(nrow * R * 4);
     if (lane == 0) {
-      if (g >= static_cast<uint32_t>(NST)) w.wait<false>(sm.empty(s), ((g / NST) - 1) & 1);
+      if (rp.wrapped) w.wait<false>(sm.empty(s), rp.par ^ 1u);
       mbar_arrive_expect_tx(sm.full(s), w.ok() ? bytes : 0u);
-      if (l.kind == kChunkA && w.ok())
-        bulk_g2s(sm.stage_u32(s), Ak + static_cast<size_t>(k0 + l.a * ch.kbe) * R,
-                 static_cast<uint32_t>(l.rows * R * kEb), sm.full(s), pol_w);
+      if (st.kind == kChunkA && w.ok())
+        bulk_g2s(sm.stage_u32(s), Ak + static_cast<size_t>(mp.k0 + st.a * mp.kbe) * R,
+                 static_cast<uint32_t>(st.rows * R * kEb), sm.full(s), pol_w);
     }
     __syncwarp();
-    if (l.kind == kChunkB) {
-      const int stride = Ch::row_stride(l.wdt);
-      for (int rr = lane; rr < l.rows && w.ok(); rr += 32)
+    if (st.kind == kChunkB) {
+      const int stride = b_row_stride(st.wdt, kEb);
+      const T* src = Bk + static_cast<size_t>(st.c0) * p.h_out + mp.n0 + st.pass * mp.w_full;
+      for (int rr = lane; rr < st.rows && w.ok(); rr += 32)
         bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(rr * stride),
-                 Bk + static_cast<size_t>(l.c0 + rr) * p.h_out + n0 + l.pass * p.wmax,
-                 static_cast<uint32_t>(l.wdt * kEb), sm.full(s), pol_w);
+                 src + static_cast<size_t>(rr) * p.h_out, static_cast<uint32_t>(st.wdt * kEb),
+                 sm.full(s), pol_w);
     }
-    if (acts) issue_acts(p, sm, w, ch, idx, s, d, nrow, k0, n0, pol_a);
+    if (acts) issue_acts(p, sm, w, mp, st, s, d, nrow, pol_a);
     __syncwarp();
   }
 
   __device__ __forceinline__ static void producer(const Params& p, const Smem& sm,
                                                   const Waiter& w, const Group& grp,
-                                                  const int* starts, const int* adapters,
-                                                  const int* base, int n_my, int k0, int n0,
-                                                  const Ch& ch) {
+                                                  const MemberPlan& mp, const int* starts,
+                                                  const int* adapters, const int* base,
+                                                  const int* gcnt, int n_my) {
     const int lane = threadIdx.x & 31;
     const uint64_t pol_w = policy_evict_first();  // weights: streamed once per call
     const uint64_t pol_a = policy_evict_last();   // activations: reused by the group
     const int NST = sm.nst;
-    uint32_t g = 0;  // ring stage counter
+    RingPos rp;
+    rp.init();
     bool prior_done = false;
     for (int li = 0; li < n_my; ++li) {
       const int b = li & 1;
       if (li >= 2 && lane == 0) w.wait<false>(sm.fixed(kDescFree0 + b), ((li >> 1) - 1) & 1);
       __syncwarp();
       int* d = sm.desc(b);
-      decode_item(p, grp.gid + li * grp.ng, starts, adapters, base, d);
+      decode_item(p, grp.gid + li * grp.ng, starts, adapters, base, gcnt, d);
       if (lane == 0) mbar_arrive(sm.fixed(kDescFull0 + b));
       const int k = d[0];
-      const int nrow = min(max(d[1], 0), p.rmax);
+      const int nrow = min(max(d[1], 0), kRowsMax);
       const T* Ak = nullptr;
       const T* Bk = nullptr;
       if (MODE != kExpand)
         Ak = static_cast<const T*>(p.A_ptrs[k]) + static_cast<size_t>(p.layer) * p.h_in * R;
       if (MODE != kShrink)
         Bk = static_cast<const T*>(p.B_ptrs[k]) + static_cast<size_t>(p.layer) * R * p.h_out;
-      for (int idx = 0; idx < ch.total; ++idx, ++g) {
-        if (!prior_done && g >= static_cast<uint32_t>(NST)) {
-          // The ring is full of weights that do not depend on the previous kernel of the
-          // stream; before any slot is reused, wait for that kernel and add the activations
-          // of the stages already issued (item 0 started at slot 0).
+      Walk st;
+      st.first(mp);
+      int issued = 0;
+      for (; st.kind != kChunkEnd; st.next(mp), rp.next(NST), ++issued) {
+        if (!prior_done && rp.wrapped) {
+          // The ring is full of weights, which do not depend on the previous kernel of the
+          // stream; before a slot is reused, wait for that kernel and add the activations of
+          // the stages already issued (item 0 started at slot 0).
           pdl_wait_prior();
           prior_done = true;
-          for (int j = 0; j < idx; ++j) issue_acts(p, sm, w, ch, j, j, d, nrow, k0, n0, pol_a);
+          Walk rw;
+          rw.first(mp);
+          for (int q = 0; q < issued; ++q, rw.next(mp)) issue_acts(p, sm, w, mp, rw, q, d, nrow, pol_a);
         }
-        issue_stage(p, sm, w, ch, idx, g, Ak, Bk, d, nrow, k0, n0, prior_done, pol_w, pol_a);
+        issue_stage(p, sm, w, mp, st, rp, Ak, Bk, d, nrow, prior_done, pol_w, pol_a);
       }
       if (!prior_done) {
         pdl_wait_prior();
         prior_done = true;
-        for (int j = 0; j < ch.total; ++j) issue_acts(p, sm, w, ch, j, j, d, nrow, k0, n0, pol_a);
+        Walk rw;
+        rw.first(mp);
+        for (int q = 0; q < issued; ++q, rw.next(mp)) issue_acts(p, sm, w, mp, rw, q, d, nrow, pol_a);
       }
     }
     if (!prior_done) pdl_wait_prior();
@@ -570,9 +581,9 @@ struct Kernel {
   // --------------------------------------------------------------- consumer warps ----
   template <int RB>
   __device__ __forceinline__ static void consume_item(const Params& p, const Smem& sm,
-                                                      const Waiter& w, const Group& grp, int li,
-                                                      bool last, uint32_t& g, const int* d,
-                                                      int nrow, int n0, const Ch& ch) {
+                                                      const Waiter& w, const Group& grp,
+                                                      const MemberPlan& mp, int li, bool last,
+                                                      RingPos& rp, const int* d, int nrow) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NST = sm.nst;
     float acc[RB][kVec];
@@ -580,28 +591,27 @@ struct Kernel {
 
     if (MODE == kExpand) {
       // ------------------------------------------------------------- v rows of the item
-      const int s = static_cast<int>(g % static_cast<uint32_t>(NST));
-      w.wait<false>(sm.full(s), (g / NST) & 1);
-      const float* vs = reinterpret_cast<const float*>(sm.stage(s));
+      w.wait<false>(sm.full(rp.s), rp.par);
+      const float* vs = reinterpret_cast<const float*>(sm.stage(rp.s));
       for (int t = tid; t < nrow * R; t += kConsumers) vfull[t] = p.scale * vs[t];
       named_bar(1, kConsumers);
       __syncwarp();
-      if (lane == 0) mbar_arrive(sm.empty(s));
-      ++g;
+      if (lane == 0) mbar_arrive(sm.empty(rp.s));
+      rp.next(NST);
     } else {
       // ----------------------------------------------------------- shrink (split-K)
 #pragma unroll
       for (int i = 0; i < RB; ++i)
 #pragma unroll
         for (int e = 0; e < kVec; ++e) acc[i][e] = 0.f;
-      const int cc = tid % kCpr, kl = tid / kCpr;
+      const int cc = tid % kCpr, kl = tid / kCpr;  // compile-time divisors
       const int xrow = p.kb * kEb;
-      for (int j = 0; j < ch.nA; ++j, ++g) {
-        const int s = static_cast<int>(g % static_cast<uint32_t>(NST));
-        w.wait<false>(sm.full(s), (g / NST) & 1);
-        const int rows = min(ch.kbe, ch.kc - j * ch.kbe);
-        const uint8_t* st = sm.stage(s);
-        const uint8_t* xs = st + p.kb * R * kEb;
+      const int xoff = p.kb * R * kEb;
+      int rows = min(mp.kbe, mp.kc);
+      for (int j = 0; j < mp.nA; ++j, rp.next(NST), rows = min(mp.kbe, mp.kc - j * mp.kbe)) {
+        w.wait<false>(sm.full(rp.s), rp.par);
+        const uint8_t* st = sm.stage(rp.s);
+        const uint8_t* xs = st + xoff;
         for (int kk = kl; kk < rows; kk += kKLanes) {
           float a[kVec];
           E::load16(st + (kk * R + cc * kVec) * kEb, a);
@@ -613,7 +623,7 @@ struct Kernel {
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(sm.empty(s));
+        if (lane == 0) mbar_arrive(sm.empty(rp.s));
       }
       // reduce over the k-lanes of the warp (lanes with equal cc), then over warps
 #pragma unroll
@@ -628,14 +638,14 @@ struct Kernel {
         for (int i = 0; i < RB; ++i)
 #pragma unroll
           for (int e = 0; e < kVec; ++e)
-            red[(warp * p.rmax + i) * R + lane * kVec + e] = acc[i][e];
+            red[(warp * kRowsMax + i) * R + lane * kVec + e] = acc[i][e];
       }
       named_bar(1, kConsumers);
       if (grp.size == 1) {
         for (int t = tid; t < nrow * R; t += kConsumers) {
           float s = 0.f;
 #pragma unroll
-          for (int ww = 0; ww < kConsumerWarps; ++ww) s += red[ww * p.rmax * R + t];
+          for (int ww = 0; ww < kConsumerWarps; ++ww) s += red[ww * kRowsMax * R + t];
           if (MODE == kFused) {
             vfull[t] = s * p.scale;
           } else if (w.ok()) {
@@ -648,7 +658,7 @@ struct Kernel {
         for (int t = tid; t < nrow * R; t += kConsumers) {
           float s = 0.f;
 #pragma unroll
-          for (int ww = 0; ww < kConsumerWarps; ++ww) s += red[ww * p.rmax * R + t];
+          for (int ww = 0; ww < kConsumerWarps; ++ww) s += red[ww * kRowsMax * R + t];
           vp[t] = s;
         }
         named_bar(1, kConsumers);
@@ -676,25 +686,26 @@ struct Kernel {
 
     if (MODE != kShrink) {
       // ------------------------------------------------------- expand over the N slice
-      for (int pass = 0; pass < ch.passes; ++pass) {
-        const int wdt = ch.pass_width(p, pass);
-        const int cb = ch.pass_rows(p, wdt);
-        const int stride = Ch::row_stride(wdt);
-        const int nch = wdt / kVec;
-        int cl_n = 1;
-        while (cl_n < 32 && nch * cl_n * 2 <= kConsumers) cl_n <<= 1;
-        const int my_ch = tid / cl_n, cl = tid % cl_n;
+      for (int pass = 0; pass < mp.passes; ++pass) {
+        const bool lastp = pass == mp.passes - 1;
+        const int wdt = lastp ? mp.w_last : mp.w_full;
+        const int cb = lastp ? mp.cb_last : mp.cb_full;
+        const int stride = b_row_stride(wdt, kEb);
+        const int nch = wdt / kVec;  // compile-time divisor
+        int lgc = 0;  // log2 of the lanes that share one 16-byte column chunk
+        while (lgc < 5 && (nch << (lgc + 1)) <= kConsumers) ++lgc;
+        const int cl_n = 1 << lgc;
+        const int my_ch = tid >> lgc, cl = tid & (cl_n - 1);
         const bool active = my_ch < nch;
 #pragma unroll
         for (int i = 0; i < RB; ++i)
 #pragma unroll
           for (int e = 0; e < kVec; ++e) acc[i][e] = 0.f;
-        for (int c0 = 0; c0 < R; c0 += cb, ++g) {
-          const int s = static_cast<int>(g % static_cast<uint32_t>(NST));
+        for (int c0 = 0; c0 < R; c0 += cb, rp.next(NST)) {
           const int rows = min(cb, R - c0);
-          w.wait<false>(sm.full(s), (g / NST) & 1);
+          w.wait<false>(sm.full(rp.s), rp.par);
           if (active) {
-            const uint8_t* st = sm.stage(s) + my_ch * 16;
+            const uint8_t* st = sm.stage(rp.s) + my_ch * 16;
             for (int c = cl; c < rows; c += cl_n) {
               float bv[kVec];
               E::load16(st + c * stride, bv);
@@ -707,19 +718,19 @@ struct Kernel {
             }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(sm.empty(s));
+          if (lane == 0) mbar_arrive(sm.empty(rp.s));
         }
         for (int o = 1; o < cl_n; o <<= 1)
 #pragma unroll
           for (int i = 0; i < RB; ++i)
 #pragma unroll
             for (int e = 0; e < kVec; ++e) acc[i][e] += __shfl_xor_sync(0xffffffffu, acc[i][e], o);
-        // the pass's y rows: add, round once, store
-        const int s = static_cast<int>(g % static_cast<uint32_t>(NST));
-        w.wait<false>(sm.full(s), (g / NST) & 1);
-        if (active && cl == 0 && w.ok()) {
+        // The pass's y rows: add, round once into the y stage, then bulk-store the rows (async
+        // proxy: the release arrives that follow do not wait for these global writes).
+        w.wait<false>(sm.full(rp.s), rp.par);
+        uint8_t* ys = sm.stage(rp.s);
+        if (active && cl == 0) {
           const int col = my_ch * kVec;
-          const uint8_t* ys = sm.stage(s);
 #pragma unroll
           for (int i = 0; i < RB; ++i) {
             if (i < nrow) {
@@ -727,15 +738,25 @@ struct Kernel {
               E::load16(ys + (i * wdt + col) * kEb, yo);
 #pragma unroll
               for (int e = 0; e < kVec; ++e) yo[e] += acc[i][e];
-              E::store16(static_cast<T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.h_out +
-                             n0 + pass * p.wmax + col,
-                         yo);
+              E::store16(ys + (i * wdt + col) * kEb, yo);
             }
           }
         }
+        fence_proxy_async();  // generic-proxy writes above, read by the bulk store below
+        named_bar(1, kConsumers);
+        if (tid == 0) {
+          if (w.ok()) {
+            for (int i = 0; i < nrow; ++i)
+              bulk_s2g(static_cast<T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.h_out + mp.n0 +
+                           pass * mp.w_full,
+                       smem_addr(ys + i * wdt * kEb), static_cast<uint32_t>(wdt * kEb));
+            bulk_commit();
+          }
+          bulk_wait_read();  // the stage may be refilled once the stores have read it
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(sm.empty(s));
-        ++g;
+        if (lane == 0) mbar_arrive(sm.empty(rp.s));
+        rp.next(NST);
       }
     }
     __syncwarp();
@@ -743,20 +764,21 @@ struct Kernel {
   }
 
   __device__ __forceinline__ static void consumer(const Params& p, const Smem& sm,
-                                                  const Waiter& w, const Group& grp, int n_my,
-                                                  int n0, const Ch& ch) {
-    uint32_t g = 0;
+                                                  const Waiter& w, const Group& grp,
+                                                  const MemberPlan& mp, int n_my) {
+    RingPos rp;
+    rp.init();
     for (int li = 0; li < n_my; ++li) {
       w.wait<false>(sm.fixed(kDescFull0 + (li & 1)), (li >> 1) & 1);
       const int* d = sm.desc(li & 1);
-      const int nrow = min(max(d[1], 0), p.rmax);
+      const int nrow = min(max(d[1], 0), kRowsMax);
       const bool last = li == n_my - 1;
       if (nrow <= 1)
-        consume_item<1>(p, sm, w, grp, li, last, g, d, nrow, n0, ch);
+        consume_item<1>(p, sm, w, grp, mp, li, last, rp, d, nrow);
       else if (nrow <= 2)
-        consume_item<2>(p, sm, w, grp, li, last, g, d, nrow, n0, ch);
+        consume_item<2>(p, sm, w, grp, mp, li, last, rp, d, nrow);
       else
-        consume_item<kRowsMax>(p, sm, w, grp, li, last, g, d, nrow, n0, ch);
+        consume_item<kRowsMax>(p, sm, w, grp, mp, li, last, rp, d, nrow);
     }
     // keep every thread's cluster barrier sequence: wait #1, arrive #2 (done per item above
     // when the group exchanges partial products)
@@ -776,6 +798,7 @@ struct Kernel {
     int* starts = reinterpret_cast<int*>(smem + p.off_tab);
     int* adapters = starts + (p.S + 1);
     int* base = adapters + p.S;
+    int* gcnt = base + (p.S + 1);
 
     if (tid == 0) {
       for (int s = 0; s < p.nstages; ++s) {
@@ -789,7 +812,7 @@ struct Kernel {
       mbar_init(sm.fixed(kNever), 1);
       ctl[0] = 0;
     }
-    build_schedule(p, starts, adapters, base, reinterpret_cast<int*>(smem + p.off_ring),
+    build_schedule(p, starts, adapters, base, gcnt, reinterpret_cast<int*>(smem + p.off_ring),
                    ctl + 4);
     // Group size E: as large as the launch cluster allows while every item still gets its own
     // group of CTAs (few items: split each across CTAs; many items: one CTA each, no exchange).
@@ -798,10 +821,11 @@ struct Kernel {
     Group grp;
     grp.size = 1;
     while (grp.size * 2 <= p.C && n_items * grp.size * 2 <= N) grp.size *= 2;
-    grp.m = static_cast<int>(blockIdx.x) % grp.size;
-    grp.gid = static_cast<int>(blockIdx.x) / grp.size;
-    grp.ng = N / grp.size;
-    grp.rank0 = (static_cast<int>(blockIdx.x) % p.C) / grp.size * grp.size;
+    const int lg = grp.size == 1 ? 0 : (grp.size == 2 ? 1 : 2);
+    grp.m = static_cast<int>(blockIdx.x) & (grp.size - 1);
+    grp.gid = static_cast<int>(blockIdx.x) >> lg;
+    grp.ng = N >> lg;
+    grp.rank0 = (static_cast<int>(blockIdx.x) & (p.C - 1)) & ~(grp.size - 1);
     if (tid == 0) {
       mbar_init(sm.fixed(kVReady0), grp.size);
       mbar_init(sm.fixed(kVReady1), grp.size);
@@ -818,20 +842,16 @@ struct Kernel {
     if (p.inject_stall) w.wait<false>(sm.fixed(kNever), 0);  // nothing completes it
 
     const int n_my = (grp.gid < n_items) ? (n_items - grp.gid + grp.ng - 1) / grp.ng : 0;
-    int k0 = 0, k1 = 0, n0 = 0, n1 = 0;
-    slice_of(p.h_in, grp.size, grp.m, k0, k1);
-    slice_of(p.h_out, grp.size, grp.m, n0, n1);
-    Ch ch;
-    ch.init(p, k1 - k0, n1 - n0);
+    const MemberPlan& mp = p.plan[(grp.size - 1) + grp.m];
 
     if (warp == kConsumerWarps) {
-      producer(p, sm, w, grp, starts, adapters, base, n_my, k0, n0, ch);
+      producer(p, sm, w, grp, mp, starts, adapters, base, gcnt, n_my);
       if (MODE != kExpand) {
         cluster_wait();
         cluster_arrive();
       }
     } else {
-      consumer(p, sm, w, grp, n_my, n0, ch);
+      consumer(p, sm, w, grp, mp, n_my);
     }
     __syncthreads();
     if (!w.ok()) {  // gave up: let every bulk copy already issued land before the CTA exits

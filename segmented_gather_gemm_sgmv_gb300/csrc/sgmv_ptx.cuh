@@ -82,6 +82,20 @@ static __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, u
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
+// Own shared memory -> global (async proxy); completion tracked by bulk groups of the issuing
+// thread, so later release operations of that thread do not wait for these writes.
+static __device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+static __device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until the shared-memory sources of all committed bulk stores have been read.
+static __device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 static __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
