@@ -186,6 +186,15 @@ int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* sme
   off += 4 * rmax * pb.r;
   p.off_red = static_cast<uint32_t>(off);
   off += 4 * sgmv::kConsumerWarps * rmax * pb.r;
+  // producer's stage-descriptor table (16 bytes per stage of the longest member plan)
+  int max_total = 0;
+  for (int E = 1, slot = 0; E <= C; E <<= 1)
+    for (int m = 0; m < E; ++m, ++slot) {
+      p.plan[slot] = member_plan(pb, E, m, kb, wmax, stage_bytes, eb);
+      max_total = std::max(max_total, p.plan[slot].total);
+    }
+  p.off_stab = static_cast<uint32_t>(up(off, 16));
+  off = p.off_stab + 16 * static_cast<size_t>(max_total);
   p.off_ring = static_cast<uint32_t>(up(off, 1024));
   // As many ring stages as the budget holds (the ring also hosts the transient hash table).
   const size_t scratch = 4 * (static_cast<size_t>(pb.S) + 3 * hs);
@@ -203,9 +212,6 @@ int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* sme
   p.stage_bytes = stage_bytes;
   p.kb = kb;
   p.hash_slots = hs;
-  int slot = 0;
-  for (int E = 1; E <= C; E <<= 1)
-    for (int m = 0; m < E; ++m) p.plan[slot++] = member_plan(pb, E, m, kb, wmax, stage_bytes, eb);
   *smem_out = off;
   return SGMV_OK;
 }

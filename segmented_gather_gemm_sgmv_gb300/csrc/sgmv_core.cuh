@@ -84,7 +84,8 @@ struct Params {
   int32_t stage_bytes;  // bytes per ring stage
   int32_t kb;           // x-row stride (elements) inside an A stage (>= every kbe)
   int32_t hash_slots;   // power of two > 1.5*S
-  uint32_t off_bars, off_ctl, off_desc, off_tab, off_vpart, off_vfull, off_red, off_ring;
+  uint32_t off_bars, off_ctl, off_desc, off_tab, off_vpart, off_vfull, off_red, off_stab,
+      off_ring;
   int32_t desc_ints;
   uint64_t wait_limit_ns;
   int32_t inject_stall;
@@ -97,6 +98,16 @@ struct Elem;
 template <>
 struct Elem<float> {
   static constexpr int kVec = 4;  // elements per 16 bytes
+  __device__ static __forceinline__ void lds(uint32_t a, float (&o)[4]) {
+    const uint4 v = lds128(a);
+    o[0] = __uint_as_float(v.x); o[1] = __uint_as_float(v.y);
+    o[2] = __uint_as_float(v.z); o[3] = __uint_as_float(v.w);
+  }
+  __device__ static __forceinline__ float lds1(uint32_t a) { return __uint_as_float(lds32(a)); }
+  __device__ static __forceinline__ void sts(uint32_t a, const float (&o)[4]) {
+    sts128(a, make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                         __float_as_uint(o[3])));
+  }
   __device__ static __forceinline__ void load16(const void* p, float (&o)[4]) {
     const float4 v = *reinterpret_cast<const float4*>(p);
     o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
@@ -111,6 +122,29 @@ struct Elem<float> {
 template <>
 struct Elem<__half> {
   static constexpr int kVec = 8;
+  __device__ static __forceinline__ void lds(uint32_t a, float (&o)[8]) {
+    const uint4 v = lds128(a);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      o[2 * i] = f.x;
+      o[2 * i + 1] = f.y;
+    }
+  }
+  __device__ static __forceinline__ float lds1(uint32_t a) {
+    const unsigned short h = static_cast<unsigned short>(lds16(a));
+    return __half2float(*reinterpret_cast<const __half*>(&h));
+  }
+  __device__ static __forceinline__ void sts(uint32_t a, const float (&o)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(o[2 * i], o[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    sts128(a, make_uint4(w[0], w[1], w[2], w[3]));
+  }
   __device__ static __forceinline__ void load16(const void* p, float (&o)[8]) {
     const uint4 v = *reinterpret_cast<const uint4*>(p);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -137,6 +171,27 @@ struct Elem<__half> {
 template <>
 struct Elem<__nv_bfloat16> {
   static constexpr int kVec = 8;
+  __device__ static __forceinline__ void lds(uint32_t a, float (&o)[8]) {
+    const uint4 v = lds128(a);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // bf16 -> fp32 is exact: the bf16 bits are the high half
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static __forceinline__ float lds1(uint32_t a) {
+    return __uint_as_float(lds16(a) << 16);
+  }
+  __device__ static __forceinline__ void sts(uint32_t a, const float (&o)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    sts128(a, make_uint4(w[0], w[1], w[2], w[3]));
+  }
   __device__ static __forceinline__ void load16(const void* p, float (&o)[8]) {
     const uint4 v = *reinterpret_cast<const uint4*>(p);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -458,81 +513,121 @@ struct Kernel {
   };
 
   // ------------------------------------------------------------------ producer warp ----
+  // Stage descriptors of one item: {kind | rows << 4, offset, column, width}.  A: offset = first
+  // h_in element of the chunk; B: offset = first B row, column = first h_out column, width =
+  // window width; Y: column, width.  Built by the 32 producer lanes in parallel so that the issue
+  // loop is a few instructions per stage.
+  __device__ __forceinline__ static void build_table(const MemberPlan& mp, int4* tab) {
+    const int lane = threadIdx.x & 31;
+    for (int t = lane; t < mp.total; t += 32) {
+      int u = t;
+      int4 e = make_int4(kChunkV, 0, 0, 0);
+      if (MODE == kExpand) --u;
+      if (u >= 0) {
+        if (u < mp.nA) {
+          const int rows = min(mp.kbe, mp.kc - u * mp.kbe);
+          e = make_int4(kChunkA | (rows << 4), mp.k0 + u * mp.kbe, 0, 0);
+        } else {
+          u -= mp.nA;
+          const int per = mp.nb_full + 1, nfull = mp.passes - 1;
+          int pass, jj, w, cb, nb;
+          if (u < nfull * per) {
+            pass = u / per;
+            jj = u - pass * per;
+            w = mp.w_full;
+            cb = mp.cb_full;
+            nb = mp.nb_full;
+          } else {
+            pass = nfull;
+            jj = u - nfull * per;
+            w = mp.w_last;
+            cb = mp.cb_last;
+            nb = mp.nb_last;
+          }
+          const int col = mp.n0 + pass * mp.w_full;
+          if (jj < nb) {
+            const int c0 = jj * cb;
+            e = make_int4(kChunkB | (min(cb, R - c0) << 4), c0, col, w);
+          } else {
+            e = make_int4(kChunkY, 0, col, w);
+          }
+        }
+      }
+      tab[t] = e;
+    }
+    __syncwarp();
+  }
+
   // Activation part of a stage (x columns of an A chunk, y rows of a pass, v rows) into slot s.
-  __device__ __forceinline__ static void issue_acts(const Params& p, const Smem& sm,
-                                                    const Waiter& w, const MemberPlan& mp,
-                                                    const Walk& st, int s, const int* d, int nrow,
+  __device__ __forceinline__ static void issue_acts(const Params& p, const Smem& sm, bool ok,
+                                                    int4 e, int s, const int* d, int nrow,
                                                     uint64_t pol) {
     const int lane = threadIdx.x & 31;
-    if (st.kind == kChunkA) {
-      const uint32_t xo = static_cast<uint32_t>(p.kb * R * kEb);
-      for (int i = lane; i < nrow && w.ok(); i += 32)
-        bulk_g2s(sm.stage_u32(s) + xo + static_cast<uint32_t>(i * p.kb * kEb),
-                 static_cast<const T*>(p.x) + static_cast<size_t>(d[2 + i]) * p.h_in + mp.k0 +
-                     st.a * mp.kbe,
-                 static_cast<uint32_t>(st.rows * kEb), sm.full(s), pol);
-    } else if (st.kind == kChunkY) {
-      for (int i = lane; i < nrow && w.ok(); i += 32)
-        bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(i * st.wdt * kEb),
-                 static_cast<const T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.h_out + mp.n0 +
-                     st.pass * mp.w_full,
-                 static_cast<uint32_t>(st.wdt * kEb), sm.full(s), pol);
-    } else if (st.kind == kChunkV) {
-      for (int i = lane; i < nrow && w.ok(); i += 32)
-        bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(i * R * 4),
-                 p.v_in + static_cast<size_t>(d[2 + i]) * R, R * 4, sm.full(s), pol);
+    if (!ok || lane >= nrow) return;
+    const int kind = e.x & 15;
+    const int row = d[2 + lane];
+    if (kind == kChunkA) {
+      const int rows = e.x >> 4;
+      bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>((p.kb * R + lane * p.kb) * kEb),
+               static_cast<const T*>(p.x) + static_cast<size_t>(row) * p.h_in + e.y,
+               static_cast<uint32_t>(rows * kEb), sm.full(s), pol);
+    } else if (kind == kChunkY) {
+      bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(lane * e.w * kEb),
+               static_cast<const T*>(p.y) + static_cast<size_t>(row) * p.h_out + e.z,
+               static_cast<uint32_t>(e.w * kEb), sm.full(s), pol);
+    } else if (kind == kChunkV) {
+      bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(lane * R * 4),
+               p.v_in + static_cast<size_t>(row) * R, R * 4, sm.full(s), pol);
     }
   }
 
   // One stage into the current ring slot: wait for the slot (after the first round), announce
-  // the stage's bytes (weights and activations), copy the weights, and the activations when
-  // `acts`.
+  // its bytes (weights and activations), copy the weights, and the activations when `acts`.
   __device__ __forceinline__ static void issue_stage(const Params& p, const Smem& sm,
-                                                     const Waiter& w, const MemberPlan& mp,
-                                                     const Walk& st, const RingPos& rp,
+                                                     const Waiter& w, int4 e, const RingPos& rp,
                                                      const T* Ak, const T* Bk, const int* d,
                                                      int nrow, bool acts, uint64_t pol_w,
                                                      uint64_t pol_a) {
     const int lane = threadIdx.x & 31;
     const int s = rp.s;
-    uint32_t bytes;
-    if (st.kind == kChunkA)
-      bytes = static_cast<uint32_t>((R + nrow) * st.rows * kEb);
-    else if (st.kind == kChunkB)
-      bytes = static_cast<uint32_t>(st.rows * st.wdt * kEb);
-    else if (st.kind == kChunkY)
-      bytes = static_cast<uint32_t>(nrow * st.wdt * kEb);
-    else
-      bytes = static_cast<uint32_t>(nrow * R * 4);
+    const int kind = e.x & 15, rows = e.x >> 4;
     if (lane == 0) {
       if (rp.wrapped) w.wait<false>(sm.empty(s), rp.par ^ 1u);
-      mbar_arrive_expect_tx(sm.full(s), w.ok() ? bytes : 0u);
-      if (st.kind == kChunkA && w.ok())
-        bulk_g2s(sm.stage_u32(s), Ak + static_cast<size_t>(mp.k0 + st.a * mp.kbe) * R,
-                 static_cast<uint32_t>(st.rows * R * kEb), sm.full(s), pol_w);
+      const bool ok = w.ok();
+      uint32_t bytes;
+      if (kind == kChunkA)
+        bytes = static_cast<uint32_t>((R + nrow) * rows * kEb);
+      else if (kind == kChunkB)
+        bytes = static_cast<uint32_t>(rows * e.w * kEb);
+      else if (kind == kChunkY)
+        bytes = static_cast<uint32_t>(nrow * e.w * kEb);
+      else
+        bytes = static_cast<uint32_t>(nrow * R * 4);
+      mbar_arrive_expect_tx(sm.full(s), ok ? bytes : 0u);
+      if (kind == kChunkA && ok)
+        bulk_g2s(sm.stage_u32(s), Ak + static_cast<size_t>(e.y) * R,
+                 static_cast<uint32_t>(rows * R * kEb), sm.full(s), pol_w);
     }
     __syncwarp();
-    if (st.kind == kChunkB) {
-      const int stride = b_row_stride(st.wdt, kEb);
-      const T* src = Bk + static_cast<size_t>(st.c0) * p.h_out + mp.n0 + st.pass * mp.w_full;
-      for (int rr = lane; rr < st.rows && w.ok(); rr += 32)
-        bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(rr * stride),
-                 src + static_cast<size_t>(rr) * p.h_out, static_cast<uint32_t>(st.wdt * kEb),
-                 sm.full(s), pol_w);
-    }
-    if (acts) issue_acts(p, sm, w, mp, st, s, d, nrow, pol_a);
-    __syncwarp();
+    const bool ok = w.ok();
+    if (kind == kChunkB && ok)
+      for (int rr = lane; rr < rows; rr += 32)  // up to R (64) rows
+        bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(rr * b_row_stride(e.w, kEb)),
+                 Bk + static_cast<size_t>(e.y + rr) * p.h_out + e.z,
+                 static_cast<uint32_t>(e.w * kEb), sm.full(s), pol_w);
+    if (acts) issue_acts(p, sm, ok, e, s, d, nrow, pol_a);
   }
 
   __device__ __forceinline__ static void producer(const Params& p, const Smem& sm,
                                                   const Waiter& w, const Group& grp,
                                                   const MemberPlan& mp, const int* starts,
                                                   const int* adapters, const int* base,
-                                                  const int* gcnt, int n_my) {
+                                                  const int* gcnt, int4* tab, int n_my) {
     const int lane = threadIdx.x & 31;
     const uint64_t pol_w = policy_evict_first();  // weights: streamed once per call
     const uint64_t pol_a = policy_evict_last();   // activations: reused by the group
     const int NST = sm.nst;
+    const int total = mp.total;
     RingPos rp;
     rp.init();
     bool prior_done = false;
@@ -551,28 +646,24 @@ struct Kernel {
         Ak = static_cast<const T*>(p.A_ptrs[k]) + static_cast<size_t>(p.layer) * p.h_in * R;
       if (MODE != kShrink)
         Bk = static_cast<const T*>(p.B_ptrs[k]) + static_cast<size_t>(p.layer) * R * p.h_out;
-      Walk st;
-      st.first(mp);
-      int issued = 0;
-      for (; st.kind != kChunkEnd; st.next(mp), rp.next(NST), ++issued) {
+      if (li == 0) build_table(mp, tab);  // the plan is the same for every item of this CTA
+      for (int t = 0; t < total; ++t, rp.next(NST)) {
         if (!prior_done && rp.wrapped) {
           // The ring is full of weights, which do not depend on the previous kernel of the
           // stream; before a slot is reused, wait for that kernel and add the activations of
           // the stages already issued (item 0 started at slot 0).
           pdl_wait_prior();
           prior_done = true;
-          Walk rw;
-          rw.first(mp);
-          for (int q = 0; q < issued; ++q, rw.next(mp)) issue_acts(p, sm, w, mp, rw, q, d, nrow, pol_a);
+          const bool ok = w.ok();
+          for (int q = 0; q < t; ++q) issue_acts(p, sm, ok, tab[q], q, d, nrow, pol_a);
         }
-        issue_stage(p, sm, w, mp, st, rp, Ak, Bk, d, nrow, prior_done, pol_w, pol_a);
+        issue_stage(p, sm, w, tab[t], rp, Ak, Bk, d, nrow, prior_done, pol_w, pol_a);
       }
       if (!prior_done) {
         pdl_wait_prior();
         prior_done = true;
-        Walk rw;
-        rw.first(mp);
-        for (int q = 0; q < issued; ++q, rw.next(mp)) issue_acts(p, sm, w, mp, rw, q, d, nrow, pol_a);
+        const bool ok = w.ok();
+        for (int q = 0; q < total; ++q) issue_acts(p, sm, ok, tab[q], q, d, nrow, pol_a);
       }
     }
     if (!prior_done) pdl_wait_prior();
@@ -588,6 +679,7 @@ struct Kernel {
     const int NST = sm.nst;
     float acc[RB][kVec];
     float* vfull = sm.vfull_p;
+    const uint32_t vfull_u32 = smem_addr(vfull);
 
     if (MODE == kExpand) {
       // ------------------------------------------------------------- v rows of the item
@@ -610,17 +702,31 @@ struct Kernel {
       int rows = min(mp.kbe, mp.kc);
       for (int j = 0; j < mp.nA; ++j, rp.next(NST), rows = min(mp.kbe, mp.kc - j * mp.kbe)) {
         w.wait<false>(sm.full(rp.s), rp.par);
-        const uint8_t* st = sm.stage(rp.s);
-        const uint8_t* xs = st + xoff;
-        for (int kk = kl; kk < rows; kk += kKLanes) {
-          float a[kVec];
-          E::load16(st + (kk * R + cc * kVec) * kEb, a);
+        const uint32_t st = sm.stage_u32(rp.s);
+        const uint32_t xs = st + xoff;
+        constexpr int U = RB <= 2 ? 4 : 2;  // rows in flight per thread (loads before FMAs)
+        for (int kk0 = kl; kk0 < rows; kk0 += U * kKLanes) {
+          float a[U][kVec], xv[U][RB];
 #pragma unroll
-          for (int i = 0; i < RB; ++i) {
-            const float xv = E::load1(xs + i * xrow + kk * kEb);
+          for (int u = 0; u < U; ++u) {
+            const int kk = kk0 + u * kKLanes;
+            if (kk < rows) {
+              E::lds(st + (kk * R + cc * kVec) * kEb, a[u]);
 #pragma unroll
-            for (int e = 0; e < kVec; ++e) acc[i][e] = fmaf(xv, a[e], acc[i][e]);
+              for (int i = 0; i < RB; ++i) xv[u][i] = E::lds1(xs + i * xrow + kk * kEb);
+            } else {
+#pragma unroll
+              for (int e = 0; e < kVec; ++e) a[u][e] = 0.f;
+#pragma unroll
+              for (int i = 0; i < RB; ++i) xv[u][i] = 0.f;
+            }
           }
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int i = 0; i < RB; ++i)
+#pragma unroll
+              for (int e = 0; e < kVec; ++e) acc[i][e] = fmaf(xv[u][i], a[u][e], acc[i][e]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty(rp.s));
@@ -705,15 +811,24 @@ struct Kernel {
           const int rows = min(cb, R - c0);
           w.wait<false>(sm.full(rp.s), rp.par);
           if (active) {
-            const uint8_t* st = sm.stage(rp.s) + my_ch * 16;
-            for (int c = cl; c < rows; c += cl_n) {
-              float bv[kVec];
-              E::load16(st + c * stride, bv);
+            const uint32_t st = sm.stage_u32(rp.s) + my_ch * 16;
+            for (int c = cl; c < rows; c += 2 * cl_n) {  // two B rows in flight per thread
+              const int c1 = c + cl_n;
+              const bool h1 = c1 < rows;
+              float b0[kVec], b1[kVec];
+              E::lds(st + c * stride, b0);
+              if (h1) {
+                E::lds(st + c1 * stride, b1);
+              } else {
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) b1[e] = 0.f;
+              }
 #pragma unroll
               for (int i = 0; i < RB; ++i) {
-                const float vv = vfull[i * R + c0 + c];
+                const float v0 = __uint_as_float(lds32(vfull_u32 + 4u * (i * R + c0 + c)));
+                const float v1 = h1 ? __uint_as_float(lds32(vfull_u32 + 4u * (i * R + c0 + c1))) : 0.f;
 #pragma unroll
-                for (int e = 0; e < kVec; ++e) acc[i][e] = fmaf(vv, bv[e], acc[i][e]);
+                for (int e = 0; e < kVec; ++e) acc[i][e] = fmaf(v1, b1[e], fmaf(v0, b0[e], acc[i][e]));
               }
             }
           }
@@ -728,17 +843,17 @@ struct Kernel {
         // The pass's y rows: add, round once into the y stage, then bulk-store the rows (async
         // proxy: the release arrives that follow do not wait for these global writes).
         w.wait<false>(sm.full(rp.s), rp.par);
-        uint8_t* ys = sm.stage(rp.s);
+        const uint32_t ys = sm.stage_u32(rp.s);
         if (active && cl == 0) {
           const int col = my_ch * kVec;
 #pragma unroll
           for (int i = 0; i < RB; ++i) {
             if (i < nrow) {
               float yo[kVec];
-              E::load16(ys + (i * wdt + col) * kEb, yo);
+              E::lds(ys + (i * wdt + col) * kEb, yo);
 #pragma unroll
               for (int e = 0; e < kVec; ++e) yo[e] += acc[i][e];
-              E::store16(ys + (i * wdt + col) * kEb, yo);
+              E::sts(ys + (i * wdt + col) * kEb, yo);
             }
           }
         }
@@ -749,7 +864,7 @@ struct Kernel {
             for (int i = 0; i < nrow; ++i)
               bulk_s2g(static_cast<T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.h_out + mp.n0 +
                            pass * mp.w_full,
-                       smem_addr(ys + i * wdt * kEb), static_cast<uint32_t>(wdt * kEb));
+                       ys + static_cast<uint32_t>(i * wdt * kEb), static_cast<uint32_t>(wdt * kEb));
             bulk_commit();
           }
           bulk_wait_read();  // the stage may be refilled once the stores have read it
@@ -845,7 +960,8 @@ struct Kernel {
     const MemberPlan& mp = p.plan[(grp.size - 1) + grp.m];
 
     if (warp == kConsumerWarps) {
-      producer(p, sm, w, grp, mp, starts, adapters, base, gcnt, n_my);
+      producer(p, sm, w, grp, mp, starts, adapters, base, gcnt,
+               reinterpret_cast<int4*>(smem + p.off_stab), n_my);
       if (MODE != kExpand) {
         cluster_wait();
         cluster_arrive();
