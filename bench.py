@@ -167,10 +167,11 @@ def barrier(world):
 class Setup:
     """Device-resident inputs of the workload: pool, NB rotating x/y sets, segment table."""
 
-    def __init__(self, w, device, nbuf=32, seed=0, overlap=True):
+    def __init__(self, w, device, nbuf=32, seed=0, overlap=True, tensor_cores=True):
         import torch
         self.w = w
         self.overlap = overlap
+        self.tensor_cores = tensor_cores
         self.ss, self.sa = workloads.make_segments(w.name, seed)
         self.M = int(self.ss[-1])
         self.A, self.B = workloads.make_pool(w, device, seed=seed + 1)
@@ -190,7 +191,7 @@ class Setup:
         i = step % self.nbuf
         lora_apply(self.y[i], self.x[i], self.A_ptrs, self.B_ptrs, self.d_ss, self.d_sa,
                    step % self.w.layers, self.w.r, self.w.scale, stream=stream,
-                   overlap_prior=self.overlap)
+                   overlap_prior=self.overlap, tensor_cores=self.tensor_cores)
 
 
 def capture(torch, fn, n, stream):
@@ -254,7 +255,7 @@ def time_e2e(torch, setup, K, stream):
         ssd.copy_(ssh, non_blocking=True)
         sad.copy_(sah, non_blocking=True)
         lora_apply(yd, xd, setup.A_ptrs, setup.B_ptrs, ssd, sad, s % w.layers, w.r, w.scale,
-                   stream=stream, overlap_prior=setup.overlap)
+                   stream=stream, overlap_prior=setup.overlap, tensor_cores=setup.tensor_cores)
         yout.copy_(yd, non_blocking=True)
 
     per = w.layers
@@ -321,7 +322,7 @@ def run_ours(args):
     from segmented_gather_gemm_sgmv_gb300 import binding
     binding.lib()
     w = workloads.WORKLOADS[args.workload]
-    setup = Setup(w, device)
+    setup = Setup(w, device, tensor_cores=not args.no_tensor_cores)
     stream = torch.cuda.Stream(device)
     nbytes, M = algorithmic_bytes(w, setup.ss, setup.sa)
     K, W = args.steps, args.warmup
@@ -458,6 +459,8 @@ def main():
     ap.add_argument("--workload", default="decode_distinct", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-tensor-cores", action="store_true",
+                    help="every adapter group on the CUDA cores (SGMV_NO_TENSOR_CORES)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain lora_apply launches (no programmatic dependent launch)")
     args = ap.parse_args()

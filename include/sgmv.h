@@ -97,6 +97,11 @@ typedef enum {
  *   scale                alpha / r, applied in fp32 to the intermediate before the expand
  *   dtype                element type of x, y, A and B
  *   stream               CUDA stream the work is enqueued on
+ * Execution: one kernel launch.  For fp16 / bf16 and r >= 16, adapter groups (all rows of
+ * one adapter in the call) of at least 64 rows run on the tensor cores (tcgen05.mma,
+ * section "Hardware-Level Optimizations in SGMV": tensor-core tiles for long segments); the
+ * intermediate is kept as a 16-bit high part plus a 16-bit low part, so it carries about 16
+ * significant bits into the expand.  Every other group runs on the CUDA cores in fp32.
  * Returns SGMV_OK or a negative sgmv_status_t (nothing enqueued on a negative status other
  * than SGMV_ECUDA from the launch itself).
  */
@@ -107,6 +112,7 @@ int lora_apply(void *y, const void *x, const void *const *A_ptrs, const void *co
 
 /* Flags of lora_apply_ex. */
 #define SGMV_OVERLAP_PRIOR 1u
+#define SGMV_NO_TENSOR_CORES 2u
 
 /*
  * lora_apply_ex -- lora_apply with launch flags.
@@ -120,6 +126,9 @@ int lora_apply(void *y, const void *x, const void *const *A_ptrs, const void *co
  *     the previous one.  Precondition: the immediately preceding kernel on the stream does not
  *     write the segment table, A_ptrs/B_ptrs or any adapter weights.  The pages describe no
  *     counterpart; it is launch mechanics for the same operation.
+ *   flags |= SGMV_NO_TENSOR_CORES: every adapter group runs on the CUDA cores, however many
+ *     rows it has (the results agree within rounding; used to check one path against the
+ *     other and by callers that know a batch holds only decode rows).
  * Other arguments, layout and errors: as for lora_apply (SGMV_EINVAL for unknown flags).
  */
 int lora_apply_ex(void *y, const void *x, const void *const *A_ptrs, const void *const *B_ptrs,

@@ -20,6 +20,7 @@ SGMV_OK, SGMV_EINVAL, SGMV_EALIGN, SGMV_EUNSUPPORTED, SGMV_ECUDA, SGMV_ETIMEOUT 
 SGMV_MAX_SEGMENTS = 4096
 SGMV_MAX_HIDDEN = 65536
 SGMV_OVERLAP_PRIOR = 1
+SGMV_NO_TENSOR_CORES = 2
 SYMBOLS = ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_expand", "sgmv_validate", "sgmv_get_error",
            "sgmv_set_wait_limit", "sgmv_status_string", "sgmv_version")
 
@@ -116,11 +117,12 @@ def _check(rc: int, where: str):
 
 
 def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None,
-               overlap_prior=False):
+               overlap_prior=False, tensor_cores=True):
     """y[t] += scale * (x[t] A_k) B_k for every segment row (in place on y).
 
     overlap_prior=True calls lora_apply_ex with SGMV_OVERLAP_PRIOR: the kernel may stream
     weights while the previous kernel on the stream is still running (see include/sgmv.h).
+    tensor_cores=False adds SGMV_NO_TENSOR_CORES: every adapter group on the CUDA cores.
     """
     _cuda(y, "y"), _cuda(x, "x")
     if x.dtype != y.dtype or x.dim() != 2 or y.dim() != 2 or x.shape[0] != y.shape[0]:
@@ -129,8 +131,10 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
     args = (y.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
             seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1],
             y.shape[1], int(r), float(scale), _dtype_code(x))
-    if overlap_prior:
-        rc = lib().lora_apply_ex(*args, SGMV_OVERLAP_PRIOR, _stream(stream, x.device))
+    flags = (SGMV_OVERLAP_PRIOR if overlap_prior else 0) | (
+        0 if tensor_cores else SGMV_NO_TENSOR_CORES)
+    if flags:
+        rc = lib().lora_apply_ex(*args, flags, _stream(stream, x.device))
         _check(rc, "lora_apply_ex")
     else:
         rc = lib().lora_apply(*args, _stream(stream, x.device))

@@ -1,5 +1,6 @@
 // sgmv_abi.cu -- the C ABI declared in include/sgmv.h: argument checks, launch geometry,
 // kernel attributes, the table-validation kernel and the library's device error word.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -49,6 +50,7 @@ struct Tuning {
   int stages = 0;     // 0: as many as shared memory holds
   int stage_kb = 16;  // ring stage size
   int budget_kb = 0;  // 0: 112 KB (two CTAs per SM), else the per-CTA shared-memory budget
+  int tc_min_rows = 64;  // adapter groups with at least this many rows use the tensor cores
 };
 
 Tuning read_tuning() {
@@ -56,6 +58,7 @@ Tuning read_tuning() {
   if (const char* s = std::getenv("SGMV_SMEM_KB")) t.budget_kb = std::max(0, std::atoi(s));
   if (const char* s = std::getenv("SGMV_STAGES")) t.stages = std::max(0, std::atoi(s));
   if (const char* s = std::getenv("SGMV_STAGE_KB")) t.stage_kb = std::max(4, std::atoi(s));
+  if (const char* s = std::getenv("SGMV_TC_MIN_ROWS")) t.tc_min_rows = std::max(16, std::atoi(s));
   return t;
 }
 const Tuning& tuning() {
@@ -74,6 +77,47 @@ int rank_index(int r) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link against the driver).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// Tensor map of a row-major [rows][cols] 16-bit matrix: boxes of 64 columns x box_rows rows
+// with the 128-byte swizzle (8-row atoms of 1024 bytes).  The row extent is not known to the library
+// (the call carries no M); the kernel only addresses rows named by the segment table, so the
+// map declares the largest row count TMA accepts.  Columns past `cols` read as zero.
+bool encode_rows(sgmv::TmaMap* out, const void* base, int cols, int dtype, int box_rows) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), 0x7fffffffull};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult rc = fn(&m, dtype == SGMV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (rc != CUDA_SUCCESS) return false;
+  static_assert(sizeof(m) == sizeof(*out), "tensor map size");
+  std::memcpy(out, &m, sizeof(m));
+  return true;
+}
 size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int device_state(DeviceState** out) {
@@ -174,12 +218,13 @@ int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* sme
   p.off_bars = static_cast<uint32_t>(off);
   off += up(8 * (2 * kMaxStages + sgmv::kNumFixedBars), 16);
   p.off_ctl = static_cast<uint32_t>(off);
-  off += 64;
+  off += 128;
   p.desc_ints = static_cast<int32_t>(up(2 + rmax, 4));
   p.off_desc = static_cast<uint32_t>(off);
   off += 2 * 4 * p.desc_ints;
-  p.off_tab = static_cast<uint32_t>(off);  // starts[S+1], adapters[S], base[S+1], gcnt[S]
-  off += up(4 * (4 * static_cast<size_t>(pb.S) + 2), 16);
+  // starts[S+1], adapters[S], base[S+1], gcnt[S], tbase[S+1]
+  p.off_tab = static_cast<uint32_t>(off);
+  off += up(4 * (5 * static_cast<size_t>(pb.S) + 3), 16);
   p.off_vpart = static_cast<uint32_t>(off);
   off += 2 * 4 * rmax * pb.r;
   p.off_vfull = static_cast<uint32_t>(off);
@@ -284,6 +329,25 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
     grid = kc.max_clusters * p.C;
   }
 
+  // Tensor role (fused, 16-bit types, r >= 16): ring slots of 24 KB in the ring region, the
+  // row table of two m-tiles in the CUDA-core scratch area, at least two clusters in the grid.
+  p.tc_min_rows = 0x7fffffff;
+  p.tc_slots = 0;
+  if (pb.mode == sgmv::kFused && pb.dtype != SGMV_F32 && pb.r >= 16 &&
+      !(flags & SGMV_NO_TENSOR_CORES) && grid >= 2 * p.C) {
+    const int slots = std::min<int>(static_cast<int>((smem - p.off_ring) / sgmv::kTcSlot),
+                                    (2 * kMaxStages + sgmv::kNumFixedBars - sgmv::kTcNumFixed) / 2);
+    if (slots >= 3 && p.off_stab - p.off_vpart >= (2 * 128 + 2) * sizeof(int)) {
+      if (!encode_rows(&p.tmap_x128, p.x, pb.h_in, pb.dtype, 128) ||
+          !encode_rows(&p.tmap_x8, p.x, pb.h_in, pb.dtype, 8) ||
+          !encode_rows(&p.tmap_y128, p.y, pb.h_out, pb.dtype, 128) ||
+          !encode_rows(&p.tmap_y8, p.y, pb.h_out, pb.dtype, 8))
+        return SGMV_ECUDA;
+      p.tc_min_rows = tuning().tc_min_rows;
+      p.tc_slots = slots;
+    }
+  }
+
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -362,7 +426,8 @@ int lora_apply_ex(void* y, const void* x, const void* const* A_ptrs, const void*
                   const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
                   int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
                   sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream) {
-  if (flags & ~static_cast<uint32_t>(SGMV_OVERLAP_PRIOR)) return SGMV_EINVAL;
+  if (flags & ~static_cast<uint32_t>(SGMV_OVERLAP_PRIOR | SGMV_NO_TENSOR_CORES))
+    return SGMV_EINVAL;
   int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
   if (rc != SGMV_OK) return rc;
   if (!y || !x || !A_ptrs || !B_ptrs) return SGMV_EINVAL;

@@ -31,6 +31,7 @@
 //    memory again.
 #pragma once
 #include <cstdint>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -67,6 +68,11 @@ struct MemberPlan {
   int32_t total;         // ring stages per item
 };
 
+// A CUDA tensor map (the driver's 128-byte opaque descriptor), 64-byte aligned as TMA needs.
+struct alignas(64) TmaMap {
+  uint64_t q[16];
+};
+
 struct Params {
   void* y;
   const void* x;
@@ -89,7 +95,12 @@ struct Params {
   int32_t desc_ints;
   uint64_t wait_limit_ns;
   int32_t inject_stall;
+  int32_t tc_min_rows;  // groups with at least this many rows go to the tensor role (INT32_MAX: none)
+  int32_t tc_slots;     // tensor-role ring slots (24 KB each) in the ring region
   MemberPlan plan[kPlanSlots];
+  // Tensor role: x [rows][h_in] and y [rows][h_out] with the 128-byte swizzle, boxes of
+  // 64 elements x 128 rows (a whole m-tile) and 64 x 8 rows (one swizzle atom).
+  TmaMap tmap_x128, tmap_x8, tmap_y128, tmap_y8;
 };
 
 // ---- element types ---------------------------------------------------------------------
@@ -360,8 +371,8 @@ static __device__ __forceinline__ uint32_t hash_slot(int k, int mask) {
 // gcnt[lead] holds the group's row count.
 // `scratch` (transient) holds slot[S] and the hash table (3 * hash_slots ints).
 static __device__ __forceinline__ void build_schedule(const Params& p, int* starts, int* adapters,
-                                                      int* base, int* gcnt, int* scratch,
-                                                      int* wsum) {
+                                                      int* base, int* gcnt, int* tbase,
+                                                      int* scratch, int* wsum) {
   const int tid = threadIdx.x;
   const int S = p.S, HS = p.hash_slots;
   int* slot = scratch;
@@ -410,13 +421,20 @@ static __device__ __forceinline__ void build_schedule(const Params& p, int* star
     slot[i] = h;
   }
   __syncthreads();
+  const int tcmin = p.tc_min_rows;
   block_exclusive_scan(S, base, wsum, [&](int i) {
     const int h = slot[i];
     const bool lead = h >= 0 && hlead[h] == i;
     const int rows = lead ? hcnt[h] : 0;
     gcnt[i] = rows;
-    return (rows + kRowsMax - 1) / kRowsMax;
+    return rows >= tcmin ? 0 : (rows + kRowsMax - 1) / kRowsMax;
   });
+  // Groups of at least tc_min_rows rows: m-tiles of 128 rows for the tensor role.
+  if (tcmin < 0x7fffffff)
+    block_exclusive_scan(S, tbase, wsum, [&](int i) {
+      const int rows = gcnt[i];
+      return rows >= tcmin ? (rows + 127) / 128 : 0;
+    });
 }
 
 // One warp: turns item t into {adapter, rows, row ids...} in d (d[0]=k, d[1]=R, d[2..]=rows).
@@ -456,6 +474,12 @@ static __device__ __forceinline__ void decode_item(const Params& p, int t, const
   }
   __syncwarp();
 }
+
+}  // namespace sgmv
+
+#include "sgmv_tc.cuh"
+
+namespace sgmv {
 
 // ---- the kernel ------------------------------------------------------------------------
 template <typename T, int R, int MODE>
@@ -903,6 +927,50 @@ struct Kernel {
     }
   }
 
+  static constexpr bool kTensorRole = MODE == kFused && sizeof(T) == 2 && R >= 16;
+
+  // Number of CTAs (a multiple of the cluster size) that take the tensor role: all of them
+  // when every group is long, else a share proportional to the estimated bytes of each side,
+  // leaving at least one cluster to each.  Every CTA computes the same value.
+  __device__ __forceinline__ static int tensor_ctas(const Params& p, const int* gcnt,
+                                                    int n_items, int n_mt, int N, int* ctl) {
+    if (n_mt == 0) return 0;
+    if (n_items == 0) return N;
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid == 0) {
+      ctl[2] = 0;
+      ctl[3] = 0;
+    }
+    __syncthreads();
+    int a = 0, b = 0;
+    for (int i = tid; i < p.S; i += kThreads) {
+      const int g = gcnt[i];
+      if (g >= p.tc_min_rows) a += g; else b += g;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+      b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+    if (lane == 0) {
+      atomicAdd(&ctl[2], a);
+      atomicAdd(&ctl[3], b);
+    }
+    __syncthreads();
+    const float act = static_cast<float>(p.h_in + 2 * p.h_out);
+    const float wtc = static_cast<float>(ctl[2]) * act;
+    const float wcc = static_cast<float>(ctl[3]) * act +
+                      static_cast<float>(n_items) * static_cast<float>(p.h_in + p.h_out) * R;
+    const int clusters = N / p.C;
+    int c_tc = __float2int_rn(static_cast<float>(clusters) * wtc / (wtc + wcc));
+    c_tc = max(1, min(c_tc, clusters - 1));
+    const long long pairs =
+        static_cast<long long>(n_mt) * ((p.h_out + kTcN - 1) / kTcN);  // (m-tile, n-tile)
+    if (static_cast<long long>(c_tc) * p.C > pairs)
+      c_tc = max(1, static_cast<int>(pairs / p.C));
+    return c_tc * p.C;
+  }
+
   __device__ __forceinline__ static void run(const Params& p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     pdl_launch_dependents();  // the next kernel of the stream may start its weight prefetch
@@ -915,6 +983,34 @@ struct Kernel {
     int* base = adapters + p.S;
     int* gcnt = base + (p.S + 1);
 
+    if (tid == 0) ctl[0] = 0;
+    int* tbase = gcnt + p.S;
+    build_schedule(p, starts, adapters, base, gcnt, tbase,
+                   reinterpret_cast<int*>(smem + p.off_ring), ctl + 4);
+    const int n_items = base[p.S];
+    const int N = static_cast<int>(gridDim.x);
+    // Long groups go to the tensor role: the first n_tc CTAs (whole clusters).
+    int n_tc = 0;
+    if constexpr (kTensorRole) {
+      if (p.tc_min_rows < 0x7fffffff) n_tc = tensor_ctas(p, gcnt, n_items, tbase[p.S], N, ctl);
+      if (static_cast<int>(blockIdx.x) < n_tc) {
+        fence_proxy_async();  // the ring held the hash table
+        cluster_arrive();
+        TcRole<T, R>::run(p, smem, starts, adapters, gcnt, tbase, ctl,
+                          static_cast<int>(blockIdx.x), n_tc, tbase[p.S]);
+        cluster_wait();
+        cluster_arrive();
+        cluster_wait();
+        return;
+      }
+    }
+    // A CUDA-core CTA never allocates tensor memory: give up the right at once, so that CTAs
+    // of the next kernel can be scheduled beside this one.
+    if constexpr (kTensorRole) {
+      if (warp == kConsumerWarps) tmem_relinquish();
+    }
+    const int bid = static_cast<int>(blockIdx.x) - n_tc;  // index among the CUDA-core CTAs
+    const int Nc = N - n_tc;
     if (tid == 0) {
       for (int s = 0; s < p.nstages; ++s) {
         mbar_init(sm.full(s), 1);
@@ -925,21 +1021,16 @@ struct Kernel {
       mbar_init(sm.fixed(kDescFree0), kConsumerWarps);
       mbar_init(sm.fixed(kDescFree1), kConsumerWarps);
       mbar_init(sm.fixed(kNever), 1);
-      ctl[0] = 0;
     }
-    build_schedule(p, starts, adapters, base, gcnt, reinterpret_cast<int*>(smem + p.off_ring),
-                   ctl + 4);
     // Group size E: as large as the launch cluster allows while every item still gets its own
     // group of CTAs (few items: split each across CTAs; many items: one CTA each, no exchange).
-    const int n_items = base[p.S];
-    const int N = static_cast<int>(gridDim.x);
     Group grp;
     grp.size = 1;
-    while (grp.size * 2 <= p.C && n_items * grp.size * 2 <= N) grp.size *= 2;
+    while (grp.size * 2 <= p.C && n_items * grp.size * 2 <= Nc) grp.size *= 2;
     const int lg = grp.size == 1 ? 0 : (grp.size == 2 ? 1 : 2);
-    grp.m = static_cast<int>(blockIdx.x) & (grp.size - 1);
-    grp.gid = static_cast<int>(blockIdx.x) >> lg;
-    grp.ng = N >> lg;
+    grp.m = bid & (grp.size - 1);
+    grp.gid = bid >> lg;
+    grp.ng = Nc >> lg;
     grp.rank0 = (static_cast<int>(blockIdx.x) & (p.C - 1)) & ~(grp.size - 1);
     if (tid == 0) {
       mbar_init(sm.fixed(kVReady0), grp.size);

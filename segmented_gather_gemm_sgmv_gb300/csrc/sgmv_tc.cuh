@@ -1,0 +1,542 @@
+// sgmv_tc.cuh -- the tensor-core role of the fused kernel: adapter groups with many rows.
+//
+// Operation (Punica Guide: Multi-Tenant LoRA Serving with SGMV, section "The SGMV Mathematical
+// Formulation"; section "Hardware-Level Optimizations in SGMV" for the tensor-core tiles of
+// long segments): for the rows of one adapter group,
+//     v = x . A_k          (rows x h_in) . (h_in x r)
+//     y += scale * v . B_k (rows x r) . (r x h_out)
+// computed with tcgen05.mma (fp16 / bf16 operands, fp32 accumulation in tensor memory).
+//
+// Work: a group is cut into m-tiles of 128 rows (the MMA's M, one TMEM lane per row; rows of
+// a group come from all of its segments, in segment order, gathered row by row).  The
+// sequence of (m-tile, 64-column n-tile) pairs, m-tile major, is split into equal contiguous
+// ranges, one per tensor CTA.  For every m-tile its range touches, a CTA computes the whole
+// shrink into TMEM, keeps v on chip, and runs the expand for its n-tiles.
+//
+// Roles inside the CTA (288 threads):
+//   warps 0-3  loaders: fill a ring of 24 KB slots -- x and y rows by TMA (one 128-row box
+//              when the tile's rows are consecutive tokens, else boxes of 8 consecutive rows),
+//              every other row and
+//              the weights by 16-byte cp.async (each thread's copies complete the slot's barrier
+//              by themselves) -- in the order the
+//              MMA consumes them: per m-tile, ceil(h_in/64) shrink slots {x rows [128 x 64]
+//              (K-major, 128-byte swizzle), A rows [64 x r] (MN-major, 128-byte swizzle)},
+//              then per n-tile one expand slot {B rows [r x 64] (MN-major, 128-byte swizzle),
+//              y rows [128 x 64] (swizzled for conflict-free row reads)}.
+//   warp 8     lane 0 issues the MMAs; the warp owns the TMEM allocation.
+//   warps 4-7  epilogue: v (fp32, TMEM) -> scale -> split into a 16-bit high part and a
+//              16-bit low part (v' = hi + lo to ~16 mantissa bits) -> TMEM, the A operand of
+//              the expand MMAs (D = hi . B + lo . B); then per n-tile y += D, written back in
+//              place in the slot and stored with coalesced 16-byte stores.
+// TMEM (256 columns): v fp32 [0, 64), hi [64, 96), lo [96, 128), two D buffers [128, 256).
+#pragma once
+
+namespace sgmv {
+
+constexpr int kTcRows = 128;    // rows per m-tile (MMA M = TMEM lanes)
+constexpr int kTcK = 64;        // h_in per shrink slot: one 128-byte row of 16-bit elements
+constexpr int kTcN = 64;        // h_out per expand slot
+constexpr int kTcSlot = 24576;  // bytes per ring slot
+constexpr int kTcXBytes = kTcRows * 128;  // x part of a shrink slot / y part of an expand slot
+constexpr uint32_t kTcCols = 256;
+constexpr uint32_t kTmV = 0, kTmHi = 64, kTmLo = 96, kTmD = 128;
+constexpr int kTcLoaders = 128;
+constexpr int kTcEpi = 128;
+
+// Fixed barriers after the 2 * slots ring barriers.
+enum TcBar : int { kTcVFull = 0, kTcVFree, kTcHReady, kTcHFree, kTcDFull0, kTcDFull1,
+                   kTcDEmpty0, kTcDEmpty1, kTcRtFull0, kTcRtFull1, kTcRtFree0, kTcRtFree1,
+                   kTcNever, kTcDrain, kTcNumFixed };
+
+// Byte offset of 16-byte chunk c of row m inside a block of 128-byte rows in the 128-byte
+// swizzle pattern (8-row atoms of 1024 bytes).
+static __device__ __forceinline__ uint32_t sw128(int m, int c) {
+  return static_cast<uint32_t>((m >> 3) * 1024 + (m & 7) * 128 + ((c ^ (m & 7)) << 4));
+}
+
+// One warp: the token index of each of the 128 rows of m-tile [p0, p0 + 128) of the group led
+// by segment `lead` (-1 past the group's end).
+static __device__ __forceinline__ void tile_rows(const int* starts, const int* adapters, int S,
+                                                 int lead, int p0, int p_hi, int* out) {
+  const int lane = threadIdx.x & 31;
+  const int k = adapters[lead];
+  for (int q = lane; q < kTcRows; q += 32) out[q] = -1;
+  __syncwarp();
+  int pos = 0;
+  for (int jb = lead; jb < S && pos < p_hi; jb += 32) {
+    const int j = jb + lane;
+    int len = 0;
+    if (j < S && adapters[j] == k) len = max(starts[j + 1] - starts[j], 0);
+    int incl = len;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int seg_lo = pos + incl - len;
+    const int a = max(seg_lo, p0), b = min(pos + incl, p_hi);
+    for (int q = a; q < b; ++q) out[q - p0] = starts[j] + (q - seg_lo);
+    pos += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+}
+
+// A bounded wait taken by all 32 lanes together: if any lane gives up, every lane does, so
+// that no warp-collective instruction (tcgen05.ld / st, shuffles) runs on a partial warp.
+static __device__ __forceinline__ bool wwait(const Waiter& w, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, w.wait<false>(bar, parity));
+}
+
+// The m-tiles of the CTA's range, walked identically by all roles.
+struct TcWalk {
+  int u, u1;       // current / end position in the (m-tile, n-tile) sequence
+  int ntile;       // n-tiles per m-tile
+  int mi, a, b;    // current m-tile and its n-tile range [a, b)
+  __device__ __forceinline__ bool next() {
+    if (u >= u1) return false;
+    mi = u / ntile;
+    a = u - mi * ntile;
+    b = min(ntile, a + (u1 - u));
+    u += b - a;
+    return true;
+  }
+};
+
+template <typename T, int R>
+struct TcRole {
+  static_assert(sizeof(T) == 2 && R >= 16 && R <= 64, "tensor role: 16-bit types, r >= 16");
+  static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  // Shrink: N = 64 columns of v (columns >= r are never read).  Expand: N = 64 columns of y.
+  static constexpr uint32_t kIdShrink = idesc_f16(kBf16, true, kTcRows, 64);
+  static constexpr uint32_t kIdExpand = idesc_f16(kBf16, true, kTcRows, kTcN);
+  static constexpr int kASlotOff = kTcXBytes;  // A rows follow the x rows in a shrink slot
+  static constexpr int kYSlotOff = 8192;       // y rows follow the B rows in an expand slot
+
+  struct Ctx {
+    uint32_t bars, ring;
+    int slots;
+    int* rowtok;  // [2][128]
+    int* tmask;   // [2]: 8-row blocks moved as one TMA box
+    const int *starts, *adapters, *gcnt, *tbase;
+    __device__ __forceinline__ uint32_t full(int s) const { return bars + 8u * s; }
+    __device__ __forceinline__ uint32_t empty(int s) const { return bars + 8u * (slots + s); }
+    __device__ __forceinline__ uint32_t fx(int b) const { return bars + 8u * (2 * slots + b); }
+    __device__ __forceinline__ uint32_t slot(int s) const {
+      return ring + static_cast<uint32_t>(s) * kTcSlot;
+    }
+    // m-tile -> (lead segment, first group row, rows in the tile)
+    __device__ __forceinline__ void tile(int S, int mi, int& lead, int& p0, int& nrow) const {
+      int lo = 0, hi = S - 1;  // largest i with tbase[i] <= mi
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tbase[mid] <= mi) lo = mid; else hi = mid - 1;
+      }
+      lead = lo;
+      p0 = (mi - tbase[lo]) * kTcRows;
+      nrow = min(kTcRows, gcnt[lo] - p0);
+    }
+  };
+
+  struct Ring {
+    int s;
+    uint32_t par;
+    __device__ __forceinline__ void next(int slots) {
+      if (++s == slots) {
+        s = 0;
+        par ^= 1u;
+      }
+    }
+  };
+
+  // ------------------------------------------------------------------------ loaders ----
+  // Ring slot s is always filled by loader warp s % 4 alone, so that up to four slots are
+  // being issued at once (one slot's issue is a chain of dependent barrier, TMA and cp.async
+  // instructions; spreading every slot over all four warps left that chain serial).  Binding
+  // the warp to the ring slot, not to the sequence number, keeps every use of a slot issued in
+  // order by one warp: a parity wait on the slot's "empty" barrier can then never be satisfied
+  // by a phase two uses old.
+  __device__ __forceinline__ static void loader(const Params& p, const Ctx& c, const Waiter& w,
+                                                TcWalk wk) {
+    const int lt = threadIdx.x;  // 0..127
+    const int warp = lt >> 5, lane = lt & 31;
+    const T* x = static_cast<const T*>(p.x);
+    const T* y = static_cast<const T*>(p.y);
+    pdl_wait_prior();  // x and y may be written by the previous kernel of the stream
+    Ring rg{0, 0};
+    const int nk = (p.h_in + kTcK - 1) / kTcK;
+    bool ok = true;
+    for (int li = 0; ok && wk.next(); ++li) {
+      const int par = li & 1;
+      int lead, p0, nrow;
+      c.tile(p.S, wk.mi, lead, p0, nrow);
+      int* rt = c.rowtok + par * kTcRows;
+      if (warp == 0) {
+        if (!wwait(w, c.fx(kTcRtFree0 + par), ((li >> 1) & 1) ^ 1)) break;
+        tile_rows(c.starts, c.adapters, p.S, lead, p0, p0 + nrow, rt);
+        // Rows of consecutive tokens move by TMA: the whole tile as one 128-row box when all
+        // 128 rows are consecutive, else each 8-row block of consecutive tokens as one box
+        // (one 1024-byte swizzle atom); every other row by cp.async.
+        bool run = false, line = false;
+        if (lane < kTcRows / 8) {
+          const int t0 = rt[8 * lane];
+          run = t0 >= 0;
+#pragma unroll
+          for (int j = 1; j < 8; ++j) run = run && rt[8 * lane + j] == t0 + j;
+          line = run && t0 == rt[0] + 8 * lane;
+        }
+        uint32_t mask = __ballot_sync(0xffffffffu, run);
+        if (__ballot_sync(0xffffffffu, line) == 0xffffu) mask |= 1u << 16;
+        if (lane == 0) {
+          c.tmask[par] = static_cast<int>(mask);
+          mbar_arrive(c.fx(kTcRtFull0 + par));
+        }
+      }
+      // A warp that fills no slot of this m-tile skips it (waiting for its row table could
+      // otherwise leave the warp two phases behind that barrier).
+      const int n_sl = nk + (wk.b - wk.a);
+      bool mine = false;
+      for (int i = 0, sl = rg.s; i < min(n_sl, c.slots); ++i) {
+        mine = mine || (sl & 3) == warp;
+        if (++sl == c.slots) sl = 0;
+      }
+      if (!mine) {
+        for (int i = 0; i < n_sl; ++i) rg.next(c.slots);
+        continue;
+      }
+      if (!wwait(w, c.fx(kTcRtFull0 + par), (li >> 1) & 1)) break;
+      const uint32_t mask = static_cast<uint32_t>(c.tmask[par]);
+      const bool whole = (mask >> 16) & 1u;
+      const bool all_boxes = whole || (mask & 0xffffu) == 0xffffu;
+      const uint32_t tx = whole ? 128u * 128u : static_cast<uint32_t>(__popc(mask & 0xffffu)) * 1024u;
+      const bool my_box = !whole && lane < 16 && ((mask >> lane) & 1u);  // 8-row box `lane`
+      const int box_tok = my_box ? rt[8 * lane] : 0;
+      const int tile_tok = rt[0];
+      const int k = c.adapters[lead];
+      const T* Ak = static_cast<const T*>(p.A_ptrs[k]) +
+                    static_cast<size_t>(p.layer) * p.h_in * R;
+      const T* Bk = static_cast<const T*>(p.B_ptrs[k]) +
+                    static_cast<size_t>(p.layer) * R * p.h_out;
+      // shrink slots: x rows [128 x 64] + A rows [64 x r]
+      for (int kc = 0; kc < nk; ++kc, rg.next(c.slots)) {
+        if ((rg.s & 3) != warp) continue;
+        if (!wwait(w, c.empty(rg.s), rg.par ^ 1u)) { ok = false; break; }
+        const uint32_t dst = c.slot(rg.s), bar = c.full(rg.s);
+        const int k0 = kc * kTcK;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, tx);
+          if (whole) tma_load_2d(dst, &p.tmap_x128, k0, tile_tok, bar);
+        }
+        if (my_box) tma_load_2d(dst + 1024u * lane, &p.tmap_x8, k0, box_tok, bar);
+        if (!all_boxes) {  // rows outside boxes, 16 bytes at a time
+          for (int u = lane; u < kTcRows * 8; u += 32) {
+            const int m = u >> 3, ch = u & 7;
+            const int tok = rt[m];
+            if (tok < 0 || ((mask >> (m >> 3)) & 1u)) continue;
+            const uint32_t d = dst + sw128(m, ch);
+            if (k0 + ch * 8 < p.h_in)
+              cp_async16(d, x + static_cast<size_t>(tok) * p.h_in + k0 + ch * 8);
+            else
+              cp_async16_zero(d, x);
+          }
+        }
+        constexpr int kCpr = R / 8;  // 16-byte chunks per A row
+#pragma unroll 4
+        for (int u = lane; u < kTcK * kCpr; u += 32) {
+          const int kr = u / kCpr, cc = u - kr * kCpr;
+          const uint32_t d = dst + kASlotOff + sw128(kr, cc);
+          if (k0 + kr < p.h_in)
+            cp_async16(d, Ak + static_cast<size_t>(k0 + kr) * R + cc * 8);
+          else
+            cp_async16_zero(d, Ak);
+        }
+        cp_async_arrive(bar);
+      }
+      if (!ok) break;
+      // expand slots: B rows [r x 64] + y rows [128 x 64]
+      for (int nt = wk.a; nt < wk.b; ++nt, rg.next(c.slots)) {
+        if ((rg.s & 3) != warp) continue;
+        if (!wwait(w, c.empty(rg.s), rg.par ^ 1u)) { ok = false; break; }
+        const uint32_t dst = c.slot(rg.s), bar = c.full(rg.s);
+        const int n0 = nt * kTcN;
+        const int nvalid = min(kTcN, p.h_out - n0) >> 3;  // 16-byte chunks in range
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, tx);
+          if (whole) tma_load_2d(dst + kYSlotOff, &p.tmap_y128, n0, tile_tok, bar);
+        }
+        if (my_box) tma_load_2d(dst + kYSlotOff + 1024u * lane, &p.tmap_y8, n0, box_tok, bar);
+#pragma unroll 4
+        for (int u = lane; u < R * 8; u += 32) {
+          const int kr = u >> 3, cc = u & 7;
+          if (cc < nvalid)
+            cp_async16(dst + sw128(kr, cc), Bk + static_cast<size_t>(kr) * p.h_out + n0 + cc * 8);
+        }
+        if (!all_boxes) {
+          for (int u = lane; u < kTcRows * 8; u += 32) {
+            const int m = u >> 3, ch = u & 7;
+            const int tok = rt[m];
+            if (tok < 0 || ch >= nvalid || ((mask >> (m >> 3)) & 1u)) continue;
+            cp_async16(dst + kYSlotOff + sw128(m, ch),
+                       y + static_cast<size_t>(tok) * p.h_out + n0 + ch * 8);
+          }
+        }
+        cp_async_arrive(bar);
+      }
+    }
+    cp_async_wait_all();  // every copy lands before the CTA moves on
+  }
+
+  // ---------------------------------------------------------------------- MMA issuer ----
+  __device__ __forceinline__ static void issuer(const Params& p, const Ctx& c, const Waiter& w,
+                                                TcWalk wk, uint32_t tm) {
+    Ring rg{0, 0};
+    int dq = 0;
+    uint32_t dpar = 0;
+    const int nk = (p.h_in + kTcK - 1) / kTcK;
+    for (int li = 0; wk.next(); ++li) {
+      for (int kc = 0; kc < nk; ++kc) {
+        if (!w.wait<false>(c.full(rg.s), rg.par)) return;
+        if (kc == 0 && !w.wait<false>(c.fx(kTcVFree), (li & 1) ^ 1)) return;
+        fence_proxy_async();  // cp.async (generic proxy) data -> the MMA's async-proxy reads
+        tc_fence_after();
+        const uint32_t sa = c.slot(rg.s);
+#pragma unroll
+        for (int j = 0; j < kTcK / 16; ++j)
+          umma_ss(tm + kTmV, sdesc_sw128(sa + 32u * j, 16, 1024),
+                  sdesc_sw128(sa + kASlotOff + 2048u * j, 8192, 1024), kIdShrink,
+                  (kc | j) != 0);
+        umma_commit(c.empty(rg.s));
+        mbar_arrive_n(c.empty(rg.s), 4);  // a shrink slot holds no y rows for the epilogue
+        rg.next(c.slots);
+      }
+      umma_commit(c.fx(kTcVFull));
+      if (!w.wait<false>(c.fx(kTcHReady), li & 1)) return;
+      tc_fence_after();
+      for (int nt = wk.a; nt < wk.b; ++nt) {
+        if (!w.wait<false>(c.full(rg.s), rg.par)) return;
+        if (!w.wait<false>(c.fx(kTcDEmpty0 + dq), dpar ^ 1u)) return;
+        fence_proxy_async();
+        tc_fence_after();
+        const uint32_t d = tm + kTmD + 64u * dq;
+        const uint32_t sb = c.slot(rg.s);
+#pragma unroll
+        for (int j = 0; j < R / 16; ++j) {
+          const uint64_t bd = sdesc_sw128(sb + 2048u * j, 8192, 1024);
+          umma_ts(d, tm + kTmHi + 8u * j, bd, kIdExpand, j != 0);
+          umma_ts(d, tm + kTmLo + 8u * j, bd, kIdExpand, 1);
+        }
+        umma_commit(c.empty(rg.s));
+        umma_commit(c.fx(kTcDFull0 + dq));
+        rg.next(c.slots);
+        if (++dq == 2) {
+          dq = 0;
+          dpar ^= 1u;
+        }
+      }
+      umma_commit(c.fx(kTcHFree));
+    }
+  }
+
+  // ------------------------------------------------------------------------ epilogue ----
+  __device__ __forceinline__ static void epilogue(const Params& p, const Ctx& c, const Waiter& w,
+                                                  TcWalk wk, uint32_t tm) {
+    const int et = threadIdx.x - kTcLoaders;  // 0..127
+    const int q = et >> 5, lane = et & 31;    // TMEM lane quarter, lane
+    const int row = et;                       // tile row = TMEM lane
+    const uint32_t tq = tm + (static_cast<uint32_t>(q * 32) << 16);
+    T* y = static_cast<T*>(p.y);
+    pdl_wait_prior();
+    Ring rg{0, 0};
+    int dq = 0;
+    uint32_t dpar = 0;
+    const int nk = (p.h_in + kTcK - 1) / kTcK;
+    for (int li = 0; wk.next(); ++li) {
+      const int par = li & 1;
+      if (!wwait(w, c.fx(kTcRtFull0 + par), (li >> 1) & 1)) return;
+      const int* rt = c.rowtok + par * kTcRows;
+      // v -> scale -> hi + lo (16-bit each) -> TMEM
+      if (!wwait(w, c.fx(kTcVFull), li & 1)) return;
+      if (!wwait(w, c.fx(kTcHFree), (li & 1) ^ 1)) return;
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < R; c0 += 16) {
+        uint32_t v[16], hi[8], lo[8];
+        tmem_ld16(tq + kTmV + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float a = p.scale * __uint_as_float(v[2 * e]);
+          const float b = p.scale * __uint_as_float(v[2 * e + 1]);
+          split2(a, b, hi[e], lo[e]);
+        }
+        tmem_st8(tq + kTmHi + c0 / 2, hi);
+        tmem_st8(tq + kTmLo + c0 / 2, lo);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(c.fx(kTcVFree));
+      mbar_arrive(c.fx(kTcHReady));
+      // skip the shrink slots of this m-tile
+      for (int kc = 0; kc < nk; ++kc) rg.next(c.slots);
+      for (int nt = wk.a; nt < wk.b; ++nt) {
+        if (!wwait(w, c.fx(kTcDFull0 + dq), dpar)) return;
+        if (!wwait(w, c.full(rg.s), rg.par)) return;
+        tc_fence_after();
+        const uint32_t ys = c.slot(rg.s) + kYSlotOff;
+        const int n0 = nt * kTcN;
+        const int nvalid = min(kTcN, p.h_out - n0) >> 3;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t d[32];
+          tmem_ld32(tq + kTmD + 64u * dq + 32u * h, d);
+          tmem_wait_ld();
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const uint32_t a = ys + sw128(row, 4 * h + cc);
+            sts128(a, add8(lds128(a), d + 8 * cc));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.fx(kTcDEmpty0 + dq));
+        // coalesced stores of this warp's 32 rows: 8 lanes per 128-byte row segment
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = q * 32 + i * 4 + (lane >> 3), cc = lane & 7;
+          const int tok = rt[rr];
+          if (tok >= 0 && cc < nvalid)
+            *reinterpret_cast<uint4*>(y + static_cast<size_t>(tok) * p.h_out + n0 + cc * 8) =
+                lds128(ys + sw128(rr, cc));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.empty(rg.s));
+        rg.next(c.slots);
+        if (++dq == 2) {
+          dq = 0;
+          dpar ^= 1u;
+        }
+      }
+      mbar_arrive(c.fx(kTcRtFree0 + par));
+    }
+  }
+
+  // v' = hi + lo with hi = round(v'), lo = round(v' - hi): two values packed per 32 bits.
+  __device__ __forceinline__ static void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    if constexpr (kBf16) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+      const float2 hf = __bfloat1622float2(h);
+      const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+      hi = *reinterpret_cast<const uint32_t*>(&h);
+      lo = *reinterpret_cast<const uint32_t*>(&l);
+    } else {
+      const __half2 h = __floats2half2_rn(a, b);
+      const float2 hf = __half22float2(h);
+      const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+      hi = *reinterpret_cast<const uint32_t*>(&h);
+      lo = *reinterpret_cast<const uint32_t*>(&l);
+    }
+  }
+
+  // Eight 16-bit y values + eight fp32 D values, rounded once.
+  __device__ __forceinline__ static uint4 add8(uint4 yv, const uint32_t* d) {
+    const uint32_t in[4] = {yv.x, yv.y, yv.z, yv.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (kBf16) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[i]));
+        const __nv_bfloat162 r = __floats2bfloat162_rn(f.x + __uint_as_float(d[2 * i]),
+                                                       f.y + __uint_as_float(d[2 * i + 1]));
+        out[i] = *reinterpret_cast<const uint32_t*>(&r);
+      } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&in[i]));
+        const __half2 r = __floats2half2_rn(f.x + __uint_as_float(d[2 * i]),
+                                            f.y + __uint_as_float(d[2 * i + 1]));
+        out[i] = *reinterpret_cast<const uint32_t*>(&r);
+      }
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+  }
+
+  // ----------------------------------------------------------------------------- run ----
+  // rank / n_tc: this CTA among the tensor CTAs.  n_mt: m-tiles of all long groups.
+  __device__ __forceinline__ static void run(const Params& p, uint8_t* smem, const int* starts,
+                                             const int* adapters, const int* gcnt,
+                                             const int* tbase, int* ctl, int rank, int n_tc,
+                                             int n_mt) {
+    const int tid = threadIdx.x, warp = tid >> 5;
+    Ctx c;
+    c.bars = smem_addr(smem + p.off_bars);
+    c.ring = smem_addr(smem + p.off_ring);
+    c.slots = p.tc_slots;
+    c.rowtok = reinterpret_cast<int*>(smem + p.off_vpart);
+    c.tmask = c.rowtok + 2 * kTcRows;
+    c.starts = starts;
+    c.adapters = adapters;
+    c.gcnt = gcnt;
+    c.tbase = tbase;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(ctl + 1);
+    if (tid == 0) {
+      for (int s = 0; s < c.slots; ++s) {
+        mbar_init(c.full(s), 32 + 1);  // the filling warp's cp.async arrivals + TMA bytes
+        mbar_init(c.empty(s), 1 + 4);
+      }
+      mbar_init(c.fx(kTcVFull), 1);
+      mbar_init(c.fx(kTcVFree), kTcEpi);
+      mbar_init(c.fx(kTcHReady), kTcEpi);
+      mbar_init(c.fx(kTcHFree), 1);
+      mbar_init(c.fx(kTcDFull0), 1);
+      mbar_init(c.fx(kTcDFull1), 1);
+      mbar_init(c.fx(kTcDEmpty0), 4);
+      mbar_init(c.fx(kTcDEmpty1), 4);
+      mbar_init(c.fx(kTcRtFull0), 1);
+      mbar_init(c.fx(kTcRtFull1), 1);
+      mbar_init(c.fx(kTcRtFree0), kTcEpi);
+      mbar_init(c.fx(kTcRtFree1), kTcEpi);
+      mbar_init(c.fx(kTcNever), 1);
+      mbar_init(c.fx(kTcDrain), 1);
+      fence_mbar_init();
+    }
+    if (warp == kConsumerWarps) {
+      tmem_alloc(smem_addr(tslot), kTcCols);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tslot;
+
+    if (tid == 0) {
+      tma_prefetch_desc(&p.tmap_x128);
+      tma_prefetch_desc(&p.tmap_x8);
+      tma_prefetch_desc(&p.tmap_y128);
+      tma_prefetch_desc(&p.tmap_y8);
+    }
+    const Waiter w{reinterpret_cast<volatile int*>(ctl), p.err, p.wait_limit_ns};
+    if (p.inject_stall) w.wait<false>(c.fx(kTcNever), 0);  // nothing completes it
+
+    TcWalk wk;
+    wk.ntile = (p.h_out + kTcN - 1) / kTcN;
+    const long long U = static_cast<long long>(n_mt) * wk.ntile;
+    wk.u = static_cast<int>(U * rank / n_tc);
+    wk.u1 = static_cast<int>(U * (rank + 1) / n_tc);
+
+    if (warp < 4) {
+      loader(p, c, w, wk);
+    } else if (warp < kConsumerWarps) {
+      epilogue(p, c, w, wk, tm);
+    } else if ((tid & 31) == 0) {
+      issuer(p, c, w, wk, tm);
+      // every MMA issued has completed before TMEM is released
+      umma_commit(c.fx(kTcDrain));
+      const uint64_t t0 = now_ns();
+      while (!mbar_try(c.fx(kTcDrain), 0) && now_ns() - t0 < p.wait_limit_ns) {
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kConsumerWarps) tmem_dealloc(tm, kTcCols);
+  }
+};
+
+}  // namespace sgmv

@@ -35,6 +35,8 @@ def test_header_constants_match_binding():
     text = open(HEADER).read()
     assert f"#define SGMV_MAX_SEGMENTS {binding.SGMV_MAX_SEGMENTS}" in text
     assert f"#define SGMV_MAX_HIDDEN {binding.SGMV_MAX_HIDDEN}" in text
+    assert f"#define SGMV_OVERLAP_PRIOR {binding.SGMV_OVERLAP_PRIOR}u" in text
+    assert f"#define SGMV_NO_TENSOR_CORES {binding.SGMV_NO_TENSOR_CORES}u" in text
     for name, val in [("SGMV_EINVAL", -1), ("SGMV_EALIGN", -2), ("SGMV_EUNSUPPORTED", -3),
                       ("SGMV_ECUDA", -4), ("SGMV_ETIMEOUT", -5)]:
         assert re.search(rf"{name}\s*=\s*{val}\b", text), name
@@ -68,6 +70,15 @@ def apply(L, **kw):
 ])
 def test_lora_apply_host_checks(L, kw, status):
     assert apply(L, **kw) == status
+
+
+def test_lora_apply_ex_flags(L):
+    a = OK_ARGS
+    args = (a["y"], a["x"], a["A"], a["B"], a["ss"], a["sa"], 0, a["layer"], a["h_in"],
+            a["h_out"], a["r"], a["scale"], a["dt"])
+    for flags in (0, 1, 2, 3):  # num_segments = 0: argument checks only, nothing launched
+        assert L.lora_apply_ex(*args, flags, None) == 0
+    assert L.lora_apply_ex(*args, 4, None) == -1
 
 
 def test_shrink_expand_validate_host_checks(L):
