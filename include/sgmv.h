@@ -97,11 +97,12 @@ typedef enum {
  *   scale                alpha / r, applied in fp32 to the intermediate before the expand
  *   dtype                element type of x, y, A and B
  *   stream               CUDA stream the work is enqueued on
- * Execution: one kernel launch.  For fp16 / bf16 and r >= 16, adapter groups (all rows of
- * one adapter in the call) of at least 64 rows run on the tensor cores (tcgen05.mma,
- * section "Hardware-Level Optimizations in SGMV": tensor-core tiles for long segments); the
- * intermediate is kept as a 16-bit high part plus a 16-bit low part, so it carries about 16
- * significant bits into the expand.  Every other group runs on the CUDA cores in fp32.
+ * Execution: one kernel launch.  For fp16 / bf16 and r >= 16, an adapter group (all rows of
+ * one adapter in the call) runs on the tensor cores (tcgen05.mma; section "Hardware-Level
+ * Optimizations in SGMV": tensor-core tiles for long segments) when it has at least 64 rows
+ * and the CUDA-core path would re-read at least 32 MB of its weights (ceil(rows / 4) x the
+ * bytes of A_k and B_k); there the intermediate is kept as a 16-bit high part plus a 16-bit
+ * low part, about 16 significant bits.  Every other group runs on the CUDA cores in fp32.
  * Returns SGMV_OK or a negative sgmv_status_t (nothing enqueued on a negative status other
  * than SGMV_ECUDA from the launch itself).
  */
@@ -113,6 +114,7 @@ int lora_apply(void *y, const void *x, const void *const *A_ptrs, const void *co
 /* Flags of lora_apply_ex. */
 #define SGMV_OVERLAP_PRIOR 1u
 #define SGMV_NO_TENSOR_CORES 2u
+#define SGMV_TENSOR_CORES_ALWAYS 4u
 
 /*
  * lora_apply_ex -- lora_apply with launch flags.
@@ -129,6 +131,9 @@ int lora_apply(void *y, const void *x, const void *const *A_ptrs, const void *co
  *   flags |= SGMV_NO_TENSOR_CORES: every adapter group runs on the CUDA cores, however many
  *     rows it has (the results agree within rounding; used to check one path against the
  *     other and by callers that know a batch holds only decode rows).
+ *   flags |= SGMV_TENSOR_CORES_ALWAYS: every adapter group of at least 64 rows runs on the
+ *     tensor cores, without the cost rule described under lora_apply (fp16 / bf16, r >= 16).
+ *     Not combinable with SGMV_NO_TENSOR_CORES (SGMV_EINVAL).
  * Other arguments, layout and errors: as for lora_apply (SGMV_EINVAL for unknown flags).
  */
 int lora_apply_ex(void *y, const void *x, const void *const *A_ptrs, const void *const *B_ptrs,

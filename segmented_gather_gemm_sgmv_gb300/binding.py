@@ -21,6 +21,7 @@ SGMV_MAX_SEGMENTS = 4096
 SGMV_MAX_HIDDEN = 65536
 SGMV_OVERLAP_PRIOR = 1
 SGMV_NO_TENSOR_CORES = 2
+SGMV_TENSOR_CORES_ALWAYS = 4
 SYMBOLS = ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_expand", "sgmv_validate", "sgmv_get_error",
            "sgmv_set_wait_limit", "sgmv_status_string", "sgmv_version")
 
@@ -117,12 +118,13 @@ def _check(rc: int, where: str):
 
 
 def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None,
-               overlap_prior=False, tensor_cores=True):
+               overlap_prior=False, tensor_cores="auto"):
     """y[t] += scale * (x[t] A_k) B_k for every segment row (in place on y).
 
     overlap_prior=True calls lora_apply_ex with SGMV_OVERLAP_PRIOR: the kernel may stream
     weights while the previous kernel on the stream is still running (see include/sgmv.h).
-    tensor_cores=False adds SGMV_NO_TENSOR_CORES: every adapter group on the CUDA cores.
+    tensor_cores: "auto" (the library's cost rule), "never" (SGMV_NO_TENSOR_CORES) or "always"
+    (SGMV_TENSOR_CORES_ALWAYS); True / False mean "auto" / "never".
     """
     _cuda(y, "y"), _cuda(x, "x")
     if x.dtype != y.dtype or x.dim() != 2 or y.dim() != 2 or x.shape[0] != y.shape[0]:
@@ -131,8 +133,11 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
     args = (y.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
             seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1],
             y.shape[1], int(r), float(scale), _dtype_code(x))
-    flags = (SGMV_OVERLAP_PRIOR if overlap_prior else 0) | (
-        0 if tensor_cores else SGMV_NO_TENSOR_CORES)
+    mode = {True: "auto", False: "never"}.get(tensor_cores, tensor_cores)
+    if mode not in ("auto", "never", "always"):
+        raise ValueError(f"tensor_cores must be 'auto', 'never' or 'always', not {tensor_cores!r}")
+    flags = (SGMV_OVERLAP_PRIOR if overlap_prior else 0) | {
+        "auto": 0, "never": SGMV_NO_TENSOR_CORES, "always": SGMV_TENSOR_CORES_ALWAYS}[mode]
     if flags:
         rc = lib().lora_apply_ex(*args, flags, _stream(stream, x.device))
         _check(rc, "lora_apply_ex")

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -50,7 +51,9 @@ struct Tuning {
   int stages = 0;     // 0: as many as shared memory holds
   int stage_kb = 16;  // ring stage size
   int budget_kb = 0;  // 0: 112 KB (two CTAs per SM), else the per-CTA shared-memory budget
-  int tc_min_rows = 64;  // adapter groups with at least this many rows use the tensor cores
+  int tc_min_rows = 64;  // adapter groups with at least this many rows use the tensor cores...
+  int tc_min_mb = 32;    // ...and whose CUDA-core items would re-read at least this many MB of
+                         // weights (ceil(rows / 4) items x the adapter's A and B)
 };
 
 Tuning read_tuning() {
@@ -59,6 +62,7 @@ Tuning read_tuning() {
   if (const char* s = std::getenv("SGMV_STAGES")) t.stages = std::max(0, std::atoi(s));
   if (const char* s = std::getenv("SGMV_STAGE_KB")) t.stage_kb = std::max(4, std::atoi(s));
   if (const char* s = std::getenv("SGMV_TC_MIN_ROWS")) t.tc_min_rows = std::max(16, std::atoi(s));
+  if (const char* s = std::getenv("SGMV_TC_MIN_MB")) t.tc_min_mb = std::max(0, std::atoi(s));
   return t;
 }
 const Tuning& tuning() {
@@ -343,7 +347,17 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
           !encode_rows(&p.tmap_y128, p.y, pb.h_out, pb.dtype, 128) ||
           !encode_rows(&p.tmap_y8, p.y, pb.h_out, pb.dtype, 8))
         return SGMV_ECUDA;
-      p.tc_min_rows = tuning().tc_min_rows;
+      // The CUDA-core path streams a group's weights once per item of 4 rows (mostly from
+      // L2); the tensor path streams them once per 128-row tile but repeats the shrink in every
+      // CTA that shares a tile.  Measured on GB300: small-rank decode groups (256 rows, r = 16,
+      // h = 4096: 17 MB of weight re-reads) run faster on the CUDA cores; prefill groups
+      // (>= 128 rows, r = 64: >= 60 MB) several times faster on the tensor cores.
+      const double w = static_cast<double>(pb.r) * (pb.h_in + pb.h_out) * 2.0;
+      const double items = std::ceil(tuning().tc_min_mb * 1048576.0 / w);
+      p.tc_min_rows = (flags & SGMV_TENSOR_CORES_ALWAYS)
+                          ? tuning().tc_min_rows
+                          : static_cast<int>(std::min(
+                                1e9, std::max<double>(tuning().tc_min_rows, 4.0 * items)));
       p.tc_slots = slots;
     }
   }
@@ -426,8 +440,10 @@ int lora_apply_ex(void* y, const void* x, const void* const* A_ptrs, const void*
                   const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
                   int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
                   sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream) {
-  if (flags & ~static_cast<uint32_t>(SGMV_OVERLAP_PRIOR | SGMV_NO_TENSOR_CORES))
+  if (flags & ~static_cast<uint32_t>(SGMV_OVERLAP_PRIOR | SGMV_NO_TENSOR_CORES |
+                                     SGMV_TENSOR_CORES_ALWAYS))
     return SGMV_EINVAL;
+  if ((flags & SGMV_NO_TENSOR_CORES) && (flags & SGMV_TENSOR_CORES_ALWAYS)) return SGMV_EINVAL;
   int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
   if (rc != SGMV_OK) return rc;
   if (!y || !x || !A_ptrs || !B_ptrs) return SGMV_EINVAL;

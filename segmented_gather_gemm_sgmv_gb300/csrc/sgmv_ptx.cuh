@@ -120,6 +120,10 @@ static __device__ __forceinline__ void bulk_commit() {
 static __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// Waits until at most one bulk group of this thread still reads shared memory.
+static __device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 static __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -178,6 +182,15 @@ static __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tma
       : "memory");
 }
 
+// 2-D tile store from shared memory (same box / swizzle as the map); elements past the tensor's
+// extent are not written.  Completion is tracked with the bulk async-groups of the thread.
+static __device__ __forceinline__ void tma_store_2d(const void* tmap, int c0, int c1,
+                                                    uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap),
+      "r"(c0), "r"(c1), "r"(src)
+      : "memory");
+}
 static __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

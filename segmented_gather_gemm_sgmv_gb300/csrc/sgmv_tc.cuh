@@ -377,43 +377,71 @@ struct TcRole {
       mbar_arrive(c.fx(kTcHReady));
       // skip the shrink slots of this m-tile
       for (int kc = 0; kc < nk; ++kc) rg.next(c.slots);
+      const uint32_t mask = static_cast<uint32_t>(c.tmask[par]);
+      int pend = -1;  // ring slot whose TMA stores may still be reading it
       for (int nt = wk.a; nt < wk.b; ++nt) {
-        if (!wwait(w, c.fx(kTcDFull0 + dq), dpar)) return;
+        // y rows of the slot (landed with the slot) into registers while the MMAs run
         if (!wwait(w, c.full(rg.s), rg.par)) return;
-        tc_fence_after();
         const uint32_t ys = c.slot(rg.s) + kYSlotOff;
+        uint4 yv[4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) yv[cc] = lds128(ys + sw128(row, cc));
+        if (!wwait(w, c.fx(kTcDFull0 + dq), dpar)) return;
+        tc_fence_after();
         const int n0 = nt * kTcN;
         const int nvalid = min(kTcN, p.h_out - n0) >> 3;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+          if (h == 1) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) yv[cc] = lds128(ys + sw128(row, 4 + cc));
+          }
           uint32_t d[32];
           tmem_ld32(tq + kTmD + 64u * dq + 32u * h, d);
           tmem_wait_ld();
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const uint32_t a = ys + sw128(row, 4 * h + cc);
-            sts128(a, add8(lds128(a), d + 8 * cc));
-          }
+          for (int cc = 0; cc < 4; ++cc)
+            sts128(ys + sw128(row, 4 * h + cc), add8(yv[cc], d + 8 * cc));
         }
         tc_fence_before();
+        fence_proxy_async();  // the rows just written are read by TMA stores
         __syncwarp();
         if (lane == 0) mbar_arrive(c.fx(kTcDEmpty0 + dq));
-        // coalesced stores of this warp's 32 rows: 8 lanes per 128-byte row segment
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = q * 32 + i * 4 + (lane >> 3), cc = lane & 7;
-          const int tok = rt[rr];
-          if (tok >= 0 && cc < nvalid)
-            *reinterpret_cast<uint4*>(y + static_cast<size_t>(tok) * p.h_out + n0 + cc * 8) =
-                lds128(ys + sw128(rr, cc));
+        // this warp's 32 rows = 8-row blocks 4q..4q+3: a block of consecutive tokens leaves by
+        // one TMA store (columns past h_out are not written), other rows by 16-byte stores
+        const int blk = 4 * q + lane;
+        const bool boxed = lane < 4 && ((mask >> blk) & 1u);
+        if (boxed) {
+          tma_store_2d(&p.tmap_y8, n0, rt[8 * blk], ys + 1024u * blk);
+          bulk_commit();
         }
+        if ((mask & (0xfu << (4 * q))) != (0xfu << (4 * q))) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = q * 32 + i * 4 + (lane >> 3), cc = lane & 7;
+            const int tok = rt[rr];
+            if (tok >= 0 && cc < nvalid && !((mask >> (rr >> 3)) & 1u))
+              *reinterpret_cast<uint4*>(y + static_cast<size_t>(tok) * p.h_out + n0 + cc * 8) =
+                  lds128(ys + sw128(rr, cc));
+          }
+        }
+        // A slot is reused only after its TMA stores have read it: release the previous
+        // n-tile's slot now (its stores have had a whole n-tile to read), this one next time.
+        if (boxed) bulk_wait_read_1();
         __syncwarp();
-        if (lane == 0) mbar_arrive(c.empty(rg.s));
+        if (lane == 0 && pend >= 0) mbar_arrive(c.empty(pend));
+        pend = rg.s;
         rg.next(c.slots);
         if (++dq == 2) {
           dq = 0;
           dpar ^= 1u;
         }
+      }
+      if (pend >= 0) {  // the m-tile's last slot
+        bulk_wait_read();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.empty(pend));
+        pend = -1;
       }
       mbar_arrive(c.fx(kTcRtFree0 + par));
     }

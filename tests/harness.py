@@ -117,7 +117,7 @@ def assert_close(y, y_ref, what="", atol=ATOL, rtol=RTOL):
     return float(err.max()) if err.size else 0.0
 
 
-def run_apply(c: Case, layer, y=None, x=None, tensor_cores=True):
+def run_apply(c: Case, layer, y=None, x=None, tensor_cores="auto"):
     from segmented_gather_gemm_sgmv_gb300 import lora_apply
     y = c.y0.clone() if y is None else y
     lora_apply(y, c.x if x is None else x, c.A_ptrs, c.B_ptrs, c.d_ss, c.d_sa, layer, c.w.r,

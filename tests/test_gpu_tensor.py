@@ -1,7 +1,7 @@
 """GPU parity of the tensor-core role (tcgen05.mma) of lora_apply, through the C ABI.
 
-Adapter groups of at least 64 rows run on the tensor cores (fp16 / bf16, r >= 16); smaller
-groups stay on the CUDA cores.  The cases below mix both kinds in one call, span several
+With SGMV_TENSOR_CORES_ALWAYS, adapter groups of at least 64 rows run on the tensor cores
+(fp16 / bf16, r >= 16); smaller groups stay on the CUDA cores.  The cases below mix both kinds in one call, span several
 128-row m-tiles and 64-column n-tiles, and give h_in / h_out ragged tails (not multiples of
 64), groups gathered from non-adjacent segments, and the 63 / 64-row boundary.  Every case is
 compared with the fp64 oracle (|y - y_ref| <= 1e-2 + 1e-2 |y_ref|) and with the same call
@@ -53,8 +53,8 @@ def test_mixed_groups_match_oracle_and_cuda_cores(dtype, r, h_in, h_out):
     ss, sa = _table(MIXED_LENS, MIXED_IDS)
     c = harness.make_case(w, ss, sa, M=int(ss[-1]) + 3)
     for layer in (0, 1):
-        y_tc = harness.run_apply(c, layer)
-        y_cc = harness.run_apply(c, layer, tensor_cores=False)
+        y_tc = harness.run_apply(c, layer, tensor_cores="always")
+        y_cc = harness.run_apply(c, layer, tensor_cores="never")
         ref = harness.oracle_apply(c, layer)
         harness.assert_close(y_tc.float().cpu().numpy(), ref, f"tensor {dtype} r{r} L{layer}")
         harness.assert_close(y_cc.float().cpu().numpy(), ref, f"cuda-core {dtype} r{r} L{layer}")
@@ -77,7 +77,7 @@ def test_integer_exact_tensor_groups(dtype):
     c = harness.make_case(w, ss, sa, pool=(A, B))
     c.x = torch.randint(-1, 2, c.x.shape, generator=g, device="cuda").to(dt)
     c.y0 = torch.randint(-4, 5, c.y0.shape, generator=g, device="cuda").to(dt)
-    y = harness.run_apply(c, 0)
+    y = harness.run_apply(c, 0, tensor_cores="always")
     ref = torch.as_tensor(harness.oracle_apply(c, 0)).to(dt)
     assert torch.equal(y.cpu(), ref), f"tensor path not bit-exact ({dtype})"
 
@@ -99,7 +99,7 @@ def test_adapter_tags_long_groups():
     c.x = torch.zeros_like(c.x)
     c.x[:, 0] = 1
     c.y0 = torch.zeros_like(c.y0)
-    y = harness.run_apply(c, 0)
+    y = harness.run_apply(c, 0, tensor_cores="always")
     want = np.zeros(c.M)
     for i, k in enumerate(sa):
         want[ss[i]:ss[i + 1]] = w.scale * (k + 1)
@@ -117,7 +117,7 @@ def test_guard_rows_around_tensor_groups():
     c.y0[:5] = float("nan")
     c.y0[140:150] = float("nan")
     c.y0[290:] = float("nan")
-    y = harness.run_apply(c, 0)
+    y = harness.run_apply(c, 0, tensor_cores="always")
     assert torch.isnan(y[:5]).all() and torch.isnan(y[140:150]).all()
     assert torch.isnan(y[290:]).all()
     ref = harness.oracle_apply(c, 0)
@@ -132,8 +132,8 @@ def test_many_tiles_deterministic():
     lens = [1500, 900, 2100, 700]
     ss, sa = _table(lens, [0, 1, 2, 3])
     c = harness.make_case(w, ss, sa)
-    y1 = harness.run_apply(c, 0)
-    y2 = harness.run_apply(c, 0)
+    y1 = harness.run_apply(c, 0, tensor_cores="always")
+    y2 = harness.run_apply(c, 0, tensor_cores="always")
     assert torch.equal(y1, y2)
     rng = np.random.default_rng(9)
     rows = set(rng.choice(c.M, 200, replace=False).tolist())
@@ -157,8 +157,8 @@ def test_large_table_gathered_group():
     ids = np.r_[[0, 5], ids].astype(np.int32)
     ss, sa = _table(lens, ids)
     c = harness.make_case(w, ss, sa)
-    y = harness.run_apply(c, 0)
-    y_cc = harness.run_apply(c, 0, tensor_cores=False)
+    y = harness.run_apply(c, 0, tensor_cores="always")
+    y_cc = harness.run_apply(c, 0, tensor_cores="never")
     ref = harness.oracle_apply(c, 0)
     harness.assert_close(y.float().cpu().numpy(), ref, "large table, tensor")
     harness.assert_close(y_cc.float().cpu().numpy(), ref, "large table, cuda cores")
