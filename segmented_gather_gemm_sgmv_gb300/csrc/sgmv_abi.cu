@@ -49,7 +49,7 @@ constexpr int kMaxStages = 16;
 
 struct Tuning {
   int stages = 0;     // 0: as many as shared memory holds
-  int stage_kb = 16;  // ring stage size
+  int stage_kb = 24;  // ring stage size
   int budget_kb = 0;  // 0: 112 KB (two CTAs per SM), else the per-CTA shared-memory budget
   int tc_min_rows = 64;  // adapter groups with at least this many rows use the tensor cores...
   int tc_min_mb = 32;    // ...and whose CUDA-core items would re-read at least this many MB of

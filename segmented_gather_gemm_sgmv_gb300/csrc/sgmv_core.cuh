@@ -422,19 +422,25 @@ static __device__ __forceinline__ void build_schedule(const Params& p, int* star
   }
   __syncthreads();
   const int tcmin = p.tc_min_rows;
+  int* any_long = wsum + kThreads / 32 + 1;  // set when some group goes to the tensor role
+  if (threadIdx.x == 0) *any_long = 0;
   block_exclusive_scan(S, base, wsum, [&](int i) {
     const int h = slot[i];
     const bool lead = h >= 0 && hlead[h] == i;
     const int rows = lead ? hcnt[h] : 0;
     gcnt[i] = rows;
+    if (rows >= tcmin) *any_long = 1;
     return rows >= tcmin ? 0 : (rows + kRowsMax - 1) / kRowsMax;
   });
   // Groups of at least tc_min_rows rows: m-tiles of 128 rows for the tensor role.
-  if (tcmin < 0x7fffffff)
+  if (*any_long)
     block_exclusive_scan(S, tbase, wsum, [&](int i) {
       const int rows = gcnt[i];
       return rows >= tcmin ? (rows + 127) / 128 : 0;
     });
+  else if (threadIdx.x == 0)
+    tbase[S] = 0;
+  __syncthreads();
 }
 
 // One warp: turns item t into {adapter, rows, row ids...} in d (d[0]=k, d[1]=R, d[2..]=rows).
@@ -983,7 +989,18 @@ struct Kernel {
     int* base = adapters + p.S;
     int* gcnt = base + (p.S + 1);
 
-    if (tid == 0) ctl[0] = 0;
+    if (tid == 0) {  // CUDA-core role barriers (a tensor-role CTA invalidates them again)
+      ctl[0] = 0;
+      for (int s = 0; s < p.nstages; ++s) {
+        mbar_init(sm.full(s), 1);
+        mbar_init(sm.empty(s), kConsumerWarps);
+      }
+      mbar_init(sm.fixed(kDescFull0), 1);
+      mbar_init(sm.fixed(kDescFull1), 1);
+      mbar_init(sm.fixed(kDescFree0), kConsumerWarps);
+      mbar_init(sm.fixed(kDescFree1), kConsumerWarps);
+      mbar_init(sm.fixed(kNever), 1);
+    }
     int* tbase = gcnt + p.S;
     build_schedule(p, starts, adapters, base, gcnt, tbase,
                    reinterpret_cast<int*>(smem + p.off_ring), ctl + 4);
@@ -994,6 +1011,14 @@ struct Kernel {
     if constexpr (kTensorRole) {
       if (p.tc_min_rows < 0x7fffffff) n_tc = tensor_ctas(p, gcnt, n_items, tbase[p.S], N, ctl);
       if (static_cast<int>(blockIdx.x) < n_tc) {
+        if (tid == 0) {  // the barrier words are re-initialised by the tensor role
+          for (int s = 0; s < p.nstages; ++s) {
+            mbar_inval(sm.full(s));
+            mbar_inval(sm.empty(s));
+          }
+          for (int b : {kDescFull0, kDescFull1, kDescFree0, kDescFree1, kNever})
+            mbar_inval(sm.fixed(b));
+        }
         fence_proxy_async();  // the ring held the hash table
         cluster_arrive();
         TcRole<T, R>::run(p, smem, starts, adapters, gcnt, tbase, ctl,
@@ -1011,17 +1036,6 @@ struct Kernel {
     }
     const int bid = static_cast<int>(blockIdx.x) - n_tc;  // index among the CUDA-core CTAs
     const int Nc = N - n_tc;
-    if (tid == 0) {
-      for (int s = 0; s < p.nstages; ++s) {
-        mbar_init(sm.full(s), 1);
-        mbar_init(sm.empty(s), kConsumerWarps);
-      }
-      mbar_init(sm.fixed(kDescFull0), 1);
-      mbar_init(sm.fixed(kDescFull1), 1);
-      mbar_init(sm.fixed(kDescFree0), kConsumerWarps);
-      mbar_init(sm.fixed(kDescFree1), kConsumerWarps);
-      mbar_init(sm.fixed(kNever), 1);
-    }
     // Group size E: as large as the launch cluster allows while every item still gets its own
     // group of CTAs (few items: split each across CTAs; many items: one CTA each, no exchange).
     Group grp;
