@@ -99,10 +99,11 @@ typedef enum {
  *   stream               CUDA stream the work is enqueued on
  * Execution: one kernel launch.  For fp16 / bf16 and r >= 16, an adapter group (all rows of
  * one adapter in the call) runs on the tensor cores (tcgen05.mma; section "Hardware-Level
- * Optimizations in SGMV": tensor-core tiles for long segments) when it has at least 64 rows
- * and the CUDA-core path would re-read at least 32 MB of its weights (ceil(rows / 4) x the
- * bytes of A_k and B_k); there the intermediate is kept as a 16-bit high part plus a 16-bit
- * low part, about 16 significant bits.  Every other group runs on the CUDA cores in fp32.
+ * Optimizations in SGMV": tensor-core tiles for long segments) when it fills at least one
+ * 128-row tile and the CUDA-core path would re-read at least 32 MB of its weights
+ * (ceil(rows / 4) x the bytes of A_k and B_k); there the intermediate is kept as a 16-bit high
+ * part plus a 16-bit low part, about 16 significant bits.  Every other group runs on the CUDA
+ * cores in fp32.
  * Returns SGMV_OK or a negative sgmv_status_t (nothing enqueued on a negative status other
  * than SGMV_ECUDA from the launch itself).
  */

@@ -51,7 +51,9 @@ struct Tuning {
   int stages = 0;     // 0: as many as shared memory holds
   int stage_kb = 24;  // ring stage size
   int budget_kb = 0;  // 0: 112 KB (two CTAs per SM), else the per-CTA shared-memory budget
-  int tc_min_rows = 64;  // adapter groups with at least this many rows use the tensor cores...
+  int tc_min_rows = 128;  // adapter groups of at least one full 128-row tile use the tensor
+                          // cores (a smaller group wastes tile rows and still repeats the
+                          // whole shrink in every CTA that shares the tile)...
   int tc_min_mb = 32;    // ...and whose CUDA-core items would re-read at least this many MB of
                          // weights (ceil(rows / 4) items x the adapter's A and B)
 };
@@ -355,7 +357,7 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
       const double w = static_cast<double>(pb.r) * (pb.h_in + pb.h_out) * 2.0;
       const double items = std::ceil(tuning().tc_min_mb * 1048576.0 / w);
       p.tc_min_rows = (flags & SGMV_TENSOR_CORES_ALWAYS)
-                          ? tuning().tc_min_rows
+                          ? 64
                           : static_cast<int>(std::min(
                                 1e9, std::max<double>(tuning().tc_min_rows, 4.0 * items)));
       p.tc_slots = slots;
