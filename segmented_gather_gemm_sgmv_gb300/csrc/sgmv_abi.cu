@@ -231,8 +231,8 @@ int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* sme
   // starts[S+1], adapters[S], base[S+1], gcnt[S], tbase[S+1]
   p.off_tab = static_cast<uint32_t>(off);
   off += up(4 * (5 * static_cast<size_t>(pb.S) + 3), 16);
-  p.off_vpart = static_cast<uint32_t>(off);
-  off += 2 * 4 * rmax * pb.r;
+  p.off_vpart = static_cast<uint32_t>(off);  // [2][kMaxGroup][rmax][r] fp32 partials
+  off += 2 * sgmv::kMaxGroup * 4 * rmax * pb.r;
   p.off_vfull = static_cast<uint32_t>(off);
   off += 4 * rmax * pb.r;
   p.off_red = static_cast<uint32_t>(off);

@@ -539,7 +539,10 @@ struct Kernel {
       return ring_u32 + static_cast<uint32_t>(s) * static_cast<uint32_t>(stage_bytes);
     }
     __device__ __forceinline__ int* desc(int b) const { return desc_p + b * desc_ints; }
-    __device__ __forceinline__ float* vpart(int b) const { return vpart_p + b * kRowsMax * R; }
+    // partial products of member m for item parity b: [2][kMaxGroup][kRowsMax][R]
+    __device__ __forceinline__ float* vpart(int b, int m) const {
+      return vpart_p + (b * kMaxGroup + m) * kRowsMax * R;
+    }
   };
 
   // The CTAs that share one item.
@@ -829,25 +832,28 @@ struct Kernel {
         }
         named_bar(1, kConsumers);
       } else {
-        float* vp = sm.vpart(li & 1);
+        // ------------------------------------------------- group all-reduce of v (DSMEM)
+        // Every member pushes its partial into slot m of every member's buffer with
+        // asynchronous stores that count bytes on that member's barrier; a member's barrier
+        // completes once all E partials have landed, and the member sums the slots locally in
+        // member order (deterministic).
+        if (li == 0) cluster_wait();  // peers' barriers are initialised (arrive #1)
+        const uint32_t vready = sm.fixed(kVReady0 + (li & 1));
+        if (tid == 0)
+          mbar_arrive_expect_tx(vready, static_cast<uint32_t>(grp.size * nrow * R * 4));
+        const uint32_t my_slot = smem_addr(sm.vpart(li & 1, grp.m));
         for (int t = tid; t < nrow * R; t += kConsumers) {
           float s = 0.f;
 #pragma unroll
           for (int ww = 0; ww < kConsumerWarps; ++ww) s += red[ww * kRowsMax * R + t];
-          vp[t] = s;
+          for (int j = 0; j < grp.size; ++j)
+            st_async_f32(cluster_map(my_slot + 4u * t, grp.rank0 + j), s,
+                         cluster_map(vready, grp.rank0 + j));
         }
-        named_bar(1, kConsumers);
-        // ------------------------------------------------- group all-reduce of v (DSMEM)
-        const uint32_t vready = sm.fixed(kVReady0 + (li & 1));
-        if (li == 0) cluster_wait();  // peers' barriers are initialised (arrive #1)
-        if (tid == 0)
-          for (int j = 0; j < grp.size; ++j) mbar_arrive_remote(vready, grp.rank0 + j);
         w.wait<true>(vready, (li >> 1) & 1);
-        const uint32_t vp_addr = smem_addr(vp);
         for (int t = tid; t < nrow * R; t += kConsumers) {
           float s = 0.f;
-          for (int j = 0; j < grp.size; ++j)
-            s += ld_cluster_f32(cluster_map(vp_addr + 4u * t, grp.rank0 + j));
+          for (int j = 0; j < grp.size; ++j) s += sm.vpart(li & 1, j)[t];
           if (MODE == kFused) {
             vfull[t] = s * p.scale;
           } else if ((t / R) % grp.size == grp.m && w.ok()) {
@@ -1099,8 +1105,8 @@ struct Kernel {
     grp.ng = Nc >> lg;
     grp.rank0 = (static_cast<int>(blockIdx.x) & (p.C - 1)) & ~(grp.size - 1);
     if (tid == 0) {
-      mbar_init(sm.fixed(kVReady0), grp.size);
-      mbar_init(sm.fixed(kVReady1), grp.size);
+      mbar_init(sm.fixed(kVReady0), 1);  // the member's own expect_tx arrival + E partials' bytes
+      mbar_init(sm.fixed(kVReady1), 1);
       fence_mbar_init();
     }
     fence_proxy_async();  // the ring held the hash table: order before bulk copies land
