@@ -54,6 +54,7 @@ struct Tuning {
   int tc_min_rows = 128;  // adapter groups of at least one full 128-row tile use the tensor
                           // cores (a smaller group wastes tile rows and still repeats the
                           // whole shrink in every CTA that shares the tile)...
+  int xchg_kb = 64;      // cost of one partial-sum exchange in streamed KB (group size rule)
   int tc_min_mb = 32;    // ...and whose CUDA-core items would re-read at least this many MB of
                          // weights (ceil(rows / 4) items x the adapter's A and B)
 };
@@ -65,6 +66,7 @@ Tuning read_tuning() {
   if (const char* s = std::getenv("SGMV_STAGE_KB")) t.stage_kb = std::max(4, std::atoi(s));
   if (const char* s = std::getenv("SGMV_TC_MIN_ROWS")) t.tc_min_rows = std::max(16, std::atoi(s));
   if (const char* s = std::getenv("SGMV_TC_MIN_MB")) t.tc_min_mb = std::max(0, std::atoi(s));
+  if (const char* s = std::getenv("SGMV_XCHG_KB")) t.xchg_kb = std::max(0, std::atoi(s));
   return t;
 }
 const Tuning& tuning() {
@@ -259,6 +261,7 @@ int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* sme
   if (off > budget) return SGMV_EUNSUPPORTED;
 
   p.C = C;
+  p.xchg_bytes = tu.xchg_kb * 1024;
   p.nstages = nst;
   p.stage_bytes = stage_bytes;
   p.kb = kb;
@@ -290,6 +293,14 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   const void* fn = kernel_for(pb.dtype, pb.mode, pb.r);
   if (!fn) return SGMV_EUNSUPPORTED;
   const bool clustered = pb.mode != sgmv::kExpand;
+  // Tensor role (fused, 16-bit types, r >= 16): it uses none of the CUDA-core scratch areas, so
+  // its row table sits at off_vpart and its ring of 24 KB slots right after it, up to the end of
+  // the budget (the launch then always takes the whole budget).
+  const uint32_t tc_base = static_cast<uint32_t>(
+      up(p.off_vpart + (2 * sgmv::kTcRows + 4) * sizeof(int), 1024));
+  const bool tc_capable = pb.mode == sgmv::kFused && pb.dtype != SGMV_F32 && pb.r >= 16 &&
+                          !(flags & SGMV_NO_TENSOR_CORES);
+  if (tc_capable && smem <= kPairSmem) smem = kPairSmem;
   int grid = 0;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -335,15 +346,14 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
     grid = kc.max_clusters * p.C;
   }
 
-  // Tensor role (fused, 16-bit types, r >= 16): ring slots of 24 KB in the ring region, the
-  // row table of two m-tiles in the CUDA-core scratch area, at least two clusters in the grid.
+  // Tensor role: at least three ring slots and two clusters in the grid.
   p.tc_min_rows = 0x7fffffff;
   p.tc_slots = 0;
-  if (pb.mode == sgmv::kFused && pb.dtype != SGMV_F32 && pb.r >= 16 &&
-      !(flags & SGMV_NO_TENSOR_CORES) && grid >= 2 * p.C) {
-    const int slots = std::min<int>(static_cast<int>((smem - p.off_ring) / sgmv::kTcSlot),
+  p.tc_base = tc_base;
+  if (tc_capable && grid >= 2 * p.C && smem > tc_base) {
+    const int slots = std::min<int>(static_cast<int>((smem - tc_base) / sgmv::kTcSlot),
                                     (2 * kMaxStages + sgmv::kNumFixedBars - sgmv::kTcNumFixed) / 2);
-    if (slots >= 3 && p.off_stab - p.off_vpart >= (2 * 128 + 2) * sizeof(int)) {
+    if (slots >= 3) {
       if (!encode_rows(&p.tmap_x128, p.x, pb.h_in, pb.dtype, 128) ||
           !encode_rows(&p.tmap_x8, p.x, pb.h_in, pb.dtype, 8) ||
           !encode_rows(&p.tmap_y128, p.y, pb.h_out, pb.dtype, 128) ||

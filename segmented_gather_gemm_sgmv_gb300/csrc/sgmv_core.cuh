@@ -96,7 +96,9 @@ struct Params {
   uint64_t wait_limit_ns;
   int32_t inject_stall;
   int32_t tc_min_rows;  // groups with at least this many rows go to the tensor role (INT32_MAX: none)
-  int32_t tc_slots;     // tensor-role ring slots (24 KB each) in the ring region
+  int32_t tc_slots;     // tensor-role ring slots (24 KB each)
+  uint32_t tc_base;     // tensor-role ring offset (1024-aligned; after its row table at off_vpart)
+  int32_t xchg_bytes;   // cost of one partial-sum exchange, in streamed bytes (group size rule)
   MemberPlan plan[kPlanSlots];
   // Tensor role: x [rows][h_in] and y [rows][h_out] with the 128-byte swizzle, boxes of
   // 64 elements x 128 rows (a whole m-tile) and 64 x 8 rows (one swizzle atom).
@@ -1083,13 +1085,13 @@ struct Kernel {
     const int Nc = N - n_tc;
     // Group size E: each item (one adapter's weights, W bytes) is split over E CTAs so that
     // the busiest CTA finishes first: minimise ceil(n_items E / Nc) x (W / E + X [E > 1]),
-    // X ~ 64 KB being the streaming time that the partial-sum exchange through distributed
-    // shared memory costs (measured: splitting 256 KB items four ways loses, 2 MB items win).
+    // X (host-set) being the streaming time, in bytes, that the partial-sum exchange through
+    // distributed shared memory costs.
     Group grp;
     grp.size = 1;
     {
       const long long W = static_cast<long long>(R) * (p.h_in + p.h_out) * kEb;
-      constexpr long long X = 64 * 1024;
+      const long long X = p.xchg_bytes;
       long long best = static_cast<long long>((n_items + Nc - 1) / Nc) * W;
       for (int e = 2; e <= p.C; e *= 2) {
         const long long cost = static_cast<long long>((n_items * e + Nc - 1) / Nc) * (W / e + X);

@@ -494,7 +494,7 @@ struct TcRole {
     const int tid = threadIdx.x, warp = tid >> 5;
     Ctx c;
     c.bars = smem_addr(smem + p.off_bars);
-    c.ring = smem_addr(smem + p.off_ring);
+    c.ring = smem_addr(smem + p.tc_base);
     c.slots = p.tc_slots;
     c.rowtok = reinterpret_cast<int*>(smem + p.off_vpart);
     c.tmask = c.rowtok + 2 * kTcRows;
