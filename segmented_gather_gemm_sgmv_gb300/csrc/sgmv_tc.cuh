@@ -544,9 +544,21 @@ struct TcRole {
 
     TcWalk wk;
     wk.ntile = (p.h_out + kTcN - 1) / kTcN;
-    const long long U = static_cast<long long>(n_mt) * wk.ntile;
-    wk.u = static_cast<int>(U * rank / n_tc);
-    wk.u1 = static_cast<int>(U * (rank + 1) / n_tc);
+    if (n_mt <= n_tc) {
+      // Fewer m-tiles than CTAs: every m-tile gets its own floor / ceil(n_tc / n_mt) CTAs,
+      // which split its n-tiles, so that no CTA repeats a second shrink.
+      const int mi = static_cast<int>(static_cast<long long>(rank) * n_mt / n_tc);
+      const int first = static_cast<int>((static_cast<long long>(mi) * n_tc + n_mt - 1) / n_mt);
+      const int next =
+          static_cast<int>((static_cast<long long>(mi + 1) * n_tc + n_mt - 1) / n_mt);
+      const int j = rank - first, cnt = next - first;
+      wk.u = mi * wk.ntile + j * wk.ntile / cnt;
+      wk.u1 = mi * wk.ntile + (j + 1) * wk.ntile / cnt;
+    } else {  // contiguous equal ranges of the (m-tile, n-tile) sequence
+      const long long U = static_cast<long long>(n_mt) * wk.ntile;
+      wk.u = static_cast<int>(U * rank / n_tc);
+      wk.u1 = static_cast<int>(U * (rank + 1) / n_tc);
+    }
 
     if (warp < 4) {
       loader(p, c, w, wk);
