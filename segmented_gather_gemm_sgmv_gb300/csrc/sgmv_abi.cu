@@ -357,7 +357,13 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
       if (!encode_rows(&p.tmap_x128, p.x, pb.h_in, pb.dtype, 128) ||
           !encode_rows(&p.tmap_x8, p.x, pb.h_in, pb.dtype, 8) ||
           !encode_rows(&p.tmap_y128, p.y, pb.h_out, pb.dtype, 128) ||
-          !encode_rows(&p.tmap_y8, p.y, pb.h_out, pb.dtype, 8))
+          !encode_rows(&p.tmap_y8, p.y, pb.h_out, pb.dtype, 8) ||
+          !encode_rows(&p.tmap_x64, p.x, pb.h_in, pb.dtype, 64) ||
+          !encode_rows(&p.tmap_x32, p.x, pb.h_in, pb.dtype, 32) ||
+          !encode_rows(&p.tmap_x16, p.x, pb.h_in, pb.dtype, 16) ||
+          !encode_rows(&p.tmap_y64, p.y, pb.h_out, pb.dtype, 64) ||
+          !encode_rows(&p.tmap_y32, p.y, pb.h_out, pb.dtype, 32) ||
+          !encode_rows(&p.tmap_y16, p.y, pb.h_out, pb.dtype, 16))
         return SGMV_ECUDA;
       // The CUDA-core path streams a group's weights once per item of 4 rows (mostly from
       // L2); the tensor path streams them once per 128-row tile but repeats the shrink in every

@@ -103,6 +103,8 @@ struct Params {
   // Tensor role: x [rows][h_in] and y [rows][h_out] with the 128-byte swizzle, boxes of
   // 64 elements x 128 rows (a whole m-tile) and 64 x 8 rows (one swizzle atom).
   TmaMap tmap_x128, tmap_x8, tmap_y128, tmap_y8;
+  // ... and 64 x 64 / 32 / 16 rows, for a tile whose rows are one shorter run (segment ends).
+  TmaMap tmap_x64, tmap_x32, tmap_x16, tmap_y64, tmap_y32, tmap_y16;
 };
 
 // ---- element types ---------------------------------------------------------------------

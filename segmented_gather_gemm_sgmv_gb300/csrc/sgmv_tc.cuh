@@ -186,6 +186,16 @@ struct TcRole {
         }
         uint32_t mask = __ballot_sync(0xffffffffu, run);
         if (__ballot_sync(0xffffffffu, line) == 0xffffu) mask |= 1u << 16;
+        // A shorter tile whose nrow rows are one run of consecutive tokens (a segment's end):
+        // its full 8-row blocks move by at most four boxes of 64 / 32 / 16 / 8 rows.
+        bool pre = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int m = lane + 32 * i;
+          pre = pre && (m >= nrow || rt[m] == rt[0] + m);
+        }
+        if (!((mask >> 16) & 1u) && nrow >= 8 && __all_sync(0xffffffffu, pre))
+          mask |= 1u << 17;
         if (lane == 0) {
           c.tmask[par] = static_cast<int>(mask);
           mbar_arrive(c.fx(kTcRtFull0 + par));
@@ -208,8 +218,20 @@ struct TcRole {
       const bool whole = (mask >> 16) & 1u;
       const bool all_boxes = whole || (mask & 0xffffu) == 0xffffu;
       const uint32_t tx = whole ? 128u * 128u : static_cast<uint32_t>(__popc(mask & 0xffffu)) * 1024u;
-      const bool my_box = !whole && lane < 16 && ((mask >> lane) & 1u);  // 8-row box `lane`
-      const int box_tok = my_box ? rt[8 * lane] : 0;
+      const bool run_tile = (mask >> 17) & 1u;
+      // 8-row box `lane` (gathered tiles), or for a run tile the box of 64 >> (lane - 1) rows
+      // (lanes 1-4, when that bit of the run's full-block length is set; larger boxes first)
+      int pbox = 0, prow = 0;
+      if (run_tile && lane >= 1 && lane <= 4) {
+        const int nb = nrow & ~7;
+        const int sz = 128 >> lane;
+        if (nb & sz) {
+          pbox = sz;
+          prow = nb & ~(2 * sz - 1);
+        }
+      }
+      const bool my_box = !whole && !run_tile && lane < 16 && ((mask >> lane) & 1u);
+      const int box_tok = my_box ? rt[8 * lane] : (pbox ? rt[prow] : 0);
       const int tile_tok = rt[0];
       const int k = c.adapters[lead];
       const T* Ak = static_cast<const T*>(p.A_ptrs[k]) +
@@ -227,6 +249,13 @@ struct TcRole {
           if (whole) tma_load_2d(dst, &p.tmap_x128, k0, tile_tok, bar);
         }
         if (my_box) tma_load_2d(dst + 1024u * lane, &p.tmap_x8, k0, box_tok, bar);
+        if (pbox) {
+          const uint32_t d = dst + 128u * prow;
+          if (pbox == 64) tma_load_2d(d, &p.tmap_x64, k0, box_tok, bar);
+          else if (pbox == 32) tma_load_2d(d, &p.tmap_x32, k0, box_tok, bar);
+          else if (pbox == 16) tma_load_2d(d, &p.tmap_x16, k0, box_tok, bar);
+          else tma_load_2d(d, &p.tmap_x8, k0, box_tok, bar);
+        }
         if (!all_boxes) {  // rows outside boxes, 16 bytes at a time
           for (int u = lane; u < kTcRows * 8; u += 32) {
             const int m = u >> 3, ch = u & 7;
@@ -264,6 +293,13 @@ struct TcRole {
           if (whole) tma_load_2d(dst + kYSlotOff, &p.tmap_y128, n0, tile_tok, bar);
         }
         if (my_box) tma_load_2d(dst + kYSlotOff + 1024u * lane, &p.tmap_y8, n0, box_tok, bar);
+        if (pbox) {
+          const uint32_t d = dst + kYSlotOff + 128u * prow;
+          if (pbox == 64) tma_load_2d(d, &p.tmap_y64, n0, box_tok, bar);
+          else if (pbox == 32) tma_load_2d(d, &p.tmap_y32, n0, box_tok, bar);
+          else if (pbox == 16) tma_load_2d(d, &p.tmap_y16, n0, box_tok, bar);
+          else tma_load_2d(d, &p.tmap_y8, n0, box_tok, bar);
+        }
 #pragma unroll 4
         for (int u = lane; u < R * 8; u += 32) {
           const int kr = u >> 3, cc = u & 7;
