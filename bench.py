@@ -242,24 +242,39 @@ def time_graph_steps(torch, setup, K, W, stream, world):
 
 
 def time_e2e(torch, setup, K, stream):
-    """Public-API path with pinned host buffers: per step H2D x, y_in, table; the call; D2H y."""
+    """Public-API path with pinned host buffers.  Per step: ONE host->device copy of the step's
+    inputs (x, y_in and the segment table packed in one pinned staging buffer), the lora_apply
+    call on views of the device copy, ONE device->host copy of y."""
     w = setup.w
     n = min(K, 2048)
     dt = workloads.torch_dtype(w.dtype)
-    xh = setup.x[0].cpu().pin_memory()
-    yh = setup.y[0].cpu().pin_memory()
-    ssh = torch.as_tensor(setup.ss).pin_memory()
-    sah = torch.as_tensor(setup.sa).pin_memory()
-    yout = torch.empty(yh.shape, dtype=dt).pin_memory()
-    xd, yd = torch.empty_like(setup.x[0]), torch.empty_like(setup.y[0])
-    ssd, sad = torch.empty_like(setup.d_ss), torch.empty_like(setup.d_sa)
+    x0, y0 = setup.x[0], setup.y[0]
+    eb = x0.element_size()
+
+    def up16(v):
+        return (v + 15) // 16 * 16
+
+    nx, ny = x0.numel() * eb, y0.numel() * eb
+    nss, nsa = 4 * len(setup.ss), 4 * len(setup.sa)
+    off_y = up16(nx)
+    off_ss = off_y + up16(ny)
+    off_sa = off_ss + up16(nss)
+    total = off_sa + up16(nsa)
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    host[0:nx].copy_(x0.cpu().contiguous().view(torch.uint8).view(-1))
+    host[off_y:off_y + ny].copy_(y0.cpu().contiguous().view(torch.uint8).view(-1))
+    host[off_ss:off_ss + nss].copy_(torch.as_tensor(setup.ss).view(torch.uint8))
+    host[off_sa:off_sa + nsa].copy_(torch.as_tensor(setup.sa).view(torch.uint8))
+    dev = torch.empty(total, dtype=torch.uint8, device=x0.device)
+    xd = dev[0:nx].view(dt).view(x0.shape)
+    yd = dev[off_y:off_y + ny].view(dt).view(y0.shape)
+    ssd = dev[off_ss:off_ss + nss].view(torch.int32)
+    sad = dev[off_sa:off_sa + nsa].view(torch.int32)
+    yout = torch.empty(y0.shape, dtype=dt).pin_memory()
     from segmented_gather_gemm_sgmv_gb300 import lora_apply
 
     def step(s):
-        xd.copy_(xh, non_blocking=True)
-        yd.copy_(yh, non_blocking=True)
-        ssd.copy_(ssh, non_blocking=True)
-        sad.copy_(sah, non_blocking=True)
+        dev.copy_(host, non_blocking=True)
         lora_apply(yd, xd, setup.A_ptrs, setup.B_ptrs, ssd, sad, s % w.layers, w.r, w.scale,
                    stream=stream, overlap_prior=setup.overlap, tensor_cores=setup.tensor_cores)
         yout.copy_(yd, non_blocking=True)
@@ -282,10 +297,7 @@ def time_e2e(torch, setup, K, stream):
         e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    h2d = xh.numel() * xh.element_size() + yh.numel() * yh.element_size() + 4 * (
-        ssh.numel() + sah.numel())
-    d2h = yout.numel() * yout.element_size()
-    return ms / (reps * per), h2d, d2h, reps * per
+    return ms / (reps * per), total, ny, reps * per
 
 
 def cpu_baseline(w, setup, seconds=10.0):
