@@ -155,6 +155,17 @@ int sgmv_shrink(float *v, const void *x, const void *const *A_ptrs, const int32_
                 int32_t h_in, int32_t r, sgmv_dtype_t dtype, sgmv_stream_t stream);
 
 /*
+ * sgmv_shrink_ex -- sgmv_shrink with the flags of lora_apply_ex (SGMV_OVERLAP_PRIOR,
+ * SGMV_NO_TENSOR_CORES, SGMV_TENSOR_CORES_ALWAYS; SGMV_EINVAL for others).  As in lora_apply,
+ * fp16 / bf16 groups that fill a 128-row tile and whose CUDA-core items would re-read at least
+ * 32 MB of A_k run on the tensor cores (v is then exact up to fp32 accumulation order).
+ */
+int sgmv_shrink_ex(float *v, const void *x, const void *const *A_ptrs,
+                   const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,
+                   int32_t layer_idx, int32_t h_in, int32_t r, sgmv_dtype_t dtype,
+                   uint32_t flags, sgmv_stream_t stream);
+
+/*
  * sgmv_expand -- y[t] += scale * v[t] . B_k for every segment row.  Source: the second factor
  * (x_i A_k) B_k of the y_i equation, times alpha/r, and the "one launch for all B projections"
  * of section "Mathematical Modeling ...", part 2.
@@ -166,6 +177,16 @@ int sgmv_shrink(float *v, const void *x, const void *const *A_ptrs, const int32_
 int sgmv_expand(void *y, const float *v, const void *const *B_ptrs, const int32_t *seg_starts,
                 const int32_t *seg_adapter, int32_t num_segments, int32_t layer_idx, int32_t r,
                 int32_t h_out, float scale, sgmv_dtype_t dtype, sgmv_stream_t stream);
+
+/*
+ * sgmv_expand_ex -- sgmv_expand with the flags of lora_apply_ex.  On the tensor cores (same
+ * routing rule, weights = B_k) scale * v enters the MMA as a 16-bit high part plus a 16-bit low
+ * part (about 16 significant bits), as in the fused path.
+ */
+int sgmv_expand_ex(void *y, const float *v, const void *const *B_ptrs,
+                   const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,
+                   int32_t layer_idx, int32_t r, int32_t h_out, float scale, sgmv_dtype_t dtype,
+                   uint32_t flags, sgmv_stream_t stream);
 
 /*
  * sgmv_validate -- checks a segment table on the device and writes an OR of these bits to

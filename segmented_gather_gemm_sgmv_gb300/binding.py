@@ -22,8 +22,9 @@ SGMV_MAX_HIDDEN = 65536
 SGMV_OVERLAP_PRIOR = 1
 SGMV_NO_TENSOR_CORES = 2
 SGMV_TENSOR_CORES_ALWAYS = 4
-SYMBOLS = ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_expand", "sgmv_validate", "sgmv_get_error",
-           "sgmv_set_wait_limit", "sgmv_status_string", "sgmv_version")
+SYMBOLS = ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_shrink_ex", "sgmv_expand",
+           "sgmv_expand_ex", "sgmv_validate", "sgmv_get_error", "sgmv_set_wait_limit",
+           "sgmv_status_string", "sgmv_version")
 
 
 class SgmvError(RuntimeError):
@@ -52,14 +53,19 @@ def lib(build_if_stale: bool = True) -> ctypes.CDLL:
                                     ctypes.c_int, ctypes.c_uint32, vp]
         L.sgmv_shrink.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp]
         L.sgmv_expand.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, ctypes.c_int, vp]
+        L.sgmv_shrink_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int,
+                                     ctypes.c_uint32, vp]
+        L.sgmv_expand_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, ctypes.c_int,
+                                     ctypes.c_uint32, vp]
         L.sgmv_validate.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         L.sgmv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
         L.sgmv_set_wait_limit.argtypes = [ctypes.c_uint64, i32]
         L.sgmv_status_string.argtypes = [ctypes.c_int]
         L.sgmv_status_string.restype = ctypes.c_char_p
         L.sgmv_version.argtypes = []
-        for name in ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_expand", "sgmv_validate",
-                     "sgmv_get_error", "sgmv_set_wait_limit", "sgmv_version"):
+        for name in ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_shrink_ex", "sgmv_expand",
+                     "sgmv_expand_ex", "sgmv_validate", "sgmv_get_error", "sgmv_set_wait_limit",
+                     "sgmv_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return L
@@ -112,6 +118,14 @@ def _ptrs(t, name):
     return t.data_ptr()
 
 
+def _flags(overlap_prior, tensor_cores) -> int:
+    mode = {True: "auto", False: "never"}.get(tensor_cores, tensor_cores)
+    if mode not in ("auto", "never", "always"):
+        raise ValueError(f"tensor_cores must be 'auto', 'never' or 'always', not {tensor_cores!r}")
+    return (SGMV_OVERLAP_PRIOR if overlap_prior else 0) | {
+        "auto": 0, "never": SGMV_NO_TENSOR_CORES, "always": SGMV_TENSOR_CORES_ALWAYS}[mode]
+
+
 def _check(rc: int, where: str):
     if rc != SGMV_OK:
         raise SgmvError(rc, where)
@@ -133,11 +147,7 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
     args = (y.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
             seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1],
             y.shape[1], int(r), float(scale), _dtype_code(x))
-    mode = {True: "auto", False: "never"}.get(tensor_cores, tensor_cores)
-    if mode not in ("auto", "never", "always"):
-        raise ValueError(f"tensor_cores must be 'auto', 'never' or 'always', not {tensor_cores!r}")
-    flags = (SGMV_OVERLAP_PRIOR if overlap_prior else 0) | {
-        "auto": 0, "never": SGMV_NO_TENSOR_CORES, "always": SGMV_TENSOR_CORES_ALWAYS}[mode]
+    flags = _flags(overlap_prior, tensor_cores)
     if flags:
         rc = lib().lora_apply_ex(*args, flags, _stream(stream, x.device))
         _check(rc, "lora_apply_ex")
@@ -147,32 +157,40 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
     return y
 
 
-def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None):
-    """v[t] = x[t] A_k (fp32) for every segment row."""
+def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None,
+                tensor_cores="auto"):
+    """v[t] = x[t] A_k (fp32) for every segment row (tensor_cores as for lora_apply)."""
     import torch
     _cuda(v, "v"), _cuda(x, "x")
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != x.shape[0]:
         raise ValueError("v must be float32 [M, r]")
     S = _table(seg_starts, seg_adapter)
-    rc = lib().sgmv_shrink(v.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"),
-                           seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx),
-                           x.shape[1], int(r), _dtype_code(x), _stream(stream, x.device))
-    _check(rc, "sgmv_shrink")
+    args = (v.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"), seg_starts.data_ptr(),
+            seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1], int(r), _dtype_code(x))
+    flags = _flags(False, tensor_cores)
+    if flags:
+        _check(lib().sgmv_shrink_ex(*args, flags, _stream(stream, x.device)), "sgmv_shrink_ex")
+    else:
+        _check(lib().sgmv_shrink(*args, _stream(stream, x.device)), "sgmv_shrink")
     return v
 
 
-def sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None):
+def sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None,
+                tensor_cores="auto"):
     """y[t] += scale * v[t] B_k for every segment row (in place on y)."""
     import torch
     _cuda(y, "y"), _cuda(v, "v")
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != y.shape[0]:
         raise ValueError("v must be float32 [M, r]")
     S = _table(seg_starts, seg_adapter)
-    rc = lib().sgmv_expand(y.data_ptr(), v.data_ptr(), _ptrs(B_ptrs, "B_ptrs"),
-                           seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx),
-                           int(r), y.shape[1], float(scale), _dtype_code(y),
-                           _stream(stream, y.device))
-    _check(rc, "sgmv_expand")
+    args = (y.data_ptr(), v.data_ptr(), _ptrs(B_ptrs, "B_ptrs"), seg_starts.data_ptr(),
+            seg_adapter.data_ptr(), S, int(layer_idx), int(r), y.shape[1], float(scale),
+            _dtype_code(y))
+    flags = _flags(False, tensor_cores)
+    if flags:
+        _check(lib().sgmv_expand_ex(*args, flags, _stream(stream, y.device)), "sgmv_expand_ex")
+    else:
+        _check(lib().sgmv_expand(*args, _stream(stream, y.device)), "sgmv_expand")
     return y
 
 

@@ -298,8 +298,7 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   // the budget (the launch then always takes the whole budget).
   const uint32_t tc_base = static_cast<uint32_t>(
       up(p.off_vpart + (2 * sgmv::kTcRows + 4) * sizeof(int), 1024));
-  const bool tc_capable = pb.mode == sgmv::kFused && pb.dtype != SGMV_F32 && pb.r >= 16 &&
-                          !(flags & SGMV_NO_TENSOR_CORES);
+  const bool tc_capable = pb.dtype != SGMV_F32 && pb.r >= 16 && !(flags & SGMV_NO_TENSOR_CORES);
   if (tc_capable && smem <= kPairSmem) smem = kPairSmem;
   int grid = 0;
   {
@@ -354,23 +353,26 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
     const int slots = std::min<int>(static_cast<int>((smem - tc_base) / sgmv::kTcSlot),
                                     (2 * kMaxStages + sgmv::kNumFixedBars - sgmv::kTcNumFixed) / 2);
     if (slots >= 3) {
-      if (!encode_rows(&p.tmap_x128, p.x, pb.h_in, pb.dtype, 128) ||
-          !encode_rows(&p.tmap_x8, p.x, pb.h_in, pb.dtype, 8) ||
-          !encode_rows(&p.tmap_y128, p.y, pb.h_out, pb.dtype, 128) ||
-          !encode_rows(&p.tmap_y8, p.y, pb.h_out, pb.dtype, 8) ||
-          !encode_rows(&p.tmap_x64, p.x, pb.h_in, pb.dtype, 64) ||
-          !encode_rows(&p.tmap_x32, p.x, pb.h_in, pb.dtype, 32) ||
-          !encode_rows(&p.tmap_x16, p.x, pb.h_in, pb.dtype, 16) ||
-          !encode_rows(&p.tmap_y64, p.y, pb.h_out, pb.dtype, 64) ||
-          !encode_rows(&p.tmap_y32, p.y, pb.h_out, pb.dtype, 32) ||
-          !encode_rows(&p.tmap_y16, p.y, pb.h_out, pb.dtype, 16))
+      const bool need_x = pb.mode != sgmv::kExpand, need_y = pb.mode != sgmv::kShrink;
+      if ((need_x && (!encode_rows(&p.tmap_x128, p.x, pb.h_in, pb.dtype, 128) ||
+                      !encode_rows(&p.tmap_x8, p.x, pb.h_in, pb.dtype, 8) ||
+                      !encode_rows(&p.tmap_x64, p.x, pb.h_in, pb.dtype, 64) ||
+                      !encode_rows(&p.tmap_x32, p.x, pb.h_in, pb.dtype, 32) ||
+                      !encode_rows(&p.tmap_x16, p.x, pb.h_in, pb.dtype, 16))) ||
+          (need_y && (!encode_rows(&p.tmap_y128, p.y, pb.h_out, pb.dtype, 128) ||
+                      !encode_rows(&p.tmap_y8, p.y, pb.h_out, pb.dtype, 8) ||
+                      !encode_rows(&p.tmap_y64, p.y, pb.h_out, pb.dtype, 64) ||
+                      !encode_rows(&p.tmap_y32, p.y, pb.h_out, pb.dtype, 32) ||
+                      !encode_rows(&p.tmap_y16, p.y, pb.h_out, pb.dtype, 16))))
         return SGMV_ECUDA;
       // The CUDA-core path streams a group's weights once per item of 4 rows (mostly from
       // L2); the tensor path streams them once per 128-row tile but repeats the shrink in every
       // CTA that shares a tile.  Measured on GB300: small-rank decode groups (256 rows, r = 16,
       // h = 4096: 17 MB of weight re-reads) run faster on the CUDA cores; prefill groups
       // (>= 128 rows, r = 64: >= 60 MB) several times faster on the tensor cores.
-      const double w = static_cast<double>(pb.r) * (pb.h_in + pb.h_out) * 2.0;
+      const double w = static_cast<double>(pb.r) * 2.0 *
+                       ((pb.mode != sgmv::kExpand ? pb.h_in : 0) +
+                        (pb.mode != sgmv::kShrink ? pb.h_out : 0));
       const double items = std::ceil(tuning().tc_min_mb * 1048576.0 / w);
       p.tc_min_rows = (flags & SGMV_TENSOR_CORES_ALWAYS)
                           ? 64
@@ -404,6 +406,13 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   void* args[] = {&p};
   if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SGMV_ECUDA;
   return SGMV_OK;
+}
+
+bool flags_ok(uint32_t flags) {
+  if (flags & ~static_cast<uint32_t>(SGMV_OVERLAP_PRIOR | SGMV_NO_TENSOR_CORES |
+                                     SGMV_TENSOR_CORES_ALWAYS))
+    return false;
+  return !((flags & SGMV_NO_TENSOR_CORES) && (flags & SGMV_TENSOR_CORES_ALWAYS));
 }
 
 int check_common(int num_segments, const void* seg_starts, const void* seg_adapter,
@@ -458,10 +467,7 @@ int lora_apply_ex(void* y, const void* x, const void* const* A_ptrs, const void*
                   const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
                   int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
                   sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream) {
-  if (flags & ~static_cast<uint32_t>(SGMV_OVERLAP_PRIOR | SGMV_NO_TENSOR_CORES |
-                                     SGMV_TENSOR_CORES_ALWAYS))
-    return SGMV_EINVAL;
-  if ((flags & SGMV_NO_TENSOR_CORES) && (flags & SGMV_TENSOR_CORES_ALWAYS)) return SGMV_EINVAL;
+  if (!flags_ok(flags)) return SGMV_EINVAL;
   int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
   if (rc != SGMV_OK) return rc;
   if (!y || !x || !A_ptrs || !B_ptrs) return SGMV_EINVAL;
@@ -484,6 +490,15 @@ int lora_apply_ex(void* y, const void* x, const void* const* A_ptrs, const void*
 int sgmv_shrink(float* v, const void* x, const void* const* A_ptrs, const int32_t* seg_starts,
                 const int32_t* seg_adapter, int32_t num_segments, int32_t layer_idx,
                 int32_t h_in, int32_t r, sgmv_dtype_t dtype, sgmv_stream_t stream) {
+  return sgmv_shrink_ex(v, x, A_ptrs, seg_starts, seg_adapter, num_segments, layer_idx, h_in, r,
+                        dtype, 0u, stream);
+}
+
+int sgmv_shrink_ex(float* v, const void* x, const void* const* A_ptrs,
+                   const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
+                   int32_t layer_idx, int32_t h_in, int32_t r, sgmv_dtype_t dtype,
+                   uint32_t flags, sgmv_stream_t stream) {
+  if (!flags_ok(flags)) return SGMV_EINVAL;
   int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
   if (rc != SGMV_OK) return rc;
   if (!v || !x || !A_ptrs) return SGMV_EINVAL;
@@ -498,12 +513,21 @@ int sgmv_shrink(float* v, const void* x, const void* const* A_ptrs, const int32_
   p.seg_starts = seg_starts;
   p.seg_adapter = seg_adapter;
   const Problem pb{sgmv::kShrink, dtype, r, num_segments, layer_idx, h_in, 8, 1.0f};
-  return launch(pb, p, 0u, reinterpret_cast<cudaStream_t>(stream));
+  return launch(pb, p, flags, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int sgmv_expand(void* y, const float* v, const void* const* B_ptrs, const int32_t* seg_starts,
                 const int32_t* seg_adapter, int32_t num_segments, int32_t layer_idx, int32_t r,
                 int32_t h_out, float scale, sgmv_dtype_t dtype, sgmv_stream_t stream) {
+  return sgmv_expand_ex(y, v, B_ptrs, seg_starts, seg_adapter, num_segments, layer_idx, r, h_out,
+                        scale, dtype, 0u, stream);
+}
+
+int sgmv_expand_ex(void* y, const float* v, const void* const* B_ptrs,
+                   const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
+                   int32_t layer_idx, int32_t r, int32_t h_out, float scale, sgmv_dtype_t dtype,
+                   uint32_t flags, sgmv_stream_t stream) {
+  if (!flags_ok(flags)) return SGMV_EINVAL;
   int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
   if (rc != SGMV_OK) return rc;
   if (!y || !v || !B_ptrs) return SGMV_EINVAL;
@@ -518,7 +542,7 @@ int sgmv_expand(void* y, const float* v, const void* const* B_ptrs, const int32_
   p.seg_starts = seg_starts;
   p.seg_adapter = seg_adapter;
   const Problem pb{sgmv::kExpand, dtype, r, num_segments, layer_idx, 8, h_out, scale};
-  return launch(pb, p, 0u, reinterpret_cast<cudaStream_t>(stream));
+  return launch(pb, p, flags, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int sgmv_validate(const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,

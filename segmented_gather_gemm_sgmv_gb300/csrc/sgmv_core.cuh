@@ -982,7 +982,7 @@ struct Kernel {
     }
   }
 
-  static constexpr bool kTensorRole = MODE == kFused && sizeof(T) == 2 && R >= 16;
+  static constexpr bool kTensorRole = sizeof(T) == 2 && R >= 16;
 
   // Number of CTAs (a multiple of the cluster size) that take the tensor role: all of them
   // when every group is long, else a share proportional to the estimated bytes of each side,
@@ -1019,8 +1019,8 @@ struct Kernel {
     const int clusters = N / p.C;
     int c_tc = __float2int_rn(static_cast<float>(clusters) * wtc / (wtc + wcc));
     c_tc = max(1, min(c_tc, clusters - 1));
-    const long long pairs =
-        static_cast<long long>(n_mt) * ((p.h_out + kTcN - 1) / kTcN);  // (m-tile, n-tile)
+    const long long pairs =  // (m-tile, n-tile) pairs (a shrink has one per m-tile)
+        static_cast<long long>(n_mt) * (MODE == kShrink ? 1 : (p.h_out + kTcN - 1) / kTcN);
     if (static_cast<long long>(c_tc) * p.C > pairs)
       c_tc = max(1, static_cast<int>(pairs / p.C));
     return c_tc * p.C;
@@ -1069,12 +1069,14 @@ struct Kernel {
             mbar_inval(sm.fixed(b));
         }
         fence_proxy_async();  // the ring held the hash table
-        cluster_arrive();
-        TcRole<T, R>::run(p, smem, starts, adapters, gcnt, tbase, ctl,
-                          static_cast<int>(blockIdx.x), n_tc, tbase[p.S]);
-        cluster_wait();
-        cluster_arrive();
-        cluster_wait();
+        if (MODE != kExpand) cluster_arrive();
+        TcRole<T, R, MODE>::run(p, smem, starts, adapters, gcnt, tbase, ctl,
+                                static_cast<int>(blockIdx.x), n_tc, tbase[p.S]);
+        if (MODE != kExpand) {
+          cluster_wait();
+          cluster_arrive();
+          cluster_wait();
+        }
         return;
       }
     }

@@ -1,4 +1,5 @@
-// sgmv_tc.cuh -- the tensor-core role of the fused kernel: adapter groups with many rows.
+// sgmv_tc.cuh -- the tensor-core role of the kernel (fused, shrink-only and expand-only):
+// adapter groups with many rows.
 //
 // Operation (Punica Guide: Multi-Tenant LoRA Serving with SGMV, section "The SGMV Mathematical
 // Formulation"; section "Hardware-Level Optimizations in SGMV" for the tensor-core tiles of
@@ -102,8 +103,12 @@ struct TcWalk {
   }
 };
 
-template <typename T, int R>
+template <typename T, int R, int MODE>
 struct TcRole {
+  // Fused: shrink, v kept in TMEM, expand.  Shrink only: v rows written to v_out (fp32).
+  // Expand only: v rows read from v_in (fp32) into TMEM, then the expand.
+  static constexpr bool kDoShrink = MODE != kExpand;
+  static constexpr bool kDoExpand = MODE != kShrink;
   static_assert(sizeof(T) == 2 && R >= 16 && R <= 64, "tensor role: 16-bit types, r >= 16");
   static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   // Shrink: N = 64 columns of v (columns >= r are never read).  Expand: N = 64 columns of y.
@@ -163,7 +168,7 @@ struct TcRole {
     const T* y = static_cast<const T*>(p.y);
     pdl_wait_prior();  // x and y may be written by the previous kernel of the stream
     Ring rg{0, 0};
-    const int nk = (p.h_in + kTcK - 1) / kTcK;
+    const int nk = kDoShrink ? (p.h_in + kTcK - 1) / kTcK : 0;
     bool ok = true;
     for (int li = 0; ok && wk.next(); ++li) {
       const int par = li & 1;
@@ -203,7 +208,7 @@ struct TcRole {
       }
       // A warp that fills no slot of this m-tile skips it (waiting for its row table could
       // otherwise leave the warp two phases behind that barrier).
-      const int n_sl = nk + (wk.b - wk.a);
+      const int n_sl = nk + (kDoExpand ? wk.b - wk.a : 0);
       bool mine = false;
       for (int i = 0, sl = rg.s; i < min(n_sl, c.slots); ++i) {
         mine = mine || (sl & 3) == warp;
@@ -234,10 +239,12 @@ struct TcRole {
       const int box_tok = my_box ? rt[8 * lane] : (pbox ? rt[prow] : 0);
       const int tile_tok = rt[0];
       const int k = c.adapters[lead];
-      const T* Ak = static_cast<const T*>(p.A_ptrs[k]) +
-                    static_cast<size_t>(p.layer) * p.h_in * R;
-      const T* Bk = static_cast<const T*>(p.B_ptrs[k]) +
-                    static_cast<size_t>(p.layer) * R * p.h_out;
+      const T* Ak = kDoShrink ? static_cast<const T*>(p.A_ptrs[k]) +
+                                    static_cast<size_t>(p.layer) * p.h_in * R
+                              : nullptr;
+      const T* Bk = kDoExpand ? static_cast<const T*>(p.B_ptrs[k]) +
+                                    static_cast<size_t>(p.layer) * R * p.h_out
+                              : nullptr;
       // shrink slots: x rows [128 x 64] + A rows [64 x r]
       for (int kc = 0; kc < nk; ++kc, rg.next(c.slots)) {
         if ((rg.s & 3) != warp) continue;
@@ -282,7 +289,7 @@ struct TcRole {
       }
       if (!ok) break;
       // expand slots: B rows [r x 64] + y rows [128 x 64]
-      for (int nt = wk.a; nt < wk.b; ++nt, rg.next(c.slots)) {
+      for (int nt = wk.a; kDoExpand && nt < wk.b; ++nt, rg.next(c.slots)) {
         if ((rg.s & 3) != warp) continue;
         if (!wwait(w, c.empty(rg.s), rg.par ^ 1u)) { ok = false; break; }
         const uint32_t dst = c.slot(rg.s), bar = c.full(rg.s);
@@ -327,7 +334,7 @@ struct TcRole {
     Ring rg{0, 0};
     int dq = 0;
     uint32_t dpar = 0;
-    const int nk = (p.h_in + kTcK - 1) / kTcK;
+    const int nk = kDoShrink ? (p.h_in + kTcK - 1) / kTcK : 0;
     for (int li = 0; wk.next(); ++li) {
       for (int kc = 0; kc < nk; ++kc) {
         if (!w.wait<false>(c.full(rg.s), rg.par)) return;
@@ -344,7 +351,8 @@ struct TcRole {
         mbar_arrive_n(c.empty(rg.s), 4);  // a shrink slot holds no y rows for the epilogue
         rg.next(c.slots);
       }
-      umma_commit(c.fx(kTcVFull));
+      if constexpr (kDoShrink) umma_commit(c.fx(kTcVFull));
+      if constexpr (!kDoExpand) continue;
       if (!w.wait<false>(c.fx(kTcHReady), li & 1)) return;
       tc_fence_after();
       for (int nt = wk.a; nt < wk.b; ++nt) {
@@ -384,20 +392,59 @@ struct TcRole {
     Ring rg{0, 0};
     int dq = 0;
     uint32_t dpar = 0;
-    const int nk = (p.h_in + kTcK - 1) / kTcK;
+    const int nk = kDoShrink ? (p.h_in + kTcK - 1) / kTcK : 0;
     for (int li = 0; wk.next(); ++li) {
       const int par = li & 1;
       if (!wwait(w, c.fx(kTcRtFull0 + par), (li >> 1) & 1)) return;
       const int* rt = c.rowtok + par * kTcRows;
-      // v -> scale -> hi + lo (16-bit each) -> TMEM
-      if (!wwait(w, c.fx(kTcVFull), li & 1)) return;
+      const int tok_row = rt[row];
+      if constexpr (MODE == kShrink) {
+        // v rows (fp32) -> v_out
+        if (!wwait(w, c.fx(kTcVFull), li & 1)) return;
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < R; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tq + kTmV + c0, v);
+          tmem_wait_ld();
+          if (tok_row >= 0) {
+            float4* dstv = reinterpret_cast<float4*>(p.v_out + static_cast<size_t>(tok_row) * R + c0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dstv[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                    __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(c.fx(kTcVFree));
+        mbar_arrive(c.fx(kTcRtFree0 + par));
+        continue;
+      }
+      // v -> scale -> hi + lo (16-bit each) -> TMEM; v from the shrink (TMEM) or from v_in
+      if constexpr (kDoShrink) {
+        if (!wwait(w, c.fx(kTcVFull), li & 1)) return;
+      }
       if (!wwait(w, c.fx(kTcHFree), (li & 1) ^ 1)) return;
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < R; c0 += 16) {
         uint32_t v[16], hi[8], lo[8];
-        tmem_ld16(tq + kTmV + c0, v);
-        tmem_wait_ld();
+        if constexpr (kDoShrink) {
+          tmem_ld16(tq + kTmV + c0, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (tok_row >= 0)
+              f = reinterpret_cast<const float4*>(p.v_in + static_cast<size_t>(tok_row) * R +
+                                                  c0)[e];
+            v[4 * e] = __float_as_uint(f.x);
+            v[4 * e + 1] = __float_as_uint(f.y);
+            v[4 * e + 2] = __float_as_uint(f.z);
+            v[4 * e + 3] = __float_as_uint(f.w);
+          }
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float a = p.scale * __uint_as_float(v[2 * e]);
@@ -409,7 +456,7 @@ struct TcRole {
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(c.fx(kTcVFree));
+      if constexpr (kDoShrink) mbar_arrive(c.fx(kTcVFree));
       mbar_arrive(c.fx(kTcHReady));
       // skip the shrink slots of this m-tile
       for (int kc = 0; kc < nk; ++kc) rg.next(c.slots);
@@ -579,7 +626,7 @@ struct TcRole {
     if (p.inject_stall) w.wait<false>(c.fx(kTcNever), 0);  // nothing completes it
 
     TcWalk wk;
-    wk.ntile = (p.h_out + kTcN - 1) / kTcN;
+    wk.ntile = kDoExpand ? (p.h_out + kTcN - 1) / kTcN : 1;
     if (n_mt <= n_tc) {
       // Fewer m-tiles than CTAs: every m-tile gets its own floor / ceil(n_tc / n_mt) CTAs,
       // which split its n-tiles, so that no CTA repeats a second shrink.

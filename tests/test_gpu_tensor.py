@@ -162,3 +162,35 @@ def test_large_table_gathered_group():
     ref = harness.oracle_apply(c, 0)
     harness.assert_close(y.float().cpu().numpy(), ref, "large table, tensor")
     harness.assert_close(y_cc.float().cpu().numpy(), ref, "large table, cuda cores")
+
+
+@pytest.mark.parametrize("dtype,r,h_in,h_out", [("bf16", 64, 512, 640), ("f16", 16, 200, 328),
+                                                ("bf16", 32, 1000, 136)])
+def test_unfused_shrink_and_expand_on_tensor_cores(dtype, r, h_in, h_out):
+    """sgmv_shrink_ex / sgmv_expand_ex with SGMV_TENSOR_CORES_ALWAYS: long groups run the
+    tensor role's shrink-only (v rows to v_out) and expand-only (v rows from v_in) forms;
+    compared with the oracle and with the CUDA-core forms of the same calls."""
+    import oracle
+    from segmented_gather_gemm_sgmv_gb300 import sgmv_expand, sgmv_shrink
+    w = workloads.Workload("tc_unfused", h_in, h_out, r, dtype, 6, 2)
+    ss, sa = _table(MIXED_LENS, MIXED_IDS)
+    c = harness.make_case(w, ss, sa, M=int(ss[-1]) + 3)
+    layer = 1
+    keys = harness.touched(sa, ss)
+    A = harness.oracle_blocks(c.A, keys, layer)
+    B = harness.oracle_blocks(c.B, keys, layer)
+    vs = {}
+    for mode in ("always", "never"):
+        v = torch.full((c.M, r), -7.0, device="cuda")
+        sgmv_shrink(v, c.x, c.A_ptrs, c.d_ss, c.d_sa, layer, r, tensor_cores=mode)
+        vs[mode] = v
+    v_ref = oracle.sgmv_shrink(np.full((c.M, r), -7.0), c.x.double().cpu().numpy(), A, ss, sa, 0)
+    for mode, v in vs.items():
+        harness.assert_close(v.cpu().numpy(), v_ref, f"shrink {mode}", atol=1e-3, rtol=1e-3)
+    v = vs["never"]
+    y_ref = oracle.sgmv_expand(c.y0.double().cpu().numpy(), v.double().cpu().numpy(), B, ss, sa,
+                               0, w.scale)
+    for mode in ("always", "never"):
+        y = c.y0.clone()
+        sgmv_expand(y, v, c.B_ptrs, c.d_ss, c.d_sa, layer, r, w.scale, tensor_cores=mode)
+        harness.assert_close(y.float().cpu().numpy(), y_ref, f"expand {mode}")
