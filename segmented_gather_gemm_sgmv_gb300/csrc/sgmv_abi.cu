@@ -349,9 +349,11 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   p.tc_min_rows = 0x7fffffff;
   p.tc_slots = 0;
   p.tc_base = tc_base;
-  if (tc_capable && grid >= 2 * p.C && smem > tc_base) {
-    const int slots = std::min<int>(static_cast<int>((smem - tc_base) / sgmv::kTcSlot),
+  const size_t xchg = pb.mode != sgmv::kExpand ? sgmv::kTcXchgBytes : 0;  // split-K buffers
+  if (tc_capable && grid >= 2 * p.C && smem > tc_base + xchg) {
+    const int slots = std::min<int>(static_cast<int>((smem - tc_base - xchg) / sgmv::kTcSlot),
                                     (2 * kMaxStages + sgmv::kNumFixedBars - sgmv::kTcNumFixed) / 2);
+    p.tc_xchg = tc_base + static_cast<uint32_t>(slots) * sgmv::kTcSlot;
     if (slots >= 3) {
       const bool need_x = pb.mode != sgmv::kExpand, need_y = pb.mode != sgmv::kShrink;
       if ((need_x && (!encode_rows(&p.tmap_x128, p.x, pb.h_in, pb.dtype, 128) ||

@@ -98,6 +98,7 @@ struct Params {
   int32_t tc_min_rows;  // groups with at least this many rows go to the tensor role (INT32_MAX: none)
   int32_t tc_slots;     // tensor-role ring slots (24 KB each)
   uint32_t tc_base;     // tensor-role ring offset (1024-aligned; after its row table at off_vpart)
+  uint32_t tc_xchg;     // tensor-role split-K exchange buffers (after the ring)
   int32_t xchg_bytes;   // cost of one partial-sum exchange, in streamed bytes (group size rule)
   MemberPlan plan[kPlanSlots];
   // Tensor role: x [rows][h_in] and y [rows][h_out] with the 128-byte swizzle, boxes of
@@ -1069,14 +1070,10 @@ struct Kernel {
             mbar_inval(sm.fixed(b));
         }
         fence_proxy_async();  // the ring held the hash table
-        if (MODE != kExpand) cluster_arrive();
+        // (the tensor role makes its own cluster barriers: one after its barriers are
+        // initialised, one before exit)
         TcRole<T, R, MODE>::run(p, smem, starts, adapters, gcnt, tbase, ctl,
                                 static_cast<int>(blockIdx.x), n_tc, tbase[p.S]);
-        if (MODE != kExpand) {
-          cluster_wait();
-          cluster_arrive();
-          cluster_wait();
-        }
         return;
       }
     }

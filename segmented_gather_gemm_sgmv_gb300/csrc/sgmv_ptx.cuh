@@ -152,6 +152,14 @@ static __device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t 
 }
 // Asynchronous store of 4 bytes into (possibly another CTA's) shared memory of the cluster that
 // completes 4 bytes of the transaction count of the mbarrier `mbar` in the same CTA as `addr`.
+static __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b,
+                                                   uint32_t c, uint32_t d, uint32_t mbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(mbar)
+      : "memory");
+}
 static __device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t mbar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(
                    addr),

@@ -47,7 +47,14 @@ constexpr int kTcEpi = 128;
 // Fixed barriers after the 2 * slots ring barriers.
 enum TcBar : int { kTcVFull = 0, kTcVFree, kTcHReady, kTcHFree, kTcDFull0, kTcDFull1,
                    kTcDEmpty0, kTcDEmpty1, kTcRtFull0, kTcRtFull1, kTcRtFree0, kTcRtFree1,
-                   kTcNever, kTcDrain, kTcNumFixed };
+                   kTcRsFull, kTcAgFull, kTcNever, kTcDrain, kTcNumFixed };
+
+// Split-K exchange between the 4 CTAs of a cluster, per round of 16 columns of v:
+// reduce-scatter buffer [3 senders][32 rows][16 fp32] and all-gather buffer
+// [3 owners][32 rows][16 hi + 16 lo 16-bit values].
+constexpr int kTcRowBytes = 64;
+constexpr int kTcHalfXchg = 3 * 32 * kTcRowBytes;  // 6144
+constexpr int kTcXchgBytes = 2 * kTcHalfXchg;
 
 // Byte offset of 16-byte chunk c of row m inside a block of 128-byte rows in the 128-byte
 // swizzle pattern (8-row atoms of 1024 bytes).
@@ -88,17 +95,27 @@ static __device__ __forceinline__ bool wwait(const Waiter& w, uint32_t bar, uint
   return __all_sync(0xffffffffu, w.wait<false>(bar, parity));
 }
 
-// The m-tiles of the CTA's range, walked identically by all roles.
+// The same, for barriers that other CTAs of the cluster complete (acquire at cluster scope).
+static __device__ __forceinline__ bool wwait_cluster(const Waiter& w, uint32_t bar,
+                                                     uint32_t parity) {
+  return __all_sync(0xffffffffu, w.wait<true>(bar, parity));
+}
+
+// The m-tiles of the CTA's (or, with the split-K shrink, its cluster's) range, walked
+// identically by all roles.  With the split, member cr takes quarter cr of each n-tile range.
 struct TcWalk {
   int u, u1;       // current / end position in the (m-tile, n-tile) sequence
   int ntile;       // n-tiles per m-tile
-  int mi, a, b;    // current m-tile and its n-tile range [a, b)
+  int split, cr;   // split-K cluster member cr of 4, or 0
+  int mi, a, b;    // current m-tile and this CTA's n-tile range [a, b) (may be empty)
   __device__ __forceinline__ bool next() {
     if (u >= u1) return false;
     mi = u / ntile;
-    a = u - mi * ntile;
-    b = min(ntile, a + (u1 - u));
-    u += b - a;
+    const int ca = u - mi * ntile;
+    const int cb = min(ntile, ca + (u1 - u));
+    u += cb - ca;
+    a = split ? ca + (cb - ca) * cr / 4 : ca;
+    b = split ? ca + (cb - ca) * (cr + 1) / 4 : cb;
     return true;
   }
 };
@@ -121,6 +138,9 @@ struct TcRole {
     uint32_t bars, ring;
     int slots;
     int* rowtok;  // [2][128]
+    uint32_t xchg;   // split-K exchange buffers
+    int cr, split;   // cluster member, split-K shrink on
+    int k_lo, k_hi;  // this CTA's shrink chunks
     int* tmask;   // [2]: 8-row blocks moved as one TMA box
     const int *starts, *adapters, *gcnt, *tbase;
     __device__ __forceinline__ uint32_t full(int s) const { return bars + 8u * s; }
@@ -168,7 +188,6 @@ struct TcRole {
     const T* y = static_cast<const T*>(p.y);
     pdl_wait_prior();  // x and y may be written by the previous kernel of the stream
     Ring rg{0, 0};
-    const int nk = kDoShrink ? (p.h_in + kTcK - 1) / kTcK : 0;
     bool ok = true;
     for (int li = 0; ok && wk.next(); ++li) {
       const int par = li & 1;
@@ -206,9 +225,12 @@ struct TcRole {
           mbar_arrive(c.fx(kTcRtFull0 + par));
         }
       }
-      // A warp that fills no slot of this m-tile skips it (waiting for its row table could
-      // otherwise leave the warp two phases behind that barrier).
-      const int n_sl = nk + (kDoExpand ? wk.b - wk.a : 0);
+      // Every loader warp takes every table hand-off in order and releases the table when it
+      // is done with it (the table's "free" barrier counts the four loader warps too), so that
+      // no warp can run ahead of, or fall two phases behind, the table barriers -- even a warp
+      // that fills no slot of this m-tile.
+      if (!wwait(w, c.fx(kTcRtFull0 + par), (li >> 1) & 1)) break;
+      const int n_sl = (c.k_hi - c.k_lo) + (kDoExpand ? wk.b - wk.a : 0);
       bool mine = false;
       for (int i = 0, sl = rg.s; i < min(n_sl, c.slots); ++i) {
         mine = mine || (sl & 3) == warp;
@@ -216,9 +238,10 @@ struct TcRole {
       }
       if (!mine) {
         for (int i = 0; i < n_sl; ++i) rg.next(c.slots);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.fx(kTcRtFree0 + par));
         continue;
       }
-      if (!wwait(w, c.fx(kTcRtFull0 + par), (li >> 1) & 1)) break;
       const uint32_t mask = static_cast<uint32_t>(c.tmask[par]);
       const bool whole = (mask >> 16) & 1u;
       const bool all_boxes = whole || (mask & 0xffffu) == 0xffffu;
@@ -246,7 +269,7 @@ struct TcRole {
                                     static_cast<size_t>(p.layer) * R * p.h_out
                               : nullptr;
       // shrink slots: x rows [128 x 64] + A rows [64 x r]
-      for (int kc = 0; kc < nk; ++kc, rg.next(c.slots)) {
+      for (int kc = c.k_lo; kc < c.k_hi; ++kc, rg.next(c.slots)) {
         if ((rg.s & 3) != warp) continue;
         if (!wwait(w, c.empty(rg.s), rg.par ^ 1u)) { ok = false; break; }
         const uint32_t dst = c.slot(rg.s), bar = c.full(rg.s);
@@ -324,6 +347,8 @@ struct TcRole {
         }
         cp_async_arrive(bar);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.fx(kTcRtFree0 + par));
     }
     cp_async_wait_all();  // every copy lands before the CTA moves on
   }
@@ -334,11 +359,13 @@ struct TcRole {
     Ring rg{0, 0};
     int dq = 0;
     uint32_t dpar = 0;
-    const int nk = kDoShrink ? (p.h_in + kTcK - 1) / kTcK : 0;
     for (int li = 0; wk.next(); ++li) {
-      for (int kc = 0; kc < nk; ++kc) {
+      // The previous tile's v has been read out of TMEM -- waited for every tile, even by a
+      // split-K member with no chunks to multiply, so that the issuer never runs two phases
+      // ahead of the epilogue on the v barriers.
+      if (kDoShrink && !w.wait<false>(c.fx(kTcVFree), (li & 1) ^ 1)) return;
+      for (int kc = c.k_lo; kc < c.k_hi; ++kc) {
         if (!w.wait<false>(c.full(rg.s), rg.par)) return;
-        if (kc == 0 && !w.wait<false>(c.fx(kTcVFree), (li & 1) ^ 1)) return;
         fence_proxy_async();  // cp.async (generic proxy) data -> the MMA's async-proxy reads
         tc_fence_after();
         const uint32_t sa = c.slot(rg.s);
@@ -346,7 +373,7 @@ struct TcRole {
         for (int j = 0; j < kTcK / 16; ++j)
           umma_ss(tm + kTmV, sdesc_sw128(sa + 32u * j, 16, 1024),
                   sdesc_sw128(sa + kASlotOff + 2048u * j, 8192, 1024), kIdShrink,
-                  (kc | j) != 0);
+                  kc != c.k_lo || j != 0);
         umma_commit(c.empty(rg.s));
         mbar_arrive_n(c.empty(rg.s), 4);  // a shrink slot holds no y rows for the epilogue
         rg.next(c.slots);
@@ -380,6 +407,129 @@ struct TcRole {
     }
   }
 
+  // 16 columns [c0, c0 + 16) of this thread's v row (fp32): shrink only -> v_out; otherwise
+  // scale -> 16-bit hi + lo -> TMEM.
+  __device__ __forceinline__ static void finish16(const Params& p, uint32_t tq, int c0,
+                                                  const uint32_t (&v)[16], int tok_row) {
+    if constexpr (MODE == kShrink) {
+      if (tok_row >= 0) {
+        float4* dst = reinterpret_cast<float4*>(p.v_out + static_cast<size_t>(tok_row) * R + c0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                               __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+      }
+    } else {
+      uint32_t hi[8], lo[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        split2(p.scale * __uint_as_float(v[2 * e]), p.scale * __uint_as_float(v[2 * e + 1]),
+               hi[e], lo[e]);
+      tmem_st8(tq + kTmHi + c0 / 2, hi);
+      tmem_st8(tq + kTmLo + c0 / 2, lo);
+    }
+  }
+
+  // Split-K shrink: this CTA (member cr of the cluster) holds the partial v of its quarter of
+  // h_in for all 128 rows; member q owns rows [32q, 32q + 32).  Per round of 16 columns: every
+  // epilogue warp q != cr pushes its rows' partial to member q (st.async, counted on q's
+  // reduce barrier); warp cr (the owner) sums the four partials in member order, finishes its
+  // rows, and pushes their hi / lo to the other members (counted on their gather barrier; in
+  // a shrink, a 4-byte acknowledgement instead).  A warp starts round j + 1 only after the
+  // gather barrier of round j completed, which proves that every buffer it writes next has
+  // been read.
+  __device__ __forceinline__ static bool exchange(const Params& p, const Ctx& c, const Waiter& w,
+                                                  uint32_t tq, int q, int lane, int tok_row,
+                                                  uint32_t rnd) {
+    const bool has_k = c.k_hi > c.k_lo;
+    const uint32_t rs = c.xchg, ag = c.xchg + kTcHalfXchg;
+    for (int j = 0; j < R / 16; ++j) {
+      const uint32_t ph = (rnd + j) & 1u;
+      uint32_t pv[16];
+      if (has_k) {
+        tmem_ld16(tq + kTmV + 16 * j, pv);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pv[e] = 0u;
+      }
+      if (q != c.cr) {
+        const int sslot = c.cr < q ? c.cr : c.cr - 1;
+        const uint32_t dst = cluster_map(rs + static_cast<uint32_t>((sslot * 32 + lane) * kTcRowBytes), q);
+        const uint32_t rb = cluster_map(c.fx(kTcRsFull), q);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          st_async_v4(dst + 16u * e, pv[4 * e], pv[4 * e + 1], pv[4 * e + 2], pv[4 * e + 3], rb);
+        if (!wwait_cluster(w, c.fx(kTcAgFull), ph)) return false;
+        if constexpr (MODE == kFused) {
+          const int tslot = q < c.cr ? q : q - 1;
+          const uint32_t src = ag + static_cast<uint32_t>((tslot * 32 + lane) * kTcRowBytes);
+          const uint4 h0 = lds128(src), h1 = lds128(src + 16), l0 = lds128(src + 32),
+                      l1 = lds128(src + 48);
+          const uint32_t hi[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+          const uint32_t lo[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+          tmem_st8(tq + kTmHi + 8 * j, hi);
+          tmem_st8(tq + kTmLo + 8 * j, lo);
+        }
+      } else {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(c.fx(kTcRsFull), kTcHalfXchg);
+          mbar_arrive_expect_tx(c.fx(kTcAgFull), MODE == kFused ? kTcHalfXchg : 3 * 4);
+        }
+        if (!wwait_cluster(w, c.fx(kTcRsFull), ph)) return false;
+        float sum[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sum[e] = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          if (m == c.cr) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sum[e] += __uint_as_float(pv[e]);
+          } else {
+            const int sl = m < c.cr ? m : m - 1;
+            const uint32_t src = rs + static_cast<uint32_t>((sl * 32 + lane) * kTcRowBytes);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint4 t = lds128(src + 16u * e);
+              sum[4 * e] += __uint_as_float(t.x);
+              sum[4 * e + 1] += __uint_as_float(t.y);
+              sum[4 * e + 2] += __uint_as_float(t.z);
+              sum[4 * e + 3] += __uint_as_float(t.w);
+            }
+          }
+        }
+        uint32_t v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(sum[e]);
+        finish16(p, tq, 16 * j, v, tok_row);
+        if constexpr (MODE == kFused) {
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            split2(p.scale * sum[2 * e], p.scale * sum[2 * e + 1], hi[e], lo[e]);
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            if (pp == c.cr) continue;
+            const int tslot = c.cr < pp ? c.cr : c.cr - 1;
+            const uint32_t dst =
+                cluster_map(ag + static_cast<uint32_t>((tslot * 32 + lane) * kTcRowBytes), pp);
+            const uint32_t gb = cluster_map(c.fx(kTcAgFull), pp);
+            st_async_v4(dst, hi[0], hi[1], hi[2], hi[3], gb);
+            st_async_v4(dst + 16, hi[4], hi[5], hi[6], hi[7], gb);
+            st_async_v4(dst + 32, lo[0], lo[1], lo[2], lo[3], gb);
+            st_async_v4(dst + 48, lo[4], lo[5], lo[6], lo[7], gb);
+          }
+        } else if (lane == 0) {
+          for (int pp = 0; pp < 4; ++pp)
+            if (pp != c.cr)
+              st_async_f32(cluster_map(ag, pp), 0.f, cluster_map(c.fx(kTcAgFull), pp));
+        }
+        if (!wwait_cluster(w, c.fx(kTcAgFull), ph)) return false;
+      }
+    }
+    return true;
+  }
+
   // ------------------------------------------------------------------------ epilogue ----
   __device__ __forceinline__ static void epilogue(const Params& p, const Ctx& c, const Waiter& w,
                                                   TcWalk wk, uint32_t tm) {
@@ -392,47 +542,36 @@ struct TcRole {
     Ring rg{0, 0};
     int dq = 0;
     uint32_t dpar = 0;
-    const int nk = kDoShrink ? (p.h_in + kTcK - 1) / kTcK : 0;
+    uint32_t rnd = 0;  // split-K exchange rounds so far (barrier parity)
     for (int li = 0; wk.next(); ++li) {
       const int par = li & 1;
       if (!wwait(w, c.fx(kTcRtFull0 + par), (li >> 1) & 1)) return;
       const int* rt = c.rowtok + par * kTcRows;
       const int tok_row = rt[row];
-      if constexpr (MODE == kShrink) {
-        // v rows (fp32) -> v_out
-        if (!wwait(w, c.fx(kTcVFull), li & 1)) return;
-        tc_fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < R; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(tq + kTmV + c0, v);
-          tmem_wait_ld();
-          if (tok_row >= 0) {
-            float4* dstv = reinterpret_cast<float4*>(p.v_out + static_cast<size_t>(tok_row) * R + c0);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dstv[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                    __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(c.fx(kTcVFree));
-        mbar_arrive(c.fx(kTcRtFree0 + par));
-        continue;
-      }
-      // v -> scale -> hi + lo (16-bit each) -> TMEM; v from the shrink (TMEM) or from v_in
       if constexpr (kDoShrink) {
         if (!wwait(w, c.fx(kTcVFull), li & 1)) return;
       }
-      if (!wwait(w, c.fx(kTcHFree), (li & 1) ^ 1)) return;
+      if constexpr (kDoExpand) {
+        if (!wwait(w, c.fx(kTcHFree), (li & 1) ^ 1)) return;
+      }
       tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < R; c0 += 16) {
-        uint32_t v[16], hi[8], lo[8];
-        if constexpr (kDoShrink) {
-          tmem_ld16(tq + kTmV + c0, v);
-          tmem_wait_ld();
+      if constexpr (kDoShrink) {
+        if (c.split) {
+          if (!exchange(p, c, w, tq, q, lane, tok_row, rnd)) return;
+          rnd += R / 16;
         } else {
+#pragma unroll
+          for (int c0 = 0; c0 < R; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tq + kTmV + c0, v);
+            tmem_wait_ld();
+            finish16(p, tq, c0, v, tok_row);
+          }
+        }
+      } else {  // expand only: v rows from v_in
+#pragma unroll
+        for (int c0 = 0; c0 < R; c0 += 16) {
+          uint32_t v[16];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -444,22 +583,19 @@ struct TcRole {
             v[4 * e + 2] = __float_as_uint(f.z);
             v[4 * e + 3] = __float_as_uint(f.w);
           }
+          finish16(p, tq, c0, v, tok_row);
         }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float a = p.scale * __uint_as_float(v[2 * e]);
-          const float b = p.scale * __uint_as_float(v[2 * e + 1]);
-          split2(a, b, hi[e], lo[e]);
-        }
-        tmem_st8(tq + kTmHi + c0 / 2, hi);
-        tmem_st8(tq + kTmLo + c0 / 2, lo);
       }
-      tmem_wait_st();
+      if constexpr (kDoExpand) tmem_wait_st();
       tc_fence_before();
       if constexpr (kDoShrink) mbar_arrive(c.fx(kTcVFree));
+      if constexpr (MODE == kShrink) {
+        mbar_arrive(c.fx(kTcRtFree0 + par));
+        continue;
+      }
       mbar_arrive(c.fx(kTcHReady));
       // skip the shrink slots of this m-tile
-      for (int kc = 0; kc < nk; ++kc) rg.next(c.slots);
+      for (int kc = c.k_lo; kc < c.k_hi; ++kc) rg.next(c.slots);
       const uint32_t mask = static_cast<uint32_t>(c.tmask[par]);
       int pend = -1;  // ring slot whose TMA stores may still be reading it
       for (int nt = wk.a; nt < wk.b; ++nt) {
@@ -585,6 +721,16 @@ struct TcRole {
     c.adapters = adapters;
     c.gcnt = gcnt;
     c.tbase = tbase;
+    c.xchg = smem_addr(smem + p.tc_xchg);
+    // Split-K shrink over the 4 CTAs of a cluster (fused and shrink forms): member cr shrinks
+    // chunks [nk cr / 4, nk (cr + 1) / 4) of h_in.
+    c.split = kDoShrink ? 1 : 0;
+    c.cr = c.split ? (rank & 3) : 0;
+    {
+      const int nk = kDoShrink ? (p.h_in + kTcK - 1) / kTcK : 0;
+      c.k_lo = c.split ? nk * c.cr / 4 : 0;
+      c.k_hi = c.split ? nk * (c.cr + 1) / 4 : nk;
+    }
     uint32_t* tslot = reinterpret_cast<uint32_t*>(ctl + 1);
     if (tid == 0) {
       for (int s = 0; s < c.slots; ++s) {
@@ -601,8 +747,10 @@ struct TcRole {
       mbar_init(c.fx(kTcDEmpty1), 4);
       mbar_init(c.fx(kTcRtFull0), 1);
       mbar_init(c.fx(kTcRtFull1), 1);
-      mbar_init(c.fx(kTcRtFree0), kTcEpi);
-      mbar_init(c.fx(kTcRtFree1), kTcEpi);
+      mbar_init(c.fx(kTcRtFree0), kTcEpi + 4);  // epilogue threads + the four loader warps
+      mbar_init(c.fx(kTcRtFree1), kTcEpi + 4);
+      mbar_init(c.fx(kTcRsFull), 1);  // the owner's expect_tx arrival + three partials' bytes
+      mbar_init(c.fx(kTcAgFull), 1);  // the owner's expect_tx arrival + three owners' bytes
       mbar_init(c.fx(kTcNever), 1);
       mbar_init(c.fx(kTcDrain), 1);
       fence_mbar_init();
@@ -615,6 +763,7 @@ struct TcRole {
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tslot;
+    if (c.split) cluster_sync_all();  // every member's barriers exist before the first st.async
 
     if (tid == 0) {
       tma_prefetch_desc(&p.tmap_x128);
@@ -627,20 +776,27 @@ struct TcRole {
 
     TcWalk wk;
     wk.ntile = kDoExpand ? (p.h_out + kTcN - 1) / kTcN : 1;
-    if (n_mt <= n_tc) {
-      // Fewer m-tiles than CTAs: every m-tile gets its own floor / ceil(n_tc / n_mt) CTAs,
-      // which split its n-tiles, so that no CTA repeats a second shrink.
-      const int mi = static_cast<int>(static_cast<long long>(rank) * n_mt / n_tc);
-      const int first = static_cast<int>((static_cast<long long>(mi) * n_tc + n_mt - 1) / n_mt);
+    wk.split = c.split;
+    wk.cr = c.cr;
+    // Work units: clusters with the split-K shrink (all members walk the cluster's range),
+    // single CTAs otherwise.
+    const int unit = c.split ? rank >> 2 : rank;
+    const int n_units = c.split ? n_tc >> 2 : n_tc;
+    if (n_mt <= n_units) {
+      // Fewer m-tiles than units: every m-tile gets its own floor / ceil(n_units / n_mt)
+      // units, which split its n-tiles, so that no unit repeats a second shrink.
+      const int mi = static_cast<int>(static_cast<long long>(unit) * n_mt / n_units);
+      const int first =
+          static_cast<int>((static_cast<long long>(mi) * n_units + n_mt - 1) / n_mt);
       const int next =
-          static_cast<int>((static_cast<long long>(mi + 1) * n_tc + n_mt - 1) / n_mt);
-      const int j = rank - first, cnt = next - first;
+          static_cast<int>((static_cast<long long>(mi + 1) * n_units + n_mt - 1) / n_mt);
+      const int j = unit - first, cnt = next - first;
       wk.u = mi * wk.ntile + j * wk.ntile / cnt;
       wk.u1 = mi * wk.ntile + (j + 1) * wk.ntile / cnt;
     } else {  // contiguous equal ranges of the (m-tile, n-tile) sequence
       const long long U = static_cast<long long>(n_mt) * wk.ntile;
-      wk.u = static_cast<int>(U * rank / n_tc);
-      wk.u1 = static_cast<int>(U * (rank + 1) / n_tc);
+      wk.u = static_cast<int>(U * unit / n_units);
+      wk.u1 = static_cast<int>(U * (unit + 1) / n_units);
     }
 
     if (warp < 4) {
@@ -659,6 +815,7 @@ struct TcRole {
     __syncthreads();
     tc_fence_after();
     if (warp == kConsumerWarps) tmem_dealloc(tm, kTcCols);
+    if (c.split) cluster_sync_all();  // no member leaves while a peer may still write to it
   }
 };
 

@@ -47,6 +47,7 @@ MIXED_IDS = [1, 4, 3, 2, 0, 2, 2, 1, 5, 1, -1]
     ("f16", 16, 200, 328),     # ragged K chunk and ragged n-tile
     ("bf16", 32, 1000, 136),
     ("f16", 64, 264, 4104),
+    ("bf16", 64, 128, 200),    # two K chunks: two of the four split-K members shrink nothing
 ])
 def test_mixed_groups_match_oracle_and_cuda_cores(dtype, r, h_in, h_out):
     w = workloads.Workload("tc_mixed", h_in, h_out, r, dtype, 6, 2)
@@ -165,7 +166,7 @@ def test_large_table_gathered_group():
 
 
 @pytest.mark.parametrize("dtype,r,h_in,h_out", [("bf16", 64, 512, 640), ("f16", 16, 200, 328),
-                                                ("bf16", 32, 1000, 136)])
+                                                ("bf16", 32, 1000, 136), ("f16", 32, 128, 72)])
 def test_unfused_shrink_and_expand_on_tensor_cores(dtype, r, h_in, h_out):
     """sgmv_shrink_ex / sgmv_expand_ex with SGMV_TENSOR_CORES_ALWAYS: long groups run the
     tensor role's shrink-only (v rows to v_out) and expand-only (v rows from v_in) forms;
