@@ -99,8 +99,8 @@ typedef enum {
  *   stream               CUDA stream the work is enqueued on
  * Execution: one kernel launch.  For fp16 / bf16 and r >= 16, an adapter group (all rows of
  * one adapter in the call) runs on the tensor cores (tcgen05.mma; section "Hardware-Level
- * Optimizations in SGMV": tensor-core tiles for long segments) when it fills at least one
- * 128-row tile and the CUDA-core path would re-read at least 32 MB of its weights
+ * Optimizations in SGMV": tensor-core tiles for long segments) when it has at least 64 rows
+ * (half a 128-row tile) and the CUDA-core path would re-read at least 32 MB of its weights
  * (ceil(rows / 4) x the bytes of A_k and B_k); there the intermediate is kept as a 16-bit high
  * part plus a 16-bit low part, about 16 significant bits.  Every other group runs on the CUDA
  * cores in fp32.
@@ -157,8 +157,8 @@ int sgmv_shrink(float *v, const void *x, const void *const *A_ptrs, const int32_
 /*
  * sgmv_shrink_ex -- sgmv_shrink with the flags of lora_apply_ex (SGMV_OVERLAP_PRIOR,
  * SGMV_NO_TENSOR_CORES, SGMV_TENSOR_CORES_ALWAYS; SGMV_EINVAL for others).  As in lora_apply,
- * fp16 / bf16 groups that fill a 128-row tile and whose CUDA-core items would re-read at least
- * 32 MB of A_k run on the tensor cores (v is then exact up to fp32 accumulation order).
+ * fp16 / bf16 groups of at least 64 rows whose CUDA-core items would re-read at least 32 MB of
+ * A_k run on the tensor cores (v is then exact up to fp32 accumulation order).
  */
 int sgmv_shrink_ex(float *v, const void *x, const void *const *A_ptrs,
                    const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,

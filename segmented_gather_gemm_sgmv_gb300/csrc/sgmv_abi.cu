@@ -51,9 +51,8 @@ struct Tuning {
   int stages = 0;     // 0: as many as shared memory holds
   int stage_kb = 24;  // ring stage size
   int budget_kb = 0;  // 0: 112 KB (two CTAs per SM), else the per-CTA shared-memory budget
-  int tc_min_rows = 128;  // adapter groups of at least one full 128-row tile use the tensor
-                          // cores (a smaller group wastes tile rows and still repeats the
-                          // whole shrink in every CTA that shares the tile)...
+  int tc_min_rows = 64;  // adapter groups of at least half a 128-row tile use the tensor
+                         // cores (measured: 64 beats 128 on the 70B mix, 16 and 32 tie)...
   int xchg_kb = 64;      // cost of one partial-sum exchange in streamed KB (group size rule)
   int tc_min_mb = 32;    // ...and whose CUDA-core items would re-read at least this many MB of
                          // weights (ceil(rows / 4) items x the adapter's A and B)
@@ -368,10 +367,10 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
                       !encode_rows(&p.tmap_y16, p.y, pb.h_out, pb.dtype, 16))))
         return SGMV_ECUDA;
       // The CUDA-core path streams a group's weights once per item of 4 rows (mostly from
-      // L2); the tensor path streams them once per 128-row tile but repeats the shrink in every
-      // CTA that shares a tile.  Measured on GB300: small-rank decode groups (256 rows, r = 16,
-      // h = 4096: 17 MB of weight re-reads) run faster on the CUDA cores; prefill groups
-      // (>= 128 rows, r = 64: >= 60 MB) several times faster on the tensor cores.
+      // L2); the tensor path streams them once per 128-row tile (split over the cluster).
+      // Measured on GB300: small-rank decode groups (256 rows, r = 16, h = 4096: 17 MB of
+      // weight re-reads) run faster on the CUDA cores; prefill groups (r = 64, >= 60 MB) and
+      // the hot groups of the 70B mix (r = 64, h = 8192) faster on the tensor cores.
       const double w = static_cast<double>(pb.r) * 2.0 *
                        ((pb.mode != sgmv::kExpand ? pb.h_in : 0) +
                         (pb.mode != sgmv::kShrink ? pb.h_out : 0));
