@@ -866,7 +866,7 @@ struct Kernel {
           }
         }
         named_bar(1, kConsumers);
-        if (last) cluster_arrive();  // no more reads of peer shared memory (arrive #2)
+        if (last) cluster_arrive_relaxed();  // all bytes for this CTA have landed (arrive #2)
       }
     }
 
@@ -979,7 +979,7 @@ struct Kernel {
     // when the group exchanges partial products)
     if (MODE != kExpand && !(grp.size > 1 && n_my > 0)) {
       cluster_wait();
-      cluster_arrive();
+      cluster_arrive_relaxed();
     }
   }
 
@@ -1115,8 +1115,9 @@ struct Kernel {
     fence_proxy_async();  // the ring held the hash table: order before bulk copies land
     __syncthreads();
     // Cluster barrier protocol (fused / shrink), per thread: arrive #1 here (barriers are
-    // initialised) -> wait #1 before the first remote arrive -> arrive #2 after the last read of
-    // peer shared memory -> wait #2 at exit (no CTA leaves while a peer may still read it).
+    // initialised; release) -> wait #1 before the first write to a peer -> arrive #2 (relaxed)
+    // once every byte pushed to this CTA has landed -> wait #2 at exit (no CTA leaves while a
+    // peer may still write to it).
     if (MODE != kExpand) cluster_arrive();
 
     const Waiter w{reinterpret_cast<volatile int*>(ctl), p.err, p.wait_limit_ns};
@@ -1130,7 +1131,7 @@ struct Kernel {
                reinterpret_cast<int4*>(smem + p.off_stab), n_my);
       if (MODE != kExpand) {
         cluster_wait();
-        cluster_arrive();
+        cluster_arrive_relaxed();
       }
     } else {
       consumer(p, sm, w, grp, mp, n_my);

@@ -815,7 +815,10 @@ struct TcRole {
     __syncthreads();
     tc_fence_after();
     if (warp == kConsumerWarps) tmem_dealloc(tm, kTcCols);
-    if (c.split) cluster_sync_all();  // no member leaves while a peer may still write to it
+    if (c.split) {  // no member leaves while a peer may still write to it (every incoming
+      cluster_arrive_relaxed();  // byte was counted by a barrier this CTA waited on)
+      cluster_wait();
+    }
   }
 };
 
