@@ -49,7 +49,7 @@ constexpr int kMaxStages = 16;
 
 struct Tuning {
   int stages = 0;     // 0: as many as shared memory holds
-  int stage_kb = 24;  // ring stage size
+  int stage_kb = 0;   // ring stage size in KB; 0: by rank (stage_kb_for)
   int budget_kb = 0;  // 0: 112 KB (two CTAs per SM), else the per-CTA shared-memory budget
   int tc_min_rows = 64;  // adapter groups of at least half a 128-row tile use the tensor
                          // cores (measured: 64 beats 128 on the 70B mix, 16 and 32 tie)...
@@ -71,6 +71,14 @@ Tuning read_tuning() {
 const Tuning& tuning() {
   static const Tuning t = read_tuning();
   return t;
+}
+// Ring stage size.  Rank 16: 20 KB, i.e. an A chunk of 512 rows plus its x columns for four
+// rows, with five stages in the ring (24 KB stages hold the same 512-row chunks, four at a
+// time: measured 5.8 vs 6.4 us per chained decode call).  Larger ranks: 24 KB (measured on the
+// 70B mix, rank 64: 136 vs 138 us).
+int stage_kb_for(int r, const Tuning& tu) {
+  if (tu.stage_kb > 0) return tu.stage_kb;
+  return r <= 16 ? 20 : 24;
 }
 
 int rank_index(int r) {
@@ -211,7 +219,7 @@ int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* sme
   const int vec = 16 / eb;
   const int C = sgmv::kMaxGroup;
   const int rmax = sgmv::kRowsMax;
-  const int stage_bytes = tu.stage_kb * 1024;
+  const int stage_bytes = stage_kb_for(pb.r, tu) * 1024;
   // A rows per stage, followed by the same rows' columns of up to rmax x rows.
   const int kb = (stage_bytes / ((pb.r + rmax) * eb)) / 8 * 8;
   // Expand pass width: one thread per 16 bytes of a B row, and rmax y rows must fit a stage.

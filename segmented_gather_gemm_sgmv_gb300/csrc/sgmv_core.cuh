@@ -1114,11 +1114,13 @@ struct Kernel {
     }
     fence_proxy_async();  // the ring held the hash table: order before bulk copies land
     __syncthreads();
-    // Cluster barrier protocol (fused / shrink), per thread: arrive #1 here (barriers are
-    // initialised; release) -> wait #1 before the first write to a peer -> arrive #2 (relaxed)
-    // once every byte pushed to this CTA has landed -> wait #2 at exit (no CTA leaves while a
-    // peer may still write to it).
-    if (MODE != kExpand) cluster_arrive();
+    // Cluster barrier protocol (fused / shrink), per thread: arrive #1 here (the barriers that
+    // peers write to are initialised; the init fence above publishes them, so the arrival is
+    // relaxed) -> wait #1 before the first write to a peer -> arrive #2 (relaxed) once every
+    // byte pushed to this CTA has landed -> wait #2 at exit (no CTA leaves while a peer may
+    // still write to it).  Peers only ever push (st.async) into this CTA: nothing here is read
+    // remotely, so no arrival has to release other writes.
+    if (MODE != kExpand) cluster_arrive_relaxed();
 
     const Waiter w{reinterpret_cast<volatile int*>(ctl), p.err, p.wait_limit_ns};
     if (p.inject_stall) w.wait<false>(sm.fixed(kNever), 0);  // nothing completes it

@@ -134,18 +134,11 @@ static __device__ __forceinline__ void fence_proxy_async() {
 }
 
 // ---- clusters ------------------------------------------------------------------------
-static __device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Split form: every thread of every CTA of the cluster arrives, then (later) waits.
-static __device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-// Arrival without release semantics, for the exit barrier of a protocol whose shared-memory
-// traffic between CTAs is all counted by mbarriers: every byte a CTA receives has landed before
-// it arrives (it waited for the bytes), so the barrier only has to say "done", not publish
-// writes.  The release form was measured at about 1 us per arrival after the decode exchange.
+// Cluster barrier, split form: every thread of every CTA of the cluster arrives, then (later)
+// waits.  The arrival has no release semantics.  The CTAs of a cluster here only push data to
+// one another (st.async), each byte counted by an mbarrier of the receiver, and the barrier
+// inits are published by fence.mbarrier_init; so the barrier only has to say "initialised" or
+// "done", not publish other writes.  The release form was measured at about 1 us per arrival.
 static __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }

@@ -763,7 +763,10 @@ struct TcRole {
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tslot;
-    if (c.split) cluster_sync_all();  // every member's barriers exist before the first st.async
+    if (c.split) {  // every member's barriers exist before the first st.async (published by
+      cluster_arrive_relaxed();  // the init fence above)
+      cluster_wait();
+    }
 
     if (tid == 0) {
       tma_prefetch_desc(&p.tmap_x128);
