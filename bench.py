@@ -173,11 +173,13 @@ def barrier(world):
 class Setup:
     """Device-resident inputs of the workload: pool, NB rotating x/y sets, segment table."""
 
-    def __init__(self, w, device, nbuf=32, seed=0, overlap=True, tensor_cores="auto"):
+    def __init__(self, w, device, nbuf=32, seed=0, overlap=True, tensor_cores="auto",
+                 long_batch=False):
         import torch
         self.w = w
         self.overlap = overlap
         self.tensor_cores = tensor_cores
+        self.long_batch = long_batch
         self.ss, self.sa = workloads.make_segments(w.name, seed)
         self.M = int(self.ss[-1])
         self.A, self.B = workloads.make_pool(w, device, seed=seed + 1)
@@ -197,7 +199,8 @@ class Setup:
         i = step % self.nbuf
         lora_apply(self.y[i], self.x[i], self.A_ptrs, self.B_ptrs, self.d_ss, self.d_sa,
                    step % self.w.layers, self.w.r, self.w.scale, stream=stream,
-                   overlap_prior=self.overlap, tensor_cores=self.tensor_cores)
+                   overlap_prior=self.overlap, tensor_cores=self.tensor_cores,
+                   long_batch=self.long_batch)
 
 
 def capture(torch, fn, n, stream):
@@ -276,7 +279,8 @@ def time_e2e(torch, setup, K, stream):
     def step(s):
         dev.copy_(host, non_blocking=True)
         lora_apply(yd, xd, setup.A_ptrs, setup.B_ptrs, ssd, sad, s % w.layers, w.r, w.scale,
-                   stream=stream, overlap_prior=setup.overlap, tensor_cores=setup.tensor_cores)
+                   stream=stream, overlap_prior=setup.overlap, tensor_cores=setup.tensor_cores,
+                   long_batch=setup.long_batch)
         yout.copy_(yd, non_blocking=True)
 
     per = w.layers
@@ -340,7 +344,8 @@ def run_ours(args):
     from segmented_gather_gemm_sgmv_gb300 import binding
     binding.lib()
     w = workloads.WORKLOADS[args.workload]
-    setup = Setup(w, device, tensor_cores=args.tensor_cores)
+    long_batch = {"auto": w.prefill, "on": True, "off": False}[args.long_batch]
+    setup = Setup(w, device, tensor_cores=args.tensor_cores, long_batch=long_batch)
     stream = torch.cuda.Stream(device)
     nbytes, M = algorithmic_bytes(w, setup.ss, setup.sa)
     K, W = args.steps, args.warmup
@@ -382,9 +387,11 @@ def run_ours(args):
         "tokens_per_s": round(world * M / per, 1),
         "us_per_call": round(per * 1e6, 3),
         "us_per_call_isolated": round(us_iso, 3),
-        "launch": "lora_apply_ex(SGMV_OVERLAP_PRIOR): each call's weight prefetch overlaps the "
-                  "previous call (programmatic dependent launch)" if setup.overlap else
-                  "lora_apply: each call starts after the previous one completes",
+        "launch": ("lora_apply_ex(SGMV_OVERLAP_PRIOR): each call's weight prefetch overlaps the "
+                   "previous call (programmatic dependent launch)" if setup.overlap else
+                   "lora_apply: each call starts after the previous one completes") +
+                  ("; SGMV_LONG_BATCH (a prefill batch: one CTA per SM, whole shared memory)"
+                   if setup.long_batch else ""),
         "config": {"workload": w.name, "h_in": w.h_in, "h_out": w.h_out, "r": w.r,
                    "tokens": M, "segments": int(len(setup.sa)),
                    "distinct_adapters": int(len({int(k) for k in setup.sa})),
@@ -479,6 +486,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tensor-cores", choices=["auto", "never", "always"], default="auto",
                     help="which adapter groups use the tensor cores (lora_apply_ex flags)")
+    ap.add_argument("--long-batch", choices=["auto", "on", "off"], default="auto",
+                    help="SGMV_LONG_BATCH launches; auto: for workloads that hold prefill "
+                         "segments (prefill_mixed, mixed_70b)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain lora_apply launches (no programmatic dependent launch)")
     args = ap.parse_args()

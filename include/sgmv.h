@@ -116,6 +116,7 @@ int lora_apply(void *y, const void *x, const void *const *A_ptrs, const void *co
 #define SGMV_OVERLAP_PRIOR 1u
 #define SGMV_NO_TENSOR_CORES 2u
 #define SGMV_TENSOR_CORES_ALWAYS 4u
+#define SGMV_LONG_BATCH 8u
 
 /*
  * lora_apply_ex -- lora_apply with launch flags.
@@ -135,6 +136,14 @@ int lora_apply(void *y, const void *x, const void *const *A_ptrs, const void *co
  *   flags |= SGMV_TENSOR_CORES_ALWAYS: every adapter group of at least 64 rows runs on the
  *     tensor cores, without the cost rule described under lora_apply (fp16 / bf16, r >= 16).
  *     Not combinable with SGMV_NO_TENSOR_CORES (SGMV_EINVAL).
+ *   flags |= SGMV_LONG_BATCH: the caller declares a long call (a prefill batch, or adapter
+ *     groups of hundreds of rows).  The kernel then runs one CTA per SM with up to 227 KB of
+ *     shared memory instead of two co-resident CTAs of 112 KB: deeper rings of weight and
+ *     activation stages for both the CUDA-core and the tensor-core paths.  The results agree
+ *     with a launch without the flag within rounding (the routing of groups and the chunking
+ *     of h_in are the same; the grid, and with it the split of work over CTAs, may differ).
+ *     With SGMV_OVERLAP_PRIOR the next call's CTAs can only start where this call's CTAs have
+ *     left, so the overlap of short calls is lost: do not use it for decode batches.
  * Other arguments, layout and errors: as for lora_apply (SGMV_EINVAL for unknown flags).
  */
 int lora_apply_ex(void *y, const void *x, const void *const *A_ptrs, const void *const *B_ptrs,

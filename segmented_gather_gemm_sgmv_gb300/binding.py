@@ -22,6 +22,7 @@ SGMV_MAX_HIDDEN = 65536
 SGMV_OVERLAP_PRIOR = 1
 SGMV_NO_TENSOR_CORES = 2
 SGMV_TENSOR_CORES_ALWAYS = 4
+SGMV_LONG_BATCH = 8
 SYMBOLS = ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_shrink_ex", "sgmv_expand",
            "sgmv_expand_ex", "sgmv_validate", "sgmv_get_error", "sgmv_set_wait_limit",
            "sgmv_status_string", "sgmv_version")
@@ -118,12 +119,12 @@ def _ptrs(t, name):
     return t.data_ptr()
 
 
-def _flags(overlap_prior, tensor_cores) -> int:
+def _flags(overlap_prior, tensor_cores, long_batch=False) -> int:
     mode = {True: "auto", False: "never"}.get(tensor_cores, tensor_cores)
     if mode not in ("auto", "never", "always"):
         raise ValueError(f"tensor_cores must be 'auto', 'never' or 'always', not {tensor_cores!r}")
-    return (SGMV_OVERLAP_PRIOR if overlap_prior else 0) | {
-        "auto": 0, "never": SGMV_NO_TENSOR_CORES, "always": SGMV_TENSOR_CORES_ALWAYS}[mode]
+    return ((SGMV_OVERLAP_PRIOR if overlap_prior else 0) | (SGMV_LONG_BATCH if long_batch else 0) |
+            {"auto": 0, "never": SGMV_NO_TENSOR_CORES, "always": SGMV_TENSOR_CORES_ALWAYS}[mode])
 
 
 def _check(rc: int, where: str):
@@ -132,13 +133,15 @@ def _check(rc: int, where: str):
 
 
 def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None,
-               overlap_prior=False, tensor_cores="auto"):
+               overlap_prior=False, tensor_cores="auto", long_batch=False):
     """y[t] += scale * (x[t] A_k) B_k for every segment row (in place on y).
 
     overlap_prior=True calls lora_apply_ex with SGMV_OVERLAP_PRIOR: the kernel may stream
     weights while the previous kernel on the stream is still running (see include/sgmv.h).
     tensor_cores: "auto" (the library's cost rule), "never" (SGMV_NO_TENSOR_CORES) or "always"
     (SGMV_TENSOR_CORES_ALWAYS); True / False mean "auto" / "never".
+    long_batch=True adds SGMV_LONG_BATCH: one CTA per SM with the whole shared memory, for
+    prefill-sized calls (see include/sgmv.h).
     """
     _cuda(y, "y"), _cuda(x, "x")
     if x.dtype != y.dtype or x.dim() != 2 or y.dim() != 2 or x.shape[0] != y.shape[0]:
@@ -147,7 +150,7 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
     args = (y.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
             seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1],
             y.shape[1], int(r), float(scale), _dtype_code(x))
-    flags = _flags(overlap_prior, tensor_cores)
+    flags = _flags(overlap_prior, tensor_cores, long_batch)
     if flags:
         rc = lib().lora_apply_ex(*args, flags, _stream(stream, x.device))
         _check(rc, "lora_apply_ex")
@@ -158,8 +161,9 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
 
 
 def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None,
-                tensor_cores="auto"):
-    """v[t] = x[t] A_k (fp32) for every segment row (tensor_cores as for lora_apply)."""
+                tensor_cores="auto", long_batch=False):
+    """v[t] = x[t] A_k (fp32) for every segment row (tensor_cores, long_batch as for
+    lora_apply)."""
     import torch
     _cuda(v, "v"), _cuda(x, "x")
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != x.shape[0]:
@@ -167,7 +171,7 @@ def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None
     S = _table(seg_starts, seg_adapter)
     args = (v.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"), seg_starts.data_ptr(),
             seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1], int(r), _dtype_code(x))
-    flags = _flags(False, tensor_cores)
+    flags = _flags(False, tensor_cores, long_batch)
     if flags:
         _check(lib().sgmv_shrink_ex(*args, flags, _stream(stream, x.device)), "sgmv_shrink_ex")
     else:
@@ -176,8 +180,9 @@ def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None
 
 
 def sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None,
-                tensor_cores="auto"):
-    """y[t] += scale * v[t] B_k for every segment row (in place on y)."""
+                tensor_cores="auto", long_batch=False):
+    """y[t] += scale * v[t] B_k for every segment row (in place on y; tensor_cores, long_batch
+    as for lora_apply)."""
     import torch
     _cuda(y, "y"), _cuda(v, "v")
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != y.shape[0]:
@@ -186,7 +191,7 @@ def sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stre
     args = (y.data_ptr(), v.data_ptr(), _ptrs(B_ptrs, "B_ptrs"), seg_starts.data_ptr(),
             seg_adapter.data_ptr(), S, int(layer_idx), int(r), y.shape[1], float(scale),
             _dtype_code(y))
-    flags = _flags(False, tensor_cores)
+    flags = _flags(False, tensor_cores, long_batch)
     if flags:
         _check(lib().sgmv_expand_ex(*args, flags, _stream(stream, y.device)), "sgmv_expand_ex")
     else:

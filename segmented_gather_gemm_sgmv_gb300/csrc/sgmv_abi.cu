@@ -28,9 +28,11 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 struct KernelCache {
   const void* fn = nullptr;
   size_t smem_set = 0;
-  int cluster = 0;
-  size_t smem_q = 0;
-  int max_clusters = 0;
+  // grid size per launch geometry (0: two CTAs per SM, 1: SGMV_LONG_BATCH), cached with the
+  // cluster size and shared-memory size it was computed for
+  int cluster[2] = {0, 0};
+  size_t smem_q[2] = {0, 0};
+  int max_clusters[2] = {0, 0};
 };
 
 struct DeviceState {
@@ -282,9 +284,11 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   int rc = device_state(&st);
   if (rc != SGMV_OK) return rc;
   size_t smem = 0;
+  const bool wide = (flags & SGMV_LONG_BATCH) != 0;
+  const size_t base_smem = wide ? kMaxSmem : kPairSmem;
   const size_t budget = tuning().budget_kb > 0
                             ? std::min<size_t>(kMaxSmem, static_cast<size_t>(tuning().budget_kb) * 1024)
-                            : kPairSmem;
+                            : base_smem;
   rc = plan_geometry(pb, budget, p, &smem);
   if (rc == SGMV_EUNSUPPORTED) rc = plan_geometry(pb, kMaxSmem, p, &smem);
   if (rc != SGMV_OK) return rc;
@@ -306,7 +310,7 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   const uint32_t tc_base = static_cast<uint32_t>(
       up(p.off_vpart + (2 * sgmv::kTcRows + 4) * sizeof(int), 1024));
   const bool tc_capable = pb.dtype != SGMV_F32 && pb.r >= 16 && !(flags & SGMV_NO_TENSOR_CORES);
-  if (tc_capable && smem <= kPairSmem) smem = kPairSmem;
+  if (tc_capable && smem <= budget) smem = budget;  // the tensor ring takes the whole budget
   int grid = 0;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -321,7 +325,8 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
         return SGMV_ECUDA;
       kc.smem_set = smem;
     }
-    if (kc.cluster != p.C || kc.smem_q != smem) {
+    const int g = wide ? 1 : 0;
+    if (kc.cluster[g] != p.C || kc.smem_q[g] != smem) {
       int n = 0;
       if (clustered) {
         cudaLaunchConfig_t cfg = {};
@@ -345,11 +350,11 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
       }
       n = std::min(n, std::max(1, st->sms / p.C));  // one CTA per SM per kernel
       if (n <= 0) return SGMV_EUNSUPPORTED;
-      kc.cluster = p.C;
-      kc.smem_q = smem;
-      kc.max_clusters = n;
+      kc.cluster[g] = p.C;
+      kc.smem_q[g] = smem;
+      kc.max_clusters[g] = n;
     }
-    grid = kc.max_clusters * p.C;
+    grid = kc.max_clusters[g] * p.C;
   }
 
   // Tensor role: at least three ring slots and two clusters in the grid.
@@ -419,7 +424,7 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
 
 bool flags_ok(uint32_t flags) {
   if (flags & ~static_cast<uint32_t>(SGMV_OVERLAP_PRIOR | SGMV_NO_TENSOR_CORES |
-                                     SGMV_TENSOR_CORES_ALWAYS))
+                                     SGMV_TENSOR_CORES_ALWAYS | SGMV_LONG_BATCH))
     return false;
   return !((flags & SGMV_NO_TENSOR_CORES) && (flags & SGMV_TENSOR_CORES_ALWAYS));
 }

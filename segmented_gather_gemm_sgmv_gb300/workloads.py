@@ -20,6 +20,9 @@ distributions and segment structure follow five named workloads:
                    a Zipf(a=1.2) law over 256 adapters (not sorted, so one adapter can own
                    several non-adjacent segments), pool stacked over 80 layers.
 
+prefill_mixed and mixed_70b hold prefill segments: a serving layer knows that of its batch and
+launches them with SGMV_LONG_BATCH (Workload.prefill).
+
 Value distributions (all workloads): x ~ N(0,1); A ~ U(-1/sqrt(h_in), +1/sqrt(h_in));
 B ~ N(0, sd=1/sqrt(r)); y_in ~ N(0,1) (the base output x W0 the LoRA term is added to);
 scale = alpha / r with alpha = 16.
@@ -46,6 +49,7 @@ class Workload:
     num_adapters: int
     layers: int
     alpha: float = 16.0
+    prefill: bool = False  # the batch holds prefill segments (a caller passes SGMV_LONG_BATCH)
 
     @property
     def scale(self) -> float:
@@ -62,8 +66,8 @@ WORKLOADS = {
     "decode_zipf": Workload("decode_zipf", 4096, 4096, 16, "f16", 1024, 16),
     "decode_uniform": Workload("decode_uniform", 4096, 4096, 16, "f16", 1024, 16),
     "decode_same": Workload("decode_same", 4096, 4096, 16, "f16", 1024, 16),
-    "prefill_mixed": Workload("prefill_mixed", 4096, 11008, 64, "bf16", 8, 1),
-    "mixed_70b": Workload("mixed_70b", 8192, 8192, 64, "bf16", 256, 80),
+    "prefill_mixed": Workload("prefill_mixed", 4096, 11008, 64, "bf16", 8, 1, prefill=True),
+    "mixed_70b": Workload("mixed_70b", 8192, 8192, 64, "bf16", 256, 80, prefill=True),
 }
 
 

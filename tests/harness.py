@@ -117,9 +117,9 @@ def assert_close(y, y_ref, what="", atol=ATOL, rtol=RTOL):
     return float(err.max()) if err.size else 0.0
 
 
-def run_apply(c: Case, layer, y=None, x=None, tensor_cores="auto"):
+def run_apply(c: Case, layer, y=None, x=None, tensor_cores="auto", long_batch=False):
     from segmented_gather_gemm_sgmv_gb300 import lora_apply
     y = c.y0.clone() if y is None else y
     lora_apply(y, c.x if x is None else x, c.A_ptrs, c.B_ptrs, c.d_ss, c.d_sa, layer, c.w.r,
-               c.w.scale, tensor_cores=tensor_cores)
+               c.w.scale, tensor_cores=tensor_cores, long_batch=long_batch)
     return y

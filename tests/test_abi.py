@@ -38,6 +38,7 @@ def test_header_constants_match_binding():
     assert f"#define SGMV_OVERLAP_PRIOR {binding.SGMV_OVERLAP_PRIOR}u" in text
     assert f"#define SGMV_NO_TENSOR_CORES {binding.SGMV_NO_TENSOR_CORES}u" in text
     assert f"#define SGMV_TENSOR_CORES_ALWAYS {binding.SGMV_TENSOR_CORES_ALWAYS}u" in text
+    assert f"#define SGMV_LONG_BATCH {binding.SGMV_LONG_BATCH}u" in text
     for name, val in [("SGMV_EINVAL", -1), ("SGMV_EALIGN", -2), ("SGMV_EUNSUPPORTED", -3),
                       ("SGMV_ECUDA", -4), ("SGMV_ETIMEOUT", -5)]:
         assert re.search(rf"{name}\s*=\s*{val}\b", text), name
@@ -77,10 +78,11 @@ def test_lora_apply_ex_flags(L):
     a = OK_ARGS
     args = (a["y"], a["x"], a["A"], a["B"], a["ss"], a["sa"], 0, a["layer"], a["h_in"],
             a["h_out"], a["r"], a["scale"], a["dt"])
-    for flags in (0, 1, 2, 3, 4, 5):  # num_segments = 0: argument checks only, no launch
+    for flags in (0, 1, 2, 3, 4, 5, 8, 9, 10, 13):  # num_segments = 0: checks only, no launch
         assert L.lora_apply_ex(*args, flags, None) == 0
     assert L.lora_apply_ex(*args, 6, None) == -1  # never + always
-    assert L.lora_apply_ex(*args, 8, None) == -1
+    assert L.lora_apply_ex(*args, 14, None) == -1
+    assert L.lora_apply_ex(*args, 16, None) == -1  # unknown bit
 
 
 def test_shrink_expand_validate_host_checks(L):
