@@ -247,7 +247,10 @@ def time_graph_steps(torch, setup, K, W, stream, world):
 def time_e2e(torch, setup, K, stream):
     """Public-API path with pinned host buffers.  Per step: ONE host->device copy of the step's
     inputs (x, y_in and the segment table packed in one pinned staging buffer), the lora_apply
-    call on views of the device copy, ONE device->host copy of y."""
+    call on views of the device copy, ONE device->host copy of y.  Steps alternate between two
+    streams and two device / host buffer sets, so that one step's copies overlap the other
+    stream's kernel; each stream runs its steps in order (a buffer set is reused only after
+    its previous step's copy back has completed)."""
     w = setup.w
     n = min(K, 2048)
     dt = workloads.torch_dtype(w.dtype)
@@ -268,27 +271,39 @@ def time_e2e(torch, setup, K, stream):
     host[off_y:off_y + ny].copy_(y0.cpu().contiguous().view(torch.uint8).view(-1))
     host[off_ss:off_ss + nss].copy_(torch.as_tensor(setup.ss).view(torch.uint8))
     host[off_sa:off_sa + nsa].copy_(torch.as_tensor(setup.sa).view(torch.uint8))
-    dev = torch.empty(total, dtype=torch.uint8, device=x0.device)
-    xd = dev[0:nx].view(dt).view(x0.shape)
-    yd = dev[off_y:off_y + ny].view(dt).view(y0.shape)
-    ssd = dev[off_ss:off_ss + nss].view(torch.int32)
-    sad = dev[off_sa:off_sa + nsa].view(torch.int32)
-    yout = torch.empty(y0.shape, dtype=dt).pin_memory()
+    streams = [stream, torch.cuda.Stream(x0.device)]
+    sets = []
+    for _ in range(2):
+        dev = torch.empty(total, dtype=torch.uint8, device=x0.device)
+        sets.append(dict(dev=dev, x=dev[0:nx].view(dt).view(x0.shape),
+                         y=dev[off_y:off_y + ny].view(dt).view(y0.shape),
+                         ss=dev[off_ss:off_ss + nss].view(torch.int32),
+                         sa=dev[off_sa:off_sa + nsa].view(torch.int32),
+                         out=torch.empty(y0.shape, dtype=dt).pin_memory()))
     from segmented_gather_gemm_sgmv_gb300 import lora_apply
 
     def step(s):
-        dev.copy_(host, non_blocking=True)
-        lora_apply(yd, xd, setup.A_ptrs, setup.B_ptrs, ssd, sad, s % w.layers, w.r, w.scale,
-                   stream=stream, overlap_prior=setup.overlap, tensor_cores=setup.tensor_cores,
-                   long_batch=setup.long_batch)
-        yout.copy_(yd, non_blocking=True)
+        st, b = streams[s % 2], sets[s % 2]
+        with torch.cuda.stream(st):
+            b["dev"].copy_(host, non_blocking=True)
+            lora_apply(b["y"], b["x"], setup.A_ptrs, setup.B_ptrs, b["ss"], b["sa"],
+                       s % w.layers, w.r, w.scale, stream=st, overlap_prior=setup.overlap,
+                       tensor_cores=setup.tensor_cores, long_batch=setup.long_batch)
+            b["out"].copy_(b["y"], non_blocking=True)
 
-    per = w.layers
-    with torch.cuda.stream(stream):
-        for s in range(3):
+    def sweep(n_steps):
+        streams[1].wait_stream(streams[0])  # fork
+        for s in range(n_steps):
             step(s)
+        streams[0].wait_stream(streams[1])  # join
+
+    per = w.layers if w.layers % 2 == 0 else 2 * w.layers
+    with torch.cuda.stream(stream):
+        sweep(4)
     torch.cuda.synchronize()
-    g = capture(torch, step, per, stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        sweep(per)
     with torch.cuda.stream(stream):
         g.replay()
     torch.cuda.synchronize()
