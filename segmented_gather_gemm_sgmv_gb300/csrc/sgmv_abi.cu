@@ -286,9 +286,10 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   size_t smem = 0;
   const bool wide = (flags & SGMV_LONG_BATCH) != 0;
   const size_t base_smem = wide ? kMaxSmem : kPairSmem;
-  const size_t budget = tuning().budget_kb > 0
-                            ? std::min<size_t>(kMaxSmem, static_cast<size_t>(tuning().budget_kb) * 1024)
-                            : base_smem;
+  const size_t budget =
+      tuning().budget_kb > 0
+          ? std::min<size_t>(kMaxSmem, static_cast<size_t>(tuning().budget_kb) * 1024)
+          : base_smem;
   rc = plan_geometry(pb, budget, p, &smem);
   if (rc == SGMV_EUNSUPPORTED) rc = plan_geometry(pb, kMaxSmem, p, &smem);
   if (rc != SGMV_OK) return rc;
@@ -304,9 +305,9 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   const void* fn = kernel_for(pb.dtype, pb.mode, pb.r);
   if (!fn) return SGMV_EUNSUPPORTED;
   const bool clustered = pb.mode != sgmv::kExpand;
-  // Tensor role (fused, 16-bit types, r >= 16): it uses none of the CUDA-core scratch areas, so
-  // its row table sits at off_vpart and its ring of 24 KB slots right after it, up to the end of
-  // the budget (the launch then always takes the whole budget).
+  // Tensor role (16-bit types, r >= 16; every mode): it uses none of the CUDA-core scratch
+  // areas, so its row table sits at off_vpart and its ring of 24 KB slots right after it, up to
+  // the end of the budget (the launch then always takes the whole budget).
   const uint32_t tc_base = static_cast<uint32_t>(
       up(p.off_vpart + (2 * sgmv::kTcRows + 4) * sizeof(int), 1024));
   const bool tc_capable = pb.dtype != SGMV_F32 && pb.r >= 16 && !(flags & SGMV_NO_TENSOR_CORES);
