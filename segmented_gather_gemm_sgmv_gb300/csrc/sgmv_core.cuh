@@ -1094,8 +1094,11 @@ struct Kernel {
       const long long W = static_cast<long long>(R) * (p.h_in + p.h_out) * kEb;
       const long long X = p.xchg_bytes;
       long long best = static_cast<long long>((n_items + Nc - 1) / Nc) * W;
-      for (int e = 2; e <= p.C; e *= 2) {
-        const long long cost = static_cast<long long>((n_items * e + Nc - 1) / Nc) * (W / e + X);
+      // (E = 2^lg2, so W / E is a shift: a 64-bit division here took ~0.7 us of start-up)
+      for (int lg2 = 1; (1 << lg2) <= p.C; ++lg2) {
+        const int e = 1 << lg2;
+        const long long cost =
+            static_cast<long long>((n_items * e + Nc - 1) / Nc) * ((W >> lg2) + X);
         if (cost < best) {
           best = cost;
           grp.size = e;
