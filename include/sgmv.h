@@ -77,6 +77,8 @@ typedef enum {
 #define SGMV_MAX_SEGMENTS 4096
 /* Largest h_in and h_out one call accepts. */
 #define SGMV_MAX_HIDDEN 65536
+/* Largest row stride (elements) of x or y that the _strided entry points accept. */
+#define SGMV_MAX_LD (1 << 24)
 
 /*
  * lora_apply -- the fused path: y[t] += scale * (x[t] . A_k) . B_k for every segment row.
@@ -152,6 +154,26 @@ int lora_apply_ex(void *y, const void *x, const void *const *A_ptrs, const void 
                   sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream);
 
 /*
+ * lora_apply_strided -- lora_apply_ex on x and y whose rows are ldx and ldy elements apart:
+ * row t of x is x + t * ldx (its first h_in elements are read), row t of y is y + t * ldy (its
+ * first h_out elements are read and written; the elements past h_out in a row are never
+ * touched).  This lets the delta apply to column slices of wider activations, for example the
+ * q, k or v part of a fused projection output, in place.  The pages describe dense [M][h]
+ * activations; the row stride is the common leading-dimension generalisation.
+ *   ldx   h_in <= ldx <= SGMV_MAX_LD, a multiple of 8 (SGMV_EINVAL if below h_in,
+ *         SGMV_EALIGN if not a multiple of 8, SGMV_EUNSUPPORTED above SGMV_MAX_LD)
+ *   ldy   the same with h_out
+ * Other arguments, layout, flags and errors: as for lora_apply_ex.  lora_apply_ex is this call
+ * with ldx = h_in and ldy = h_out.
+ */
+int lora_apply_strided(void *y, int32_t ldy, const void *x, int32_t ldx,
+                       const void *const *A_ptrs, const void *const *B_ptrs,
+                       const int32_t *seg_starts, const int32_t *seg_adapter,
+                       int32_t num_segments, int32_t layer_idx, int32_t h_in, int32_t h_out,
+                       int32_t r, float scale, sgmv_dtype_t dtype, uint32_t flags,
+                       sgmv_stream_t stream);
+
+/*
  * sgmv_shrink -- v[t] = x[t] . A_k for every segment row (overwrites those rows of v; other
  * rows of v are not written).  Source: the first factor x_i A_{k(i)} of the y_i equation and
  * the "one launch for all A projections" of section "Mathematical Modeling ...", part 2.
@@ -175,6 +197,15 @@ int sgmv_shrink_ex(float *v, const void *x, const void *const *A_ptrs,
                    uint32_t flags, sgmv_stream_t stream);
 
 /*
+ * sgmv_shrink_strided -- sgmv_shrink_ex with x rows ldx elements apart (ldx as for
+ * lora_apply_strided; v stays dense [M][r]).
+ */
+int sgmv_shrink_strided(float *v, const void *x, int32_t ldx, const void *const *A_ptrs,
+                        const int32_t *seg_starts, const int32_t *seg_adapter,
+                        int32_t num_segments, int32_t layer_idx, int32_t h_in, int32_t r,
+                        sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream);
+
+/*
  * sgmv_expand -- y[t] += scale * v[t] . B_k for every segment row.  Source: the second factor
  * (x_i A_k) B_k of the y_i equation, times alpha/r, and the "one launch for all B projections"
  * of section "Mathematical Modeling ...", part 2.
@@ -196,6 +227,15 @@ int sgmv_expand_ex(void *y, const float *v, const void *const *B_ptrs,
                    const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,
                    int32_t layer_idx, int32_t r, int32_t h_out, float scale, sgmv_dtype_t dtype,
                    uint32_t flags, sgmv_stream_t stream);
+
+/*
+ * sgmv_expand_strided -- sgmv_expand_ex with y rows ldy elements apart (ldy as for
+ * lora_apply_strided; the elements past h_out in a row are never touched).
+ */
+int sgmv_expand_strided(void *y, int32_t ldy, const float *v, const void *const *B_ptrs,
+                        const int32_t *seg_starts, const int32_t *seg_adapter,
+                        int32_t num_segments, int32_t layer_idx, int32_t r, int32_t h_out,
+                        float scale, sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream);
 
 /*
  * sgmv_validate -- checks a segment table on the device and writes an OR of these bits to

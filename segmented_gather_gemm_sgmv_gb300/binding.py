@@ -23,9 +23,11 @@ SGMV_OVERLAP_PRIOR = 1
 SGMV_NO_TENSOR_CORES = 2
 SGMV_TENSOR_CORES_ALWAYS = 4
 SGMV_LONG_BATCH = 8
-SYMBOLS = ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_shrink_ex", "sgmv_expand",
-           "sgmv_expand_ex", "sgmv_validate", "sgmv_get_error", "sgmv_set_wait_limit",
-           "sgmv_status_string", "sgmv_version")
+SGMV_MAX_LD = 1 << 24
+SYMBOLS = ("lora_apply", "lora_apply_ex", "lora_apply_strided", "sgmv_shrink", "sgmv_shrink_ex",
+           "sgmv_shrink_strided", "sgmv_expand", "sgmv_expand_ex", "sgmv_expand_strided",
+           "sgmv_validate", "sgmv_get_error", "sgmv_set_wait_limit", "sgmv_status_string",
+           "sgmv_version")
 
 
 class SgmvError(RuntimeError):
@@ -58,16 +60,21 @@ def lib(build_if_stale: bool = True) -> ctypes.CDLL:
                                      ctypes.c_uint32, vp]
         L.sgmv_expand_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, ctypes.c_int,
                                      ctypes.c_uint32, vp]
+        L.lora_apply_strided.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32,
+                                         i32, f32, ctypes.c_int, ctypes.c_uint32, vp]
+        L.sgmv_shrink_strided.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, i32,
+                                          ctypes.c_int, ctypes.c_uint32, vp]
+        L.sgmv_expand_strided.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, f32,
+                                          ctypes.c_int, ctypes.c_uint32, vp]
         L.sgmv_validate.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         L.sgmv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
         L.sgmv_set_wait_limit.argtypes = [ctypes.c_uint64, i32]
         L.sgmv_status_string.argtypes = [ctypes.c_int]
         L.sgmv_status_string.restype = ctypes.c_char_p
         L.sgmv_version.argtypes = []
-        for name in ("lora_apply", "lora_apply_ex", "sgmv_shrink", "sgmv_shrink_ex", "sgmv_expand",
-                     "sgmv_expand_ex", "sgmv_validate", "sgmv_get_error", "sgmv_set_wait_limit",
-                     "sgmv_version"):
-            getattr(L, name).restype = ctypes.c_int
+        for name in SYMBOLS:
+            if name != "sgmv_status_string":
+                getattr(L, name).restype = ctypes.c_int
         _lib = L
         return L
 
@@ -90,6 +97,16 @@ def _cuda(t, name):
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t
+
+
+def _rows(t, name):
+    """A CUDA matrix whose rows may be apart by more than their length (a column slice of a
+    wider tensor): returns the row stride in elements."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1) or t.stride(0) < t.shape[1]:
+        raise ValueError(f"{name} must be a 2-D matrix with unit column stride")
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1]
 
 
 def _stream(stream, device):
@@ -142,15 +159,24 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
     (SGMV_TENSOR_CORES_ALWAYS); True / False mean "auto" / "never".
     long_batch=True adds SGMV_LONG_BATCH: one CTA per SM with the whole shared memory, for
     prefill-sized calls (see include/sgmv.h).
+    x and y may be column slices of wider matrices (unit column stride, row stride a multiple
+    of 8 elements): they then go through lora_apply_strided.
     """
-    _cuda(y, "y"), _cuda(x, "x")
-    if x.dtype != y.dtype or x.dim() != 2 or y.dim() != 2 or x.shape[0] != y.shape[0]:
+    ldy, ldx = _rows(y, "y"), _rows(x, "x")
+    if x.dtype != y.dtype or x.shape[0] != y.shape[0]:
         raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
     S = _table(seg_starts, seg_adapter)
+    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    if ldx != x.shape[1] or ldy != y.shape[1]:  # column slices of wider activations
+        rc = lib().lora_apply_strided(
+            y.data_ptr(), ldy, x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
+            seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1],
+            y.shape[1], int(r), float(scale), _dtype_code(x), flags, _stream(stream, x.device))
+        _check(rc, "lora_apply_strided")
+        return y
     args = (y.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
             seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1],
             y.shape[1], int(r), float(scale), _dtype_code(x))
-    flags = _flags(overlap_prior, tensor_cores, long_batch)
     if flags:
         rc = lib().lora_apply_ex(*args, flags, _stream(stream, x.device))
         _check(rc, "lora_apply_ex")
@@ -165,13 +191,20 @@ def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None
     """v[t] = x[t] A_k (fp32) for every segment row (tensor_cores, long_batch as for
     lora_apply)."""
     import torch
-    _cuda(v, "v"), _cuda(x, "x")
+    _cuda(v, "v")
+    ldx = _rows(x, "x")
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != x.shape[0]:
         raise ValueError("v must be float32 [M, r]")
     S = _table(seg_starts, seg_adapter)
+    flags = _flags(False, tensor_cores, long_batch)
+    if ldx != x.shape[1]:
+        _check(lib().sgmv_shrink_strided(
+            v.data_ptr(), x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"), seg_starts.data_ptr(),
+            seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1], int(r), _dtype_code(x), flags,
+            _stream(stream, x.device)), "sgmv_shrink_strided")
+        return v
     args = (v.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"), seg_starts.data_ptr(),
             seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1], int(r), _dtype_code(x))
-    flags = _flags(False, tensor_cores, long_batch)
     if flags:
         _check(lib().sgmv_shrink_ex(*args, flags, _stream(stream, x.device)), "sgmv_shrink_ex")
     else:
@@ -184,14 +217,21 @@ def sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stre
     """y[t] += scale * v[t] B_k for every segment row (in place on y; tensor_cores, long_batch
     as for lora_apply)."""
     import torch
-    _cuda(y, "y"), _cuda(v, "v")
+    _cuda(v, "v")
+    ldy = _rows(y, "y")
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != y.shape[0]:
         raise ValueError("v must be float32 [M, r]")
     S = _table(seg_starts, seg_adapter)
+    flags = _flags(False, tensor_cores, long_batch)
+    if ldy != y.shape[1]:
+        _check(lib().sgmv_expand_strided(
+            y.data_ptr(), ldy, v.data_ptr(), _ptrs(B_ptrs, "B_ptrs"), seg_starts.data_ptr(),
+            seg_adapter.data_ptr(), S, int(layer_idx), int(r), y.shape[1], float(scale),
+            _dtype_code(y), flags, _stream(stream, y.device)), "sgmv_expand_strided")
+        return y
     args = (y.data_ptr(), v.data_ptr(), _ptrs(B_ptrs, "B_ptrs"), seg_starts.data_ptr(),
             seg_adapter.data_ptr(), S, int(layer_idx), int(r), y.shape[1], float(scale),
             _dtype_code(y))
-    flags = _flags(False, tensor_cores, long_batch)
     if flags:
         _check(lib().sgmv_expand_ex(*args, flags, _stream(stream, y.device)), "sgmv_expand_ex")
     else:

@@ -117,12 +117,12 @@ EncodeTiledFn encode_tiled() {
 // with the 128-byte swizzle (8-row atoms of 1024 bytes).  The row extent is not known to the library
 // (the call carries no M); the kernel only addresses rows named by the segment table, so the
 // map declares the largest row count TMA accepts.  Columns past `cols` read as zero.
-bool encode_rows(sgmv::TmaMap* out, const void* base, int cols, int dtype, int box_rows) {
+bool encode_rows(sgmv::TmaMap* out, const void* base, int cols, int ld, int dtype, int box_rows) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
   CUtensorMap m;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), 0x7fffffffull};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};  // row stride, bytes
   const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult rc = fn(&m, dtype == SGMV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -369,16 +369,16 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
     p.tc_xchg = tc_base + static_cast<uint32_t>(slots) * sgmv::kTcSlot;
     if (slots >= 3) {
       const bool need_x = pb.mode != sgmv::kExpand, need_y = pb.mode != sgmv::kShrink;
-      if ((need_x && (!encode_rows(&p.tmap_x128, p.x, pb.h_in, pb.dtype, 128) ||
-                      !encode_rows(&p.tmap_x8, p.x, pb.h_in, pb.dtype, 8) ||
-                      !encode_rows(&p.tmap_x64, p.x, pb.h_in, pb.dtype, 64) ||
-                      !encode_rows(&p.tmap_x32, p.x, pb.h_in, pb.dtype, 32) ||
-                      !encode_rows(&p.tmap_x16, p.x, pb.h_in, pb.dtype, 16))) ||
-          (need_y && (!encode_rows(&p.tmap_y128, p.y, pb.h_out, pb.dtype, 128) ||
-                      !encode_rows(&p.tmap_y8, p.y, pb.h_out, pb.dtype, 8) ||
-                      !encode_rows(&p.tmap_y64, p.y, pb.h_out, pb.dtype, 64) ||
-                      !encode_rows(&p.tmap_y32, p.y, pb.h_out, pb.dtype, 32) ||
-                      !encode_rows(&p.tmap_y16, p.y, pb.h_out, pb.dtype, 16))))
+      if ((need_x && (!encode_rows(&p.tmap_x128, p.x, pb.h_in, p.ldx, pb.dtype, 128) ||
+                      !encode_rows(&p.tmap_x8, p.x, pb.h_in, p.ldx, pb.dtype, 8) ||
+                      !encode_rows(&p.tmap_x64, p.x, pb.h_in, p.ldx, pb.dtype, 64) ||
+                      !encode_rows(&p.tmap_x32, p.x, pb.h_in, p.ldx, pb.dtype, 32) ||
+                      !encode_rows(&p.tmap_x16, p.x, pb.h_in, p.ldx, pb.dtype, 16))) ||
+          (need_y && (!encode_rows(&p.tmap_y128, p.y, pb.h_out, p.ldy, pb.dtype, 128) ||
+                      !encode_rows(&p.tmap_y8, p.y, pb.h_out, p.ldy, pb.dtype, 8) ||
+                      !encode_rows(&p.tmap_y64, p.y, pb.h_out, p.ldy, pb.dtype, 64) ||
+                      !encode_rows(&p.tmap_y32, p.y, pb.h_out, p.ldy, pb.dtype, 32) ||
+                      !encode_rows(&p.tmap_y16, p.y, pb.h_out, p.ldy, pb.dtype, 16))))
         return SGMV_ECUDA;
       // The CUDA-core path streams a group's weights once per item of 4 rows (mostly from
       // L2); the tensor path streams them once per 128-row tile (split over the cluster).
@@ -450,6 +450,15 @@ int check_hidden(int h) {
   return SGMV_OK;
 }
 
+// Row stride (elements) of x or y: at least the row length, a multiple of 8 elements (rows
+// start 16-byte aligned for the bulk and tensor copies), at most SGMV_MAX_LD.
+int check_ld(int ld, int h) {
+  if (ld < h) return SGMV_EINVAL;
+  if (ld > SGMV_MAX_LD) return SGMV_EUNSUPPORTED;
+  if (ld % 8) return SGMV_EALIGN;
+  return SGMV_OK;
+}
+
 // Checks table entries on the device; see sgmv_validate in include/sgmv.h.
 __global__ void validate_kernel(const int32_t* ss, const int32_t* sa, int S, int num_adapters,
                                 int M, int32_t* err) {
@@ -482,11 +491,22 @@ int lora_apply_ex(void* y, const void* x, const void* const* A_ptrs, const void*
                   const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
                   int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
                   sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream) {
+  return lora_apply_strided(y, h_out, x, h_in, A_ptrs, B_ptrs, seg_starts, seg_adapter,
+                            num_segments, layer_idx, h_in, h_out, r, scale, dtype, flags, stream);
+}
+
+int lora_apply_strided(void* y, int32_t ldy, const void* x, int32_t ldx,
+                       const void* const* A_ptrs, const void* const* B_ptrs,
+                       const int32_t* seg_starts, const int32_t* seg_adapter,
+                       int32_t num_segments, int32_t layer_idx, int32_t h_in, int32_t h_out,
+                       int32_t r, float scale, sgmv_dtype_t dtype, uint32_t flags,
+                       sgmv_stream_t stream) {
   if (!flags_ok(flags)) return SGMV_EINVAL;
   int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
   if (rc != SGMV_OK) return rc;
   if (!y || !x || !A_ptrs || !B_ptrs) return SGMV_EINVAL;
   if ((rc = check_hidden(h_in)) != SGMV_OK || (rc = check_hidden(h_out)) != SGMV_OK) return rc;
+  if ((rc = check_ld(ldx, h_in)) != SGMV_OK || (rc = check_ld(ldy, h_out)) != SGMV_OK) return rc;
   if (!aligned16(y) || !aligned16(x) || (reinterpret_cast<uintptr_t>(A_ptrs) & 7u) ||
       (reinterpret_cast<uintptr_t>(B_ptrs) & 7u))
     return SGMV_EALIGN;
@@ -494,6 +514,8 @@ int lora_apply_ex(void* y, const void* x, const void* const* A_ptrs, const void*
   sgmv::Params p = {};
   p.y = y;
   p.x = x;
+  p.ldx = ldx;
+  p.ldy = ldy;
   p.A_ptrs = A_ptrs;
   p.B_ptrs = B_ptrs;
   p.seg_starts = seg_starts;
@@ -513,16 +535,27 @@ int sgmv_shrink_ex(float* v, const void* x, const void* const* A_ptrs,
                    const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
                    int32_t layer_idx, int32_t h_in, int32_t r, sgmv_dtype_t dtype,
                    uint32_t flags, sgmv_stream_t stream) {
+  return sgmv_shrink_strided(v, x, h_in, A_ptrs, seg_starts, seg_adapter, num_segments,
+                             layer_idx, h_in, r, dtype, flags, stream);
+}
+
+int sgmv_shrink_strided(float* v, const void* x, int32_t ldx, const void* const* A_ptrs,
+                        const int32_t* seg_starts, const int32_t* seg_adapter,
+                        int32_t num_segments, int32_t layer_idx, int32_t h_in, int32_t r,
+                        sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream) {
   if (!flags_ok(flags)) return SGMV_EINVAL;
   int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
   if (rc != SGMV_OK) return rc;
   if (!v || !x || !A_ptrs) return SGMV_EINVAL;
   if ((rc = check_hidden(h_in)) != SGMV_OK) return rc;
+  if ((rc = check_ld(ldx, h_in)) != SGMV_OK) return rc;
   if (!aligned16(v) || !aligned16(x) || (reinterpret_cast<uintptr_t>(A_ptrs) & 7u))
     return SGMV_EALIGN;
   if (num_segments == 0) return SGMV_OK;
   sgmv::Params p = {};
   p.x = x;
+  p.ldx = ldx;
+  p.ldy = 8;
   p.v_out = v;
   p.A_ptrs = A_ptrs;
   p.seg_starts = seg_starts;
@@ -542,16 +575,27 @@ int sgmv_expand_ex(void* y, const float* v, const void* const* B_ptrs,
                    const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
                    int32_t layer_idx, int32_t r, int32_t h_out, float scale, sgmv_dtype_t dtype,
                    uint32_t flags, sgmv_stream_t stream) {
+  return sgmv_expand_strided(y, h_out, v, B_ptrs, seg_starts, seg_adapter, num_segments,
+                             layer_idx, r, h_out, scale, dtype, flags, stream);
+}
+
+int sgmv_expand_strided(void* y, int32_t ldy, const float* v, const void* const* B_ptrs,
+                        const int32_t* seg_starts, const int32_t* seg_adapter,
+                        int32_t num_segments, int32_t layer_idx, int32_t r, int32_t h_out,
+                        float scale, sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream) {
   if (!flags_ok(flags)) return SGMV_EINVAL;
   int rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r, dtype);
   if (rc != SGMV_OK) return rc;
   if (!y || !v || !B_ptrs) return SGMV_EINVAL;
   if ((rc = check_hidden(h_out)) != SGMV_OK) return rc;
+  if ((rc = check_ld(ldy, h_out)) != SGMV_OK) return rc;
   if (!aligned16(y) || !aligned16(v) || (reinterpret_cast<uintptr_t>(B_ptrs) & 7u))
     return SGMV_EALIGN;
   if (num_segments == 0) return SGMV_OK;
   sgmv::Params p = {};
   p.y = y;
+  p.ldx = 8;
+  p.ldy = ldy;
   p.v_in = v;
   p.B_ptrs = B_ptrs;
   p.seg_starts = seg_starts;

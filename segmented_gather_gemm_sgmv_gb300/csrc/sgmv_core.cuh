@@ -84,6 +84,7 @@ struct Params {
   const int32_t* seg_adapter;
   int* err;  // library device error word
   int32_t S, layer, h_in, h_out;
+  int32_t ldx, ldy;     // row strides of x and y, in elements (>= h_in / h_out)
   float scale;
   int32_t C;            // launch cluster size (a multiple of every group size used)
   int32_t nstages;      // ring stages
@@ -615,11 +616,11 @@ struct Kernel {
     if (kind == kChunkA) {
       const int rows = e.x >> 4;
       bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>((p.kb * R + lane * p.kb) * kEb),
-               static_cast<const T*>(p.x) + static_cast<size_t>(row) * p.h_in + e.y,
+               static_cast<const T*>(p.x) + static_cast<size_t>(row) * p.ldx + e.y,
                static_cast<uint32_t>(rows * kEb), sm.full(s), pol);
     } else if (kind == kChunkY) {
       bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(lane * e.w * kEb),
-               static_cast<const T*>(p.y) + static_cast<size_t>(row) * p.h_out + e.z,
+               static_cast<const T*>(p.y) + static_cast<size_t>(row) * p.ldy + e.z,
                static_cast<uint32_t>(e.w * kEb), sm.full(s), pol);
     } else if (kind == kChunkV) {
       bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(lane * R * 4),
@@ -942,7 +943,7 @@ struct Kernel {
         if (tid == 0) {
           if (w.ok()) {
             for (int i = 0; i < nrow; ++i)
-              bulk_s2g(static_cast<T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.h_out + mp.n0 +
+              bulk_s2g(static_cast<T*>(p.y) + static_cast<size_t>(d[2 + i]) * p.ldy + mp.n0 +
                            pass * mp.w_full,
                        ys + static_cast<uint32_t>(i * wdt * kEb), static_cast<uint32_t>(wdt * kEb));
             bulk_commit();

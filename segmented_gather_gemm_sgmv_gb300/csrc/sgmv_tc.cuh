@@ -293,7 +293,7 @@ struct TcRole {
             if (tok < 0 || ((mask >> (m >> 3)) & 1u)) continue;
             const uint32_t d = dst + sw128(m, ch);
             if (k0 + ch * 8 < p.h_in)
-              cp_async16(d, x + static_cast<size_t>(tok) * p.h_in + k0 + ch * 8);
+              cp_async16(d, x + static_cast<size_t>(tok) * p.ldx + k0 + ch * 8);
             else
               cp_async16_zero(d, x);
           }
@@ -342,7 +342,7 @@ struct TcRole {
             const int tok = rt[m];
             if (tok < 0 || ch >= nvalid || ((mask >> (m >> 3)) & 1u)) continue;
             cp_async16(dst + kYSlotOff + sw128(m, ch),
-                       y + static_cast<size_t>(tok) * p.h_out + n0 + ch * 8);
+                       y + static_cast<size_t>(tok) * p.ldy + n0 + ch * 8);
           }
         }
         cp_async_arrive(bar);
@@ -640,7 +640,7 @@ struct TcRole {
             const int rr = q * 32 + i * 4 + (lane >> 3), cc = lane & 7;
             const int tok = rt[rr];
             if (tok >= 0 && cc < nvalid && !((mask >> (rr >> 3)) & 1u))
-              *reinterpret_cast<uint4*>(y + static_cast<size_t>(tok) * p.h_out + n0 + cc * 8) =
+              *reinterpret_cast<uint4*>(y + static_cast<size_t>(tok) * p.ldy + n0 + cc * 8) =
                   lds128(ys + sw128(rr, cc));
           }
         }

@@ -39,6 +39,7 @@ def test_header_constants_match_binding():
     assert f"#define SGMV_NO_TENSOR_CORES {binding.SGMV_NO_TENSOR_CORES}u" in text
     assert f"#define SGMV_TENSOR_CORES_ALWAYS {binding.SGMV_TENSOR_CORES_ALWAYS}u" in text
     assert f"#define SGMV_LONG_BATCH {binding.SGMV_LONG_BATCH}u" in text
+    assert "#define SGMV_MAX_LD (1 << 24)" in text and binding.SGMV_MAX_LD == 1 << 24
     for name, val in [("SGMV_EINVAL", -1), ("SGMV_EALIGN", -2), ("SGMV_EUNSUPPORTED", -3),
                       ("SGMV_ECUDA", -4), ("SGMV_ETIMEOUT", -5)]:
         assert re.search(rf"{name}\s*=\s*{val}\b", text), name
@@ -83,6 +84,32 @@ def test_lora_apply_ex_flags(L):
     assert L.lora_apply_ex(*args, 6, None) == -1  # never + always
     assert L.lora_apply_ex(*args, 14, None) == -1
     assert L.lora_apply_ex(*args, 16, None) == -1  # unknown bit
+
+
+def test_strided_host_checks(L):
+    """Row strides: below the row length -> EINVAL, not a multiple of 8 -> EALIGN, above
+    SGMV_MAX_LD -> EUNSUPPORTED; valid strides with num_segments = 0 -> OK (no launch)."""
+    a = OK_ARGS
+    h_in, h_out = a["h_in"], a["h_out"]
+
+    def fused(ldy, ldx, S=0):
+        return L.lora_apply_strided(a["y"], ldy, a["x"], ldx, a["A"], a["B"], a["ss"], a["sa"], S,
+                                    a["layer"], h_in, h_out, a["r"], a["scale"], a["dt"], 0, None)
+    assert fused(h_out, h_in) == 0
+    assert fused(h_out + 64, h_in + 8) == 0
+    assert fused(h_out - 8, h_in, S=4) == -1
+    assert fused(h_out, h_in - 8, S=4) == -1
+    assert fused(h_out + 4, h_in, S=4) == -2
+    assert fused(h_out, h_in + 12, S=4) == -2
+    assert fused(h_out, (1 << 24) + 8, S=4) == -3
+    assert L.sgmv_shrink_strided(a["y"], a["x"], h_in - 8, a["A"], a["ss"], a["sa"], 4, 0, h_in,
+                                 16, 1, 0, None) == -1
+    assert L.sgmv_shrink_strided(a["y"], a["x"], h_in + 8, a["A"], a["ss"], a["sa"], 0, 0, h_in,
+                                 16, 1, 0, None) == 0
+    assert L.sgmv_expand_strided(a["y"], h_out + 2, a["x"], a["B"], a["ss"], a["sa"], 4, 0, 16,
+                                 h_out, 1.0, 1, 0, None) == -2
+    assert L.sgmv_expand_strided(a["y"], h_out + 8, a["x"], a["B"], a["ss"], a["sa"], 0, 0, 16,
+                                 h_out, 1.0, 1, 0, None) == 0
 
 
 def test_shrink_expand_validate_host_checks(L):
