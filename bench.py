@@ -174,7 +174,7 @@ class Setup:
     """Device-resident inputs of the workload: pool, NB rotating x/y sets, segment table."""
 
     def __init__(self, w, device, nbuf=32, seed=0, overlap=True, tensor_cores="auto",
-                 long_batch=False):
+                 long_batch=False, strided=False):
         import torch
         self.w = w
         self.overlap = overlap
@@ -189,8 +189,15 @@ class Setup:
         self.d_sa = torch.as_tensor(self.sa, device=device)
         self.nbuf = nbuf
         self.x, self.y = [], []
+        self.strided = strided
         for i in range(nbuf):
             x, y = workloads.make_activations(w, self.M, device, seed=seed + 100 + i)
+            if strided:  # the middle third of 3x-wide rows, as q / k / v of a fused output
+                X = torch.zeros((self.M, 3 * w.h_in), dtype=x.dtype, device=device)
+                Y = torch.zeros((self.M, 3 * w.h_out), dtype=y.dtype, device=device)
+                X[:, w.h_in:2 * w.h_in] = x
+                Y[:, w.h_out:2 * w.h_out] = y
+                x, y = X[:, w.h_in:2 * w.h_in], Y[:, w.h_out:2 * w.h_out]
             self.x.append(x)
             self.y.append(y)
 
@@ -360,7 +367,8 @@ def run_ours(args):
     binding.lib()
     w = workloads.WORKLOADS[args.workload]
     long_batch = {"auto": w.prefill, "on": True, "off": False}[args.long_batch]
-    setup = Setup(w, device, tensor_cores=args.tensor_cores, long_batch=long_batch)
+    setup = Setup(w, device, tensor_cores=args.tensor_cores, long_batch=long_batch,
+                  strided=args.strided)
     stream = torch.cuda.Stream(device)
     nbytes, M = algorithmic_bytes(w, setup.ss, setup.sa)
     K, W = args.steps, args.warmup
@@ -416,10 +424,13 @@ def run_ours(args):
                              "launching stream",
                    "l2": "inputs larger than L2: each step reads another layer's weights and "
                          "another x/y set (sweep footprint > 129 MB)",
+                   "layout": ("x, y: middle column third of rows 3 h apart (lora_apply_strided)"
+                              if setup.strided else "x [M][h_in], y [M][h_out] dense"),
                    "parallelism": f"replica x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "traffic": recorded_traffic(w.name), "peak_source": peak_kind,
+                     "traffic": None if setup.strided else recorded_traffic(w.name),
+                     "peak_source": peak_kind,
                      "kernel": "sgmv_kernel<fused> (lora_apply)"},
         "e2e": {"value": round(job_value(world, nbytes, e2e_s), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -504,6 +515,9 @@ def main():
     ap.add_argument("--long-batch", choices=["auto", "on", "off"], default="auto",
                     help="SGMV_LONG_BATCH launches; auto: for workloads that hold prefill "
                          "segments (prefill_mixed, mixed_70b)")
+    ap.add_argument("--strided", action="store_true",
+                    help="x and y are the middle column third of 3x-wide activations "
+                         "(lora_apply_strided; the e2e figure stays on dense copies)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain lora_apply launches (no programmatic dependent launch)")
     args = ap.parse_args()
