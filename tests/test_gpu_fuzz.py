@@ -41,6 +41,9 @@ def _draw(i):
     r = int(rng.choice([8, 16, 32, 64]))
     h_in = int(8 * rng.integers(4, 80))
     h_out = int(8 * rng.integers(4, 80))
+    if rng.random() < 0.12:  # now and then a model-sized projection
+        h_in = int(rng.choice([4096, 8192]))
+        h_out = int(rng.choice([4096, 11008]))
     n_adapters = int(rng.integers(2, 9))
     lens, ids = [], []
     for _ in range(int(rng.integers(1, 24))):
@@ -91,3 +94,31 @@ def test_random_case_matches_oracle(i):
         outside = torch.ones_like(Y, dtype=torch.bool)
         outside[:, 16:16 + h_out] = False
         assert torch.equal(Y[outside], Y0[outside]), f"{what}: elements outside the slice changed"
+
+
+@pytest.mark.parametrize("i", range(N_CASES // 2))
+def test_random_unfused_case_matches_oracle(i):
+    """sgmv_shrink then sgmv_expand on the same draws: v against the oracle's shrink, y against
+    the oracle's expand of the library's v."""
+    import oracle
+    from segmented_gather_gemm_sgmv_gb300 import sgmv_expand, sgmv_shrink
+    dtype, r, h_in, h_out, n_adapters, lens, ids, opts, strided = _draw(5000 + i)
+    ss = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    sa = np.asarray(ids, np.int32)
+    w = workloads.Workload("fuzz_unfused", h_in, h_out, r, dtype, n_adapters, 2)
+    c = harness.make_case(w, ss, sa, M=int(ss[-1]) + 2, seed=i)
+    layer = 1 - i % 2
+    what = f"unfused case {i}: {dtype} r{r} {h_in}->{h_out} lens={lens} ids={ids} {opts}"
+    keys = harness.touched(sa, ss)
+    A = harness.oracle_blocks(c.A, keys, layer)
+    B = harness.oracle_blocks(c.B, keys, layer)
+    kw = dict(tensor_cores=opts["tensor_cores"], long_batch=opts["long_batch"])
+    v = torch.full((c.M, r), -7.0, device="cuda")
+    sgmv_shrink(v, c.x, c.A_ptrs, c.d_ss, c.d_sa, layer, r, **kw)
+    v_ref = oracle.sgmv_shrink(np.full((c.M, r), -7.0), c.x.double().cpu().numpy(), A, ss, sa, 0)
+    harness.assert_close(v.cpu().numpy(), v_ref, what + " shrink", atol=1e-3, rtol=1e-3)
+    y = c.y0.clone()
+    sgmv_expand(y, v, c.B_ptrs, c.d_ss, c.d_sa, layer, r, w.scale, **kw)
+    y_ref = oracle.sgmv_expand(c.y0.double().cpu().numpy(), v.double().cpu().numpy(), B, ss, sa,
+                               0, w.scale)
+    harness.assert_close(y.float().cpu().numpy(), y_ref, what + " expand")
