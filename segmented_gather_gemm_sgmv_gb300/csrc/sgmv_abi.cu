@@ -23,16 +23,15 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kPairSmem = 114688;  // 112 KB: two CTAs fit on an SM (228 KB), so the next
                                       // kernel of the stream can start beside this one
 constexpr size_t kMaxSmem = 232448;   // 227 KB: large segment tables (one CTA per SM)
+constexpr int kWideMaxSegments = 64;  // long-batch tables up to this size use the wide kernel
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
-struct KernelCache {
+struct KernelCache {  // per kernel instantiation
   const void* fn = nullptr;
   size_t smem_set = 0;
-  // grid size per launch geometry (0: two CTAs per SM, 1: SGMV_LONG_BATCH), cached with the
-  // cluster size and shared-memory size it was computed for
-  int cluster[2] = {0, 0};
-  size_t smem_q[2] = {0, 0};
-  int max_clusters[2] = {0, 0};
+  int cluster = 0;     // the grid size below was computed for this cluster size...
+  size_t smem_q = 0;   // ...and this shared-memory size
+  int max_clusters = 0;
 };
 
 struct DeviceState {
@@ -41,7 +40,7 @@ struct DeviceState {
   int* err = nullptr;
   uint64_t wait_ns = kDefaultWaitNs;
   int inject = 0;
-  KernelCache cache[3][3][4];  // dtype, mode, rank index
+  KernelCache cache[3][3][4][2];  // dtype, mode, rank index, geometry (SGMV_LONG_BATCH)
 };
 
 std::mutex g_mu;
@@ -58,6 +57,7 @@ struct Tuning {
   int xchg_kb = 64;      // cost of one partial-sum exchange in streamed KB (group size rule)
   int tc_min_mb = 32;    // ...and whose CUDA-core items would re-read at least this many MB of
                          // weights (ceil(rows / 4) items x the adapter's A and B)
+  int wide_threads = 1;  // SGMV_LONG_BATCH launches use the 416-thread kernel (0: 288 threads)
 };
 
 Tuning read_tuning() {
@@ -68,6 +68,7 @@ Tuning read_tuning() {
   if (const char* s = std::getenv("SGMV_TC_MIN_ROWS")) t.tc_min_rows = std::max(16, std::atoi(s));
   if (const char* s = std::getenv("SGMV_TC_MIN_MB")) t.tc_min_mb = std::max(0, std::atoi(s));
   if (const char* s = std::getenv("SGMV_XCHG_KB")) t.xchg_kb = std::max(0, std::atoi(s));
+  if (const char* s = std::getenv("SGMV_WIDE_THREADS")) t.wide_threads = std::atoi(s) != 0;
   return t;
 }
 const Tuning& tuning() {
@@ -153,11 +154,11 @@ int device_state(DeviceState** out) {
   return SGMV_OK;
 }
 
-const void* kernel_for(int dtype, int mode, int r) {
+const void* kernel_for(int dtype, int mode, int r, bool wide) {
   switch (dtype) {
-    case SGMV_F32: return sgmv::kernel_f32(mode, r);
-    case SGMV_F16: return sgmv::kernel_f16(mode, r);
-    case SGMV_BF16: return sgmv::kernel_bf16(mode, r);
+    case SGMV_F32: return sgmv::kernel_f32(mode, r, wide);
+    case SGMV_F16: return sgmv::kernel_f16(mode, r, wide);
+    case SGMV_BF16: return sgmv::kernel_bf16(mode, r, wide);
     default: return nullptr;
   }
 }
@@ -302,7 +303,13 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   p.wait_limit_ns = st->wait_ns;
   p.inject_stall = st->inject;
 
-  const void* fn = kernel_for(pb.dtype, pb.mode, pb.r);
+  // The 416-thread kernel (a second tensor-role epilogue warpgroup) measured faster where the
+  // tensor role dominates (prefill_mixed, 8 segments: 61.1 -> 58.3 us) and slower on the
+  // CUDA-core role (the 70B mix, 482 segments: 101.0 -> 105.6 us); a table of many segments
+  // means many decode rows, so those keep the 288-thread kernel.
+  const bool wide_kernel = wide && tuning().wide_threads && pb.S <= kWideMaxSegments;
+  const void* fn = kernel_for(pb.dtype, pb.mode, pb.r, wide_kernel);
+  const int threads = wide_kernel ? sgmv::kThreadsWide : sgmv::kThreads;
   if (!fn) return SGMV_EUNSUPPORTED;
   const bool clustered = pb.mode != sgmv::kExpand;
   // Tensor role (16-bit types, r >= 16; every mode): it uses none of the CUDA-core scratch
@@ -315,7 +322,7 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   int grid = 0;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    KernelCache& kc = st->cache[pb.dtype][pb.mode][rank_index(pb.r)];
+    KernelCache& kc = st->cache[pb.dtype][pb.mode][rank_index(pb.r)][wide_kernel ? 1 : 0];
     if (kc.smem_set < smem) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem)) != cudaSuccess)
@@ -326,14 +333,13 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
         return SGMV_ECUDA;
       kc.smem_set = smem;
     }
-    const int g = wide ? 1 : 0;
-    if (kc.cluster[g] != p.C || kc.smem_q[g] != smem) {
+    if (kc.cluster != p.C || kc.smem_q != smem) {
       int n = 0;
       if (clustered) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         cfg.gridDim = dim3(static_cast<unsigned>(p.C * st->sms), 1, 1);
-        cfg.blockDim = dim3(sgmv::kThreads, 1, 1);
+        cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
         cfg.dynamicSmemBytes = smem;
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
@@ -344,18 +350,18 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
         if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) return SGMV_ECUDA;
       } else {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, sgmv::kThreads, smem) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) !=
             cudaSuccess)
           return SGMV_ECUDA;
         n = per_sm * st->sms / p.C;
       }
       n = std::min(n, std::max(1, st->sms / p.C));  // one CTA per SM per kernel
       if (n <= 0) return SGMV_EUNSUPPORTED;
-      kc.cluster[g] = p.C;
-      kc.smem_q[g] = smem;
-      kc.max_clusters[g] = n;
+      kc.cluster = p.C;
+      kc.smem_q = smem;
+      kc.max_clusters = n;
     }
-    grid = kc.max_clusters[g] * p.C;
+    grid = kc.max_clusters * p.C;
   }
 
   // Tensor role: at least three ring slots and two clusters in the grid.
@@ -400,7 +406,7 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(sgmv::kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   unsigned na = 0;

@@ -41,7 +41,9 @@ namespace sgmv {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kThreads = kConsumers + 32;  // + one producer warp (two CTAs per SM)
+// Long-batch launches (one CTA per SM): + four warps, a second tensor-role epilogue warpgroup.
+constexpr int kThreadsWide = kThreads + 128;
 constexpr int kStatusTimeout = -5;         // SGMV_ETIMEOUT
 constexpr int kRowsMax = 4;                // rows per CUDA-core work item
 
@@ -340,11 +342,11 @@ struct RingPos {
 
 // ---- scheduler ------------------------------------------------------------------------
 // Exclusive scan of `cnt(i)` over i in [0, n) into out[0..n] (out[n] = total), all threads.
-template <typename F>
+template <int NT, typename F>
 __device__ __forceinline__ void block_exclusive_scan(int n, int* out, int* wsum, F cnt) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kWarps = kThreads / 32;
-  const int per = (n + kThreads - 1) / kThreads;
+  constexpr int kWarps = NT / 32;
+  const int per = (n + NT - 1) / NT;
   const int lo = min(tid * per, n), hi = min(lo + per, n);
   int local = 0;
   for (int i = lo; i < hi; ++i) local += cnt(i);
@@ -384,6 +386,7 @@ static __device__ __forceinline__ uint32_t hash_slot(int k, int mask) {
 // first non-empty segment of its adapter; its group gets ceil(rows / kRowsMax) items, and
 // gcnt[lead] holds the group's row count.
 // `scratch` (transient) holds slot[S] and the hash table (3 * hash_slots ints).
+template <int NT>
 static __device__ __forceinline__ void build_schedule(const Params& p, int* starts, int* adapters,
                                                       int* base, int* gcnt, int* tbase,
                                                       int* scratch, int* wsum) {
@@ -398,27 +401,27 @@ static __device__ __forceinline__ void build_schedule(const Params& p, int* star
   int st_v[kPer], ad_v[kPer];
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
-    const int i = tid + u * kThreads;
+    const int i = tid + u * NT;
     st_v[u] = (i <= S) ? __ldg(p.seg_starts + i) : 0;
     ad_v[u] = (i < S) ? __ldg(p.seg_adapter + i) : 0;
   }
-  for (int h = tid; h < HS; h += kThreads) {
+  for (int h = tid; h < HS; h += NT) {
     hkey[h] = -1;
     hlead[h] = 0x7fffffff;
     hcnt[h] = 0;
   }
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
-    const int i = tid + u * kThreads;
+    const int i = tid + u * NT;
     if (i <= S) starts[i] = st_v[u];
     if (i < S) adapters[i] = ad_v[u];
   }
-  for (int i = tid + kPer * kThreads; i <= S; i += kThreads) {
+  for (int i = tid + kPer * NT; i <= S; i += NT) {
     starts[i] = __ldg(p.seg_starts + i);
     if (i < S) adapters[i] = __ldg(p.seg_adapter + i);
   }
   __syncthreads();
-  for (int i = tid; i < S; i += kThreads) {
+  for (int i = tid; i < S; i += NT) {
     const int k = adapters[i];
     const int len = starts[i + 1] - starts[i];
     int h = -1;
@@ -436,9 +439,9 @@ static __device__ __forceinline__ void build_schedule(const Params& p, int* star
   }
   __syncthreads();
   const int tcmin = p.tc_min_rows;
-  int* any_long = wsum + kThreads / 32 + 1;  // set when some group goes to the tensor role
+  int* any_long = wsum + NT / 32 + 1;  // set when some group goes to the tensor role
   if (threadIdx.x == 0) *any_long = 0;
-  block_exclusive_scan(S, base, wsum, [&](int i) {
+  block_exclusive_scan<NT>(S, base, wsum, [&](int i) {
     const int h = slot[i];
     const bool lead = h >= 0 && hlead[h] == i;
     const int rows = lead ? hcnt[h] : 0;
@@ -448,7 +451,7 @@ static __device__ __forceinline__ void build_schedule(const Params& p, int* star
   });
   // Groups of at least tc_min_rows rows: m-tiles of 128 rows for the tensor role.
   if (*any_long)
-    block_exclusive_scan(S, tbase, wsum, [&](int i) {
+    block_exclusive_scan<NT>(S, tbase, wsum, [&](int i) {
       const int rows = gcnt[i];
       return rows >= tcmin ? (rows + 127) / 128 : 0;
     });
@@ -502,7 +505,7 @@ static __device__ __forceinline__ void decode_item(const Params& p, int t, const
 namespace sgmv {
 
 // ---- the kernel ------------------------------------------------------------------------
-template <typename T, int R, int MODE>
+template <typename T, int R, int MODE, int NT>
 struct Kernel {
   using E = Elem<T>;
   using Walk = StageWalk<R, MODE>;
@@ -1000,7 +1003,7 @@ struct Kernel {
     }
     __syncthreads();
     int a = 0, b = 0;
-    for (int i = tid; i < p.S; i += kThreads) {
+    for (int i = tid; i < p.S; i += NT) {
       const int g = gcnt[i];
       if (g >= p.tc_min_rows) a += g; else b += g;
     }
@@ -1053,7 +1056,7 @@ struct Kernel {
       mbar_init(sm.fixed(kNever), 1);
     }
     int* tbase = gcnt + p.S;
-    build_schedule(p, starts, adapters, base, gcnt, tbase,
+    build_schedule<NT>(p, starts, adapters, base, gcnt, tbase,
                    reinterpret_cast<int*>(smem + p.off_ring), ctl + 4);
     const int n_items = base[p.S];
     const int N = static_cast<int>(gridDim.x);
@@ -1073,7 +1076,7 @@ struct Kernel {
         fence_proxy_async();  // the ring held the hash table
         // (the tensor role makes its own cluster barriers: one after its barriers are
         // initialised, one before exit)
-        TcRole<T, R, MODE>::run(p, smem, starts, adapters, gcnt, tbase, ctl,
+        TcRole<T, R, MODE, NT>::run(p, smem, starts, adapters, gcnt, tbase, ctl,
                                 static_cast<int>(blockIdx.x), n_tc, tbase[p.S]);
         return;
       }
@@ -1132,9 +1135,10 @@ struct Kernel {
     const int n_my = (grp.gid < n_items) ? (n_items - grp.gid + grp.ng - 1) / grp.ng : 0;
     const MemberPlan& mp = p.plan[(grp.size - 1) + grp.m];
 
-    if (warp == kConsumerWarps) {
-      producer(p, sm, w, grp, mp, starts, adapters, base, gcnt,
-               reinterpret_cast<int4*>(smem + p.off_stab), n_my);
+    if (warp >= kConsumerWarps) {  // the producer, and the warps of the wide geometry that
+      if (warp == kConsumerWarps)   // only the tensor role uses
+        producer(p, sm, w, grp, mp, starts, adapters, base, gcnt,
+                 reinterpret_cast<int4*>(smem + p.off_stab), n_my);
       if (MODE != kExpand) {
         cluster_wait();
         cluster_arrive_relaxed();
@@ -1151,9 +1155,24 @@ struct Kernel {
   }
 };
 
+// Two CTAs per SM (the default geometry): 288 threads at <= 96 registers.
 template <typename T, int R, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) sgmv_kernel(const __grid_constant__ Params p) {
-  Kernel<T, R, MODE>::run(p);
+  Kernel<T, R, MODE, kThreads>::run(p);
+}
+
+// One CTA per SM (SGMV_LONG_BATCH): 416 threads (a second tensor-role epilogue warpgroup).
+template <typename T, int R, int MODE>
+__global__ void __launch_bounds__(kThreadsWide, 1)
+    sgmv_kernel_wide(const __grid_constant__ Params p) {
+  Kernel<T, R, MODE, kThreadsWide>::run(p);
+}
+
+// Host-side handle of one instantiation (for the launch).
+template <typename T, int R, int MODE>
+static const void* kernel_ptr(bool wide) {
+  return wide ? reinterpret_cast<const void*>(&sgmv_kernel_wide<T, R, MODE>)
+              : reinterpret_cast<const void*>(&sgmv_kernel<T, R, MODE>);
 }
 
 }  // namespace sgmv

@@ -5,21 +5,21 @@
 namespace sgmv {
 
 template <int MODE>
-static const void* pick_bf16(int r) {
+static const void* pick_bf16(int r, bool wide) {
   switch (r) {
-    case 8: return reinterpret_cast<const void*>(&sgmv_kernel<__nv_bfloat16, 8, MODE>);
-    case 16: return reinterpret_cast<const void*>(&sgmv_kernel<__nv_bfloat16, 16, MODE>);
-    case 32: return reinterpret_cast<const void*>(&sgmv_kernel<__nv_bfloat16, 32, MODE>);
-    case 64: return reinterpret_cast<const void*>(&sgmv_kernel<__nv_bfloat16, 64, MODE>);
+    case 8: return kernel_ptr<__nv_bfloat16, 8, MODE>(wide);
+    case 16: return kernel_ptr<__nv_bfloat16, 16, MODE>(wide);
+    case 32: return kernel_ptr<__nv_bfloat16, 32, MODE>(wide);
+    case 64: return kernel_ptr<__nv_bfloat16, 64, MODE>(wide);
     default: return nullptr;
   }
 }
 
-const void* kernel_bf16(int mode, int r) {
+const void* kernel_bf16(int mode, int r, bool wide) {
   switch (mode) {
-    case kFused: return pick_bf16<kFused>(r);
-    case kShrink: return pick_bf16<kShrink>(r);
-    case kExpand: return pick_bf16<kExpand>(r);
+    case kFused: return pick_bf16<kFused>(r, wide);
+    case kShrink: return pick_bf16<kShrink>(r, wide);
+    case kExpand: return pick_bf16<kExpand>(r, wide);
     default: return nullptr;
   }
 }

@@ -5,21 +5,21 @@
 namespace sgmv {
 
 template <int MODE>
-static const void* pick_f32(int r) {
+static const void* pick_f32(int r, bool wide) {
   switch (r) {
-    case 8: return reinterpret_cast<const void*>(&sgmv_kernel<float, 8, MODE>);
-    case 16: return reinterpret_cast<const void*>(&sgmv_kernel<float, 16, MODE>);
-    case 32: return reinterpret_cast<const void*>(&sgmv_kernel<float, 32, MODE>);
-    case 64: return reinterpret_cast<const void*>(&sgmv_kernel<float, 64, MODE>);
+    case 8: return kernel_ptr<float, 8, MODE>(wide);
+    case 16: return kernel_ptr<float, 16, MODE>(wide);
+    case 32: return kernel_ptr<float, 32, MODE>(wide);
+    case 64: return kernel_ptr<float, 64, MODE>(wide);
     default: return nullptr;
   }
 }
 
-const void* kernel_f32(int mode, int r) {
+const void* kernel_f32(int mode, int r, bool wide) {
   switch (mode) {
-    case kFused: return pick_f32<kFused>(r);
-    case kShrink: return pick_f32<kShrink>(r);
-    case kExpand: return pick_f32<kExpand>(r);
+    case kFused: return pick_f32<kFused>(r, wide);
+    case kShrink: return pick_f32<kShrink>(r, wide);
+    case kExpand: return pick_f32<kExpand>(r, wide);
     default: return nullptr;
   }
 }

@@ -6,9 +6,10 @@
 namespace sgmv {
 
 // Returns the __global__ function for (mode, rank) of one element type, or nullptr when the
-// rank is not instantiated.  mode: 0 fused, 1 shrink, 2 expand.
-const void* kernel_f32(int mode, int r);
-const void* kernel_f16(int mode, int r);
-const void* kernel_bf16(int mode, int r);
+// rank is not instantiated.  mode: 0 fused, 1 shrink, 2 expand.  wide: the long-batch
+// instantiation (kThreadsWide threads, one CTA per SM) instead of the default one.
+const void* kernel_f32(int mode, int r, bool wide);
+const void* kernel_f16(int mode, int r, bool wide);
+const void* kernel_bf16(int mode, int r, bool wide);
 
 }  // namespace sgmv

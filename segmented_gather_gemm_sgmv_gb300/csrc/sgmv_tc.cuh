@@ -120,7 +120,7 @@ struct TcWalk {
   }
 };
 
-template <typename T, int R, int MODE>
+template <typename T, int R, int MODE, int NT>
 struct TcRole {
   // Fused: shrink, v kept in TMEM, expand.  Shrink only: v rows written to v_out (fp32).
   // Expand only: v rows read from v_in (fp32) into TMEM, then the expand.
@@ -131,6 +131,10 @@ struct TcRole {
   // Shrink: N = 64 columns of v (columns >= r are never read).  Expand: N = 64 columns of y.
   static constexpr uint32_t kIdShrink = idesc_f16(kBf16, true, kTcRows, 64);
   static constexpr uint32_t kIdExpand = idesc_f16(kBf16, true, kTcRows, kTcN);
+  // Epilogue warpgroups: the wide (long-batch) instantiation has a second one (warps 9-12)
+  // that takes every other n-tile and owns the second D buffer; the first one (warps 4-7) also
+  // does the per-m-tile work (v exchange, hi / lo into TMEM).
+  static constexpr int kGroups = (NT == kThreadsWide && kDoExpand) ? 2 : 1;
   static constexpr int kASlotOff = kTcXBytes;  // A rows follow the x rows in a shrink slot
   static constexpr int kYSlotOff = 8192;       // y rows follow the B rows in an expand slot
 
@@ -532,73 +536,81 @@ struct TcRole {
 
   // ------------------------------------------------------------------------ epilogue ----
   __device__ __forceinline__ static void epilogue(const Params& p, const Ctx& c, const Waiter& w,
-                                                  TcWalk wk, uint32_t tm) {
-    const int et = threadIdx.x - kTcLoaders;  // 0..127
-    const int q = et >> 5, lane = et & 31;    // TMEM lane quarter, lane
-    const int row = et;                       // tile row = TMEM lane
+                                                  TcWalk wk, uint32_t tm, int g) {
+    const int q = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;  // TMEM lane quarter, lane
+    const int row = q * 32 + lane;                                   // tile row = TMEM lane
     const uint32_t tq = tm + (static_cast<uint32_t>(q * 32) << 16);
     T* y = static_cast<T*>(p.y);
     pdl_wait_prior();
     Ring rg{0, 0};
-    int dq = 0;
+    // D buffer of the n-tiles this warpgroup takes: the issuer alternates the two buffers over
+    // the CTA's n-tile sequence; with two groups, group g owns buffer g (every other n-tile).
+    int dq = kGroups == 2 ? g : 0;
     uint32_t dpar = 0;
+    uint32_t jn = 0;   // n-tiles of the CTA so far (all groups)
     uint32_t rnd = 0;  // split-K exchange rounds so far (barrier parity)
     for (int li = 0; wk.next(); ++li) {
       const int par = li & 1;
       if (!wwait(w, c.fx(kTcRtFull0 + par), (li >> 1) & 1)) return;
       const int* rt = c.rowtok + par * kTcRows;
       const int tok_row = rt[row];
-      if constexpr (kDoShrink) {
-        if (!wwait(w, c.fx(kTcVFull), li & 1)) return;
-      }
-      if constexpr (kDoExpand) {
-        if (!wwait(w, c.fx(kTcHFree), (li & 1) ^ 1)) return;
-      }
-      tc_fence_after();
-      if constexpr (kDoShrink) {
-        if (c.split) {
-          if (!exchange(p, c, w, tq, q, lane, tok_row, rnd)) return;
-          rnd += R / 16;
-        } else {
+      if (g == 0) {  // the per-m-tile work: v into TMEM as hi / lo
+        if constexpr (kDoShrink) {
+          if (!wwait(w, c.fx(kTcVFull), li & 1)) return;
+        }
+        if constexpr (kDoExpand) {
+          if (!wwait(w, c.fx(kTcHFree), (li & 1) ^ 1)) return;
+        }
+        tc_fence_after();
+        if constexpr (kDoShrink) {
+          if (c.split) {
+            if (!exchange(p, c, w, tq, q, lane, tok_row, rnd)) return;
+            rnd += R / 16;
+          } else {
+#pragma unroll
+            for (int c0 = 0; c0 < R; c0 += 16) {
+              uint32_t v[16];
+              tmem_ld16(tq + kTmV + c0, v);
+              tmem_wait_ld();
+              finish16(p, tq, c0, v, tok_row);
+            }
+          }
+        } else {  // expand only: v rows from v_in
 #pragma unroll
           for (int c0 = 0; c0 < R; c0 += 16) {
             uint32_t v[16];
-            tmem_ld16(tq + kTmV + c0, v);
-            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (tok_row >= 0)
+                f = reinterpret_cast<const float4*>(p.v_in + static_cast<size_t>(tok_row) * R +
+                                                    c0)[e];
+              v[4 * e] = __float_as_uint(f.x);
+              v[4 * e + 1] = __float_as_uint(f.y);
+              v[4 * e + 2] = __float_as_uint(f.z);
+              v[4 * e + 3] = __float_as_uint(f.w);
+            }
             finish16(p, tq, c0, v, tok_row);
           }
         }
-      } else {  // expand only: v rows from v_in
-#pragma unroll
-        for (int c0 = 0; c0 < R; c0 += 16) {
-          uint32_t v[16];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (tok_row >= 0)
-              f = reinterpret_cast<const float4*>(p.v_in + static_cast<size_t>(tok_row) * R +
-                                                  c0)[e];
-            v[4 * e] = __float_as_uint(f.x);
-            v[4 * e + 1] = __float_as_uint(f.y);
-            v[4 * e + 2] = __float_as_uint(f.z);
-            v[4 * e + 3] = __float_as_uint(f.w);
-          }
-          finish16(p, tq, c0, v, tok_row);
+        if constexpr (kDoExpand) tmem_wait_st();
+        tc_fence_before();
+        if constexpr (kDoShrink) mbar_arrive(c.fx(kTcVFree));
+        if constexpr (MODE == kShrink) {
+          mbar_arrive(c.fx(kTcRtFree0 + par));
+          continue;
         }
+        mbar_arrive(c.fx(kTcHReady));
       }
-      if constexpr (kDoExpand) tmem_wait_st();
-      tc_fence_before();
-      if constexpr (kDoShrink) mbar_arrive(c.fx(kTcVFree));
-      if constexpr (MODE == kShrink) {
-        mbar_arrive(c.fx(kTcRtFree0 + par));
-        continue;
-      }
-      mbar_arrive(c.fx(kTcHReady));
       // skip the shrink slots of this m-tile
       for (int kc = c.k_lo; kc < c.k_hi; ++kc) rg.next(c.slots);
       const uint32_t mask = static_cast<uint32_t>(c.tmask[par]);
       int pend = -1;  // ring slot whose TMA stores may still be reading it
-      for (int nt = wk.a; nt < wk.b; ++nt) {
+      for (int nt = wk.a; nt < wk.b; ++nt, ++jn) {
+        if (kGroups == 2 && static_cast<int>(jn & 1u) != g) {  // the other group's n-tile
+          rg.next(c.slots);
+          continue;
+        }
         // y rows of the slot (landed with the slot) into registers while the MMAs run
         if (!wwait(w, c.full(rg.s), rg.par)) return;
         const uint32_t ys = c.slot(rg.s) + kYSlotOff;
@@ -651,7 +663,9 @@ struct TcRole {
         if (lane == 0 && pend >= 0) mbar_arrive(c.empty(pend));
         pend = rg.s;
         rg.next(c.slots);
-        if (++dq == 2) {
+        if (kGroups == 2) {
+          dpar ^= 1u;
+        } else if (++dq == 2) {
           dq = 0;
           dpar ^= 1u;
         }
@@ -747,8 +761,8 @@ struct TcRole {
       mbar_init(c.fx(kTcDEmpty1), 4);
       mbar_init(c.fx(kTcRtFull0), 1);
       mbar_init(c.fx(kTcRtFull1), 1);
-      mbar_init(c.fx(kTcRtFree0), kTcEpi + 4);  // epilogue threads + the four loader warps
-      mbar_init(c.fx(kTcRtFree1), kTcEpi + 4);
+      mbar_init(c.fx(kTcRtFree0), kTcEpi * kGroups + 4);  // epilogue threads + 4 loader warps
+      mbar_init(c.fx(kTcRtFree1), kTcEpi * kGroups + 4);
       mbar_init(c.fx(kTcRsFull), 1);  // the owner's expect_tx arrival + three partials' bytes
       mbar_init(c.fx(kTcAgFull), 1);  // the owner's expect_tx arrival + three owners' bytes
       mbar_init(c.fx(kTcNever), 1);
@@ -805,8 +819,10 @@ struct TcRole {
     if (warp < 4) {
       loader(p, c, w, wk);
     } else if (warp < kConsumerWarps) {
-      epilogue(p, c, w, wk, tm);
-    } else if ((tid & 31) == 0) {
+      epilogue(p, c, w, wk, tm, 0);
+    } else if (kGroups == 2 && warp > kConsumerWarps) {
+      epilogue(p, c, w, wk, tm, 1);
+    } else if (warp == kConsumerWarps && (tid & 31) == 0) {
       issuer(p, c, w, wk, tm);
       // every MMA issued has completed before TMEM is released
       umma_commit(c.fx(kTcDrain));
