@@ -26,6 +26,12 @@
 //  * Programmatic dependent launch: a kernel lets the next one start at once; the producer
 //    fills the ring with weights, then waits for the previous kernel before any activation
 //    copy (x, y, v).
+//  * Groups with enough rows and weight re-use (a host-set row threshold) go to the tensor
+//    role (sgmv_tc.cuh) on the first CTAs of the grid, whole clusters, in proportion to the
+//    estimated bytes of each side; the other CTAs run the items above.
+//  * Two instantiations per (type, rank, mode): 288 threads, two CTAs per SM (the default
+//    geometry), and 416 threads, one CTA per SM (long batches of few segments; the extra
+//    warps are a second tensor-role epilogue warpgroup and idle in the CUDA-core role).
 //  * Every wait is bounded (globaltimer); a wait that runs out flags the CTA, sets the
 //    library's device error word and lets the kernel run to its end without touching global
 //    memory again.

@@ -9,26 +9,30 @@
 // computed with tcgen05.mma (fp16 / bf16 operands, fp32 accumulation in tensor memory).
 //
 // Work: a group is cut into m-tiles of 128 rows (the MMA's M, one TMEM lane per row; rows of
-// a group come from all of its segments, in segment order, gathered row by row).  The
-// sequence of (m-tile, 64-column n-tile) pairs, m-tile major, is split into equal contiguous
-// ranges, one per tensor CTA.  For every m-tile its range touches, a CTA computes the whole
-// shrink into TMEM, keeps v on chip, and runs the expand for its n-tiles.
+// a group come from all of its segments, in segment order, gathered row by row).  The unit of
+// work is a cluster of 4 CTAs (fused and shrink-only forms) or a CTA (expand-only).  With fewer
+// m-tiles than units, every m-tile gets its own units, which split its 64-column n-tiles;
+// otherwise the (m-tile, n-tile) sequence is cut into equal contiguous ranges.  Within a
+// cluster the shrink is split over K: member m multiplies a quarter of h_in, and the partial
+// v rows are reduced over distributed shared memory (st.async), each member owning 32 rows.
 //
-// Roles inside the CTA (288 threads):
+// Roles inside the CTA (288 threads; 416 in the long-batch instantiation):
 //   warps 0-3  loaders: fill a ring of 24 KB slots -- x and y rows by TMA (one 128-row box
 //              when the tile's rows are consecutive tokens, else boxes of 8 consecutive rows),
-//              every other row and
-//              the weights by 16-byte cp.async (each thread's copies complete the slot's barrier
-//              by themselves) -- in the order the
-//              MMA consumes them: per m-tile, ceil(h_in/64) shrink slots {x rows [128 x 64]
-//              (K-major, 128-byte swizzle), A rows [64 x r] (MN-major, 128-byte swizzle)},
-//              then per n-tile one expand slot {B rows [r x 64] (MN-major, 128-byte swizzle),
-//              y rows [128 x 64] (swizzled for conflict-free row reads)}.
+//              every other row and the weights by 16-byte cp.async (each thread's copies
+//              complete the slot's barrier by themselves) -- in the order the MMA consumes
+//              them: per m-tile, this CTA's shrink slots {x rows [128 x 64] (K-major, 128-byte
+//              swizzle), A rows [64 x r] (MN-major, 128-byte swizzle)}, then per n-tile one
+//              expand slot {B rows [r x 64] (MN-major, 128-byte swizzle), y rows [128 x 64]
+//              (swizzled for conflict-free row reads)}.
 //   warp 8     lane 0 issues the MMAs; the warp owns the TMEM allocation.
-//   warps 4-7  epilogue: v (fp32, TMEM) -> scale -> split into a 16-bit high part and a
-//              16-bit low part (v' = hi + lo to ~16 mantissa bits) -> TMEM, the A operand of
-//              the expand MMAs (D = hi . B + lo . B); then per n-tile y += D, written back in
-//              place in the slot and stored with coalesced 16-byte stores.
+//   warps 4-7  epilogue: v (fp32, TMEM) -> cluster reduction -> scale -> split into a 16-bit
+//              high part and a 16-bit low part (v' = hi + lo to ~16 mantissa bits) -> TMEM,
+//              the A operand of the expand MMAs (D = hi . B + lo . B); then per n-tile
+//              y += D, written back in place in the slot and stored by TMA (8-row boxes of
+//              consecutive tokens; other rows by 16-byte stores).
+//   warps 9-12 (long-batch instantiation) a second epilogue warpgroup: every other n-tile,
+//              with its own D buffer.
 // TMEM (256 columns): v fp32 [0, 64), hi [64, 96), lo [96, 128), two D buffers [128, 256).
 #pragma once
 
