@@ -134,3 +134,37 @@ def test_python_binding_refuses_cpu_tensors():
         lora_apply(y, y, torch.zeros(1, dtype=torch.int64), torch.zeros(1, dtype=torch.int64),
                    torch.zeros(2, dtype=torch.int32), torch.zeros(1, dtype=torch.int32), 0, 16,
                    1.0)
+
+
+class _FakeMatrix:
+    """Stands in for a CUDA tensor in the binding's shape / stride checks (no device needed)."""
+
+    def __init__(self, shape, stride, is_cuda=True):
+        self.shape, self._stride, self.is_cuda = shape, stride, is_cuda
+
+    def dim(self):
+        return len(self.shape)
+
+    def stride(self, i):
+        return self._stride[i]
+
+
+@pytest.mark.parametrize("shape,stride,ld", [
+    ((5, 64), (64, 1), 64),      # dense
+    ((5, 64), (192, 1), 192),    # the middle third of 3x-wide rows
+    ((1, 64), (999, 1), 64),     # one row: its stride does not matter
+    ((5, 1), (8, 7), 8),         # one column: its column stride does not matter
+])
+def test_binding_row_stride(shape, stride, ld):
+    assert binding._rows(_FakeMatrix(shape, stride), "x") == ld
+
+
+@pytest.mark.parametrize("m", [
+    _FakeMatrix((5, 64), (1, 5)),          # column-major
+    _FakeMatrix((5, 64), (32, 1)),         # rows overlap
+    _FakeMatrix((5, 64, 2), (128, 2, 1)),  # not a matrix
+    _FakeMatrix((5, 64), (64, 1), is_cuda=False),
+])
+def test_binding_rejects_unusable_layouts(m):
+    with pytest.raises(ValueError):
+        binding._rows(m, "x")
