@@ -37,6 +37,8 @@ BAD_ORDER = 1
 BAD_FIRST = 2
 BAD_LAST = 4
 BAD_ADAPTER = 8
+BAD_A_PTR = 16
+BAD_B_PTR = 32
 
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
@@ -112,6 +114,8 @@ class OracleLib:
         lib.oracle_sgmv_expand.restype = ctypes.c_int
         lib.oracle_validate.argtypes = [dp, dp, i32, i32, i32]
         lib.oracle_validate.restype = ctypes.c_int32
+        lib.oracle_validate_pointers.argtypes = [dp, dp, dp, dp, i32, i32]
+        lib.oracle_validate_pointers.restype = ctypes.c_int32
         self.lib = lib
         self.path = lib_path
 
@@ -166,6 +170,27 @@ class OracleLib:
         return int(self.lib.oracle_validate(ss.ctypes.data, sa.ctypes.data, len(sa),
                                             int(num_adapters), int(M)))
 
+    def validate_pointers(self, A_addr, B_addr, seg_starts, seg_adapter, num_adapters) -> int:
+        """OR of BAD_A_PTR / BAD_B_PTR for the weight addresses (integer sequences of
+        num_adapters entries, or None) that the table's non-empty segments use."""
+        ss, sa = _i32(seg_starts), _i32(seg_adapter)
+        if len(ss) != len(sa) + 1:
+            raise ValueError("seg_starts must hold num_segments + 1 offsets")
+        keep = []
+
+        def arr(a):
+            if a is None:
+                return None
+            v = np.ascontiguousarray(np.asarray(a, dtype=np.uint64))
+            if len(v) < num_adapters:
+                raise ValueError("an address array needs num_adapters entries")
+            keep.append(v)
+            return v.ctypes.data
+
+        return int(self.lib.oracle_validate_pointers(arr(A_addr), arr(B_addr), ss.ctypes.data,
+                                                     sa.ctypes.data, len(sa),
+                                                     int(num_adapters)))
+
 
 def _load() -> OracleLib:
     global _lib
@@ -191,10 +216,15 @@ def validate(*args, **kw):
     return _load().validate(*args, **kw)
 
 
+def validate_pointers(*args, **kw):
+    return _load().validate_pointers(*args, **kw)
+
+
 lora_apply.__doc__ = OracleLib.lora_apply.__doc__
 sgmv_shrink.__doc__ = OracleLib.sgmv_shrink.__doc__
 sgmv_expand.__doc__ = OracleLib.sgmv_expand.__doc__
 validate.__doc__ = OracleLib.validate.__doc__
+validate_pointers.__doc__ = OracleLib.validate_pointers.__doc__
 
 
 class PreparedApply:

@@ -41,6 +41,8 @@
 #define ORACLE_BAD_FIRST    2  /* seg_starts[0] < 0                                  */
 #define ORACLE_BAD_LAST     4  /* seg_starts[S] > M                                  */
 #define ORACLE_BAD_ADAPTER  8  /* adapter id >= num_adapters (negative = no adapter) */
+#define ORACLE_BAD_A_PTR   16  /* a used adapter's A pointer is null or not 16-byte aligned */
+#define ORACLE_BAD_B_PTR   32  /* the same for its B pointer                                */
 
 /* v[t][c] = sum_j x[t][j] * A_k[layer][j][c]   for every row t of every segment.
  * "Shrink": the first factor of the equation, x_i A_k (h_in -> r).  v is [M][r]; rows outside
@@ -139,6 +141,26 @@ int32_t oracle_validate(const int32_t *seg_starts, const int32_t *seg_adapter,
     for (int32_t i = 0; i < num_segments; ++i) {
         if (seg_starts[i + 1] < seg_starts[i]) bits |= ORACLE_BAD_ORDER;
         if (seg_adapter[i] >= num_adapters) bits |= ORACLE_BAD_ADAPTER;
+    }
+    return bits;
+}
+
+/* Checks the per-adapter weight addresses that the segment table will dereference ("Punica
+ * Guide: Multi-Tenant LoRA Serving with SGMV", section "Core Innovation 1", figure "SGMV Kernel
+ * Memory Layout & Execution Grid": a pointer array to each adapter's contiguous weights).
+ * A_addr / B_addr hold the addresses as integers (either may be NULL: not checked).  Only
+ * adapters of non-empty segments with 0 <= id < num_adapters are looked at.  Returns an OR of
+ * ORACLE_BAD_A_PTR / ORACLE_BAD_B_PTR (0 = valid). */
+int32_t oracle_validate_pointers(const uint64_t *A_addr, const uint64_t *B_addr,
+                                 const int32_t *seg_starts, const int32_t *seg_adapter,
+                                 int32_t num_segments, int32_t num_adapters)
+{
+    int32_t bits = 0;
+    for (int32_t i = 0; i < num_segments; ++i) {
+        const int32_t k = seg_adapter[i];
+        if (k < 0 || k >= num_adapters || seg_starts[i + 1] <= seg_starts[i]) continue;
+        if (A_addr && (A_addr[k] == 0 || A_addr[k] % 16 != 0)) bits |= ORACLE_BAD_A_PTR;
+        if (B_addr && (B_addr[k] == 0 || B_addr[k] % 16 != 0)) bits |= ORACLE_BAD_B_PTR;
     }
     return bits;
 }

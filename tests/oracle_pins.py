@@ -228,7 +228,28 @@ def check_validate(o):
     assert o.validate([1, 0, 9], [7, 0], 4, 5) == 1 | 4 | 8
 
 
+def check_validate_pointers(o):
+    """The pointer check flags exactly a null or non-16-byte-aligned address of an adapter that
+    a non-empty segment uses, and looks at nothing else."""
+    good = [0x1000, 0x2010, 0x3020, 0x4030]
+    ss, sa = [0, 2, 2, 5], [0, 3, 1]
+    assert o.validate_pointers(good, good, ss, sa, 4) == 0
+    # segment 1 is empty, so adapter 3's pointers are never used
+    assert o.validate_pointers([0x1000, 0x2010, 0x3020, 0], good, ss, sa, 4) == 0
+    assert o.validate_pointers([0x1000, 0, 0x3020, 0x4030], good, ss, sa, 4) == 16   # A[1] null
+    assert o.validate_pointers(good, [0x1000, 0x2018, 0, 0], ss, sa, 4) == 32        # B[1] odd
+    assert o.validate_pointers(good, [0x1008, 0x2010, 0x3020, 0x4031], ss, sa, 4) == 32  # B[0]
+    # adapter 1 sits in an empty segment and adapter 2 in none: their pointers are not used
+    assert o.validate_pointers([0x1000, 0, 0x3001, 0x4030], good, [0, 2, 2, 5], [0, 1, 3], 4) == 0
+    # a negative id carries no adapter; an id past the pool is reported by validate(), not here
+    assert o.validate_pointers([0x1000, 0x2010, 0x3020, 0x4030], good, [0, 1, 2], [-1, 9], 4) == 0
+    assert o.validate_pointers([8, 16], [0, 32], [0, 1, 2], [0, 1], 2) == 16 | 32
+    assert o.validate_pointers(None, [0, 32], [0, 1, 2], [0, 1], 2) == 32       # A not checked
+    assert o.validate_pointers([8, 16], None, [0, 1, 2], [0, 1], 2) == 16       # B not checked
+    assert o.validate_pointers(good, good, [0], [], 4) == 0                      # no segments
+
+
 ALL_CHECKS = [check_hand_example, check_merged_weights, check_per_request_gemv,
               check_single_adapter_dense, check_zero_adapter, check_permutation,
               check_brute_force, check_layer_selection, check_shrink_expand,
-              check_untouched_rows, check_validate]
+              check_untouched_rows, check_validate, check_validate_pointers]

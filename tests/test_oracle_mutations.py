@@ -31,6 +31,11 @@ MUTATIONS = [
     ("validate_order_off_by_one", "if (seg_starts[i + 1] < seg_starts[i])",
      "if (seg_starts[i + 1] <= seg_starts[i])", None),
     ("negative_id_not_skipped", "if (k < 0) continue;", "if (k < 0) k = 0;", None),
+    ("pointer_alignment_8", "A_addr[k] % 16 != 0", "A_addr[k] % 8 != 0", None),
+    ("pointer_check_of_empty_segments", "|| seg_starts[i + 1] <= seg_starts[i]) continue;",
+     ") continue;", None),
+    ("pointer_check_b_alignment_dropped", "B_addr[k] == 0 || B_addr[k] % 16 != 0",
+     "B_addr[k] == 0", None),
 ]
 
 
