@@ -41,10 +41,14 @@
  *   the device, which sets the kernels' attributes).  Calls on one stream are ordered; calls
  *   on different streams that write the same rows race.
  * Errors.  Host-checkable violations return a negative status and enqueue nothing.  Defects
- *   that only the device can see (decreasing offsets, an adapter id past the pool) are not
- *   checked on the fast path: run sgmv_validate() on untrusted tables.  Every device-side wait
- *   is bounded; a wait that runs out sets the library's device error word, which
- *   sgmv_get_error() reads (SGMV_ETIMEOUT), and the kernel returns without hanging.
+ *   that only the device can see are not checked on the fast path and are undefined behaviour
+ *   there (typically a memory fault): decreasing offsets and adapter ids past the pool (run
+ *   sgmv_validate() on untrusted tables), a null or misaligned A_ptrs[k] / B_ptrs[k] of an
+ *   adapter the table uses (sgmv_validate_pointers()), and a layer_idx at or past the number
+ *   of layers L of the adapter blocks (the library is never told L; the caller checks it).
+ *   Every device-side wait is bounded; a wait that runs out sets the library's device error
+ *   word, which sgmv_get_error() reads (SGMV_ETIMEOUT), and the kernel returns without
+ *   hanging.
  */
 #ifndef SGMV_GB300_H
 #define SGMV_GB300_H
@@ -93,7 +97,8 @@ typedef enum {
  *   seg_adapter  in      [num_segments] int32 (negative: no adapter; may be null when
  *                        num_segments == 0)
  *   num_segments         0 <= num_segments <= SGMV_MAX_SEGMENTS (0: returns SGMV_OK, no-op)
- *   layer_idx            >= 0, selects the layer inside each adapter block
+ *   layer_idx            0 <= layer_idx < L (the layer count of every adapter block the
+ *                        table uses; only the sign is checked), selects the layer
  *   h_in, h_out          multiples of 8, <= SGMV_MAX_HIDDEN
  *   r                    8, 16, 32 or 64
  *   scale                alpha / r, applied in fp32 to the intermediate before the expand
@@ -252,6 +257,29 @@ int sgmv_expand_strided(void *y, int32_t ldy, const float *v, const void *const 
  */
 int sgmv_validate(const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,
                   int32_t num_adapters, int32_t M, int32_t *d_err, sgmv_stream_t stream);
+
+/*
+ * sgmv_validate_pointers -- checks, on the device, the weight pointers of every adapter that a
+ * non-empty segment of the table uses, and writes an OR of these bits to *d_err (device int32,
+ * overwritten; 0 = valid):
+ *   16  A_ptrs[k] is null or not 16-byte aligned     32  the same for B_ptrs[k]
+ * Only the pointer values are read, never the memory they point to, so a bad table cannot
+ * fault here.  Adapter ids < 0 (no adapter) or >= num_adapters (reported by sgmv_validate,
+ * bit 8) are skipped.  Either pointer array may be null (not checked: a shrink-only or
+ * expand-only caller), not both.  The pages' pointer arrays (section "Core Innovation 1",
+ * figure "SGMV Kernel Memory Layout & Execution Grid") carry no such check; this is the
+ * debugging counterpart of the fast path, which dereferences them unchecked.
+ *   A_ptrs, B_ptrs           in   device arrays of num_adapters device pointers (or null)
+ *   seg_starts, seg_adapter  in   device table as for lora_apply
+ *   num_segments, num_adapters    >= 0
+ *   d_err                    out  device int32
+ * Returns SGMV_OK, SGMV_EINVAL (null table, both arrays null, negative sizes), SGMV_EALIGN (a
+ * pointer array not 8-byte aligned) or SGMV_ECUDA.
+ */
+int sgmv_validate_pointers(const void *const *A_ptrs, const void *const *B_ptrs,
+                           const int32_t *seg_starts, const int32_t *seg_adapter,
+                           int32_t num_segments, int32_t num_adapters, int32_t *d_err,
+                           sgmv_stream_t stream);
 
 /*
  * sgmv_get_error -- synchronises `stream`, copies the current device's library error word to

@@ -26,8 +26,8 @@ SGMV_LONG_BATCH = 8
 SGMV_MAX_LD = 1 << 24
 SYMBOLS = ("lora_apply", "lora_apply_ex", "lora_apply_strided", "sgmv_shrink", "sgmv_shrink_ex",
            "sgmv_shrink_strided", "sgmv_expand", "sgmv_expand_ex", "sgmv_expand_strided",
-           "sgmv_validate", "sgmv_get_error", "sgmv_set_wait_limit", "sgmv_status_string",
-           "sgmv_version")
+           "sgmv_validate", "sgmv_validate_pointers", "sgmv_get_error", "sgmv_set_wait_limit",
+           "sgmv_status_string", "sgmv_version")
 
 
 class SgmvError(RuntimeError):
@@ -67,6 +67,7 @@ def lib(build_if_stale: bool = True) -> ctypes.CDLL:
         L.sgmv_expand_strided.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, f32,
                                           ctypes.c_int, ctypes.c_uint32, vp]
         L.sgmv_validate.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+        L.sgmv_validate_pointers.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp]
         L.sgmv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
         L.sgmv_set_wait_limit.argtypes = [ctypes.c_uint64, i32]
         L.sgmv_status_string.argtypes = [ctypes.c_int]
@@ -114,6 +115,17 @@ def _stream(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _on(t, *others):
+    """The library plans a launch for the CURRENT device: make the tensors' device current
+    (every tensor of the call must live on it)."""
+    import torch
+    for o in others:
+        if o is not None and o.device != t.device:
+            raise ValueError(f"all tensors of a call must be on one device ({t.device}, not "
+                             f"{o.device})")
+    return torch.cuda.device(t.device)
 
 
 def _table(seg_starts, seg_adapter):
@@ -167,6 +179,13 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
         raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
     S = _table(seg_starts, seg_adapter)
     flags = _flags(overlap_prior, tensor_cores, long_batch)
+    with _on(x, y, A_ptrs, B_ptrs, seg_starts, seg_adapter):
+        return _lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale,
+                           stream, flags, ldx, ldy, S)
+
+
+def _lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream,
+                flags, ldx, ldy, S):
     if ldx != x.shape[1] or ldy != y.shape[1]:  # column slices of wider activations
         rc = lib().lora_apply_strided(
             y.data_ptr(), ldy, x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
@@ -187,16 +206,22 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
 
 
 def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None,
-                tensor_cores="auto", long_batch=False):
-    """v[t] = x[t] A_k (fp32) for every segment row (tensor_cores, long_batch as for
-    lora_apply)."""
+                tensor_cores="auto", long_batch=False, overlap_prior=False):
+    """v[t] = x[t] A_k (fp32) for every segment row (tensor_cores, long_batch, overlap_prior as
+    for lora_apply)."""
     import torch
     _cuda(v, "v")
     ldx = _rows(x, "x")
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != x.shape[0]:
         raise ValueError("v must be float32 [M, r]")
     S = _table(seg_starts, seg_adapter)
-    flags = _flags(False, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    with _on(x, v, A_ptrs, seg_starts, seg_adapter):
+        return _sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream, flags,
+                            ldx, S)
+
+
+def _sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream, flags, ldx, S):
     if ldx != x.shape[1]:
         _check(lib().sgmv_shrink_strided(
             v.data_ptr(), x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"), seg_starts.data_ptr(),
@@ -213,16 +238,23 @@ def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None
 
 
 def sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None,
-                tensor_cores="auto", long_batch=False):
-    """y[t] += scale * v[t] B_k for every segment row (in place on y; tensor_cores, long_batch
-    as for lora_apply)."""
+                tensor_cores="auto", long_batch=False, overlap_prior=False):
+    """y[t] += scale * v[t] B_k for every segment row (in place on y; tensor_cores, long_batch,
+    overlap_prior as for lora_apply)."""
     import torch
     _cuda(v, "v")
     ldy = _rows(y, "y")
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != y.shape[0]:
         raise ValueError("v must be float32 [M, r]")
     S = _table(seg_starts, seg_adapter)
-    flags = _flags(False, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    with _on(y, v, B_ptrs, seg_starts, seg_adapter):
+        return _sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream,
+                            flags, ldy, S)
+
+
+def _sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream, flags, ldy,
+                 S):
     if ldy != y.shape[1]:
         _check(lib().sgmv_expand_strided(
             y.data_ptr(), ldy, v.data_ptr(), _ptrs(B_ptrs, "B_ptrs"), seg_starts.data_ptr(),
@@ -246,9 +278,35 @@ def sgmv_validate(seg_starts, seg_adapter, num_adapters, M, d_err, stream=None):
     _cuda(d_err, "d_err")
     if d_err.dtype != torch.int32 or d_err.numel() < 1:
         raise TypeError("d_err must be a device int32 tensor")
-    rc = lib().sgmv_validate(seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(num_adapters),
-                             int(M), d_err.data_ptr(), _stream(stream, seg_starts.device))
+    with _on(seg_starts, seg_adapter, d_err):
+        rc = lib().sgmv_validate(seg_starts.data_ptr(), seg_adapter.data_ptr(), S,
+                                 int(num_adapters), int(M), d_err.data_ptr(),
+                                 _stream(stream, seg_starts.device))
     _check(rc, "sgmv_validate")
+    return d_err
+
+
+def sgmv_validate_pointers(A_ptrs, B_ptrs, seg_starts, seg_adapter, d_err, stream=None):
+    """Writes the pointer-check bits (16: a used A pointer is null or misaligned, 32: the same
+    for B) into the device int32 tensor d_err.  A_ptrs / B_ptrs: int64 device tensors of
+    addresses (one may be None); reads pointer values only (see include/sgmv.h)."""
+    import torch
+    S = _table(seg_starts, seg_adapter)
+    _cuda(d_err, "d_err")
+    if d_err.dtype != torch.int32 or d_err.numel() < 1:
+        raise TypeError("d_err must be a device int32 tensor")
+    tabs = [t for t in (A_ptrs, B_ptrs) if t is not None]
+    if not tabs:
+        raise ValueError("A_ptrs and B_ptrs cannot both be None")
+    n = tabs[0].numel()
+    if any(t.numel() != n for t in tabs):
+        raise ValueError("A_ptrs and B_ptrs must have one entry per adapter")
+    a = _ptrs(A_ptrs, "A_ptrs") if A_ptrs is not None else None
+    b = _ptrs(B_ptrs, "B_ptrs") if B_ptrs is not None else None
+    with _on(seg_starts, seg_adapter, d_err, A_ptrs, B_ptrs):
+        rc = lib().sgmv_validate_pointers(a, b, seg_starts.data_ptr(), seg_adapter.data_ptr(), S,
+                                          n, d_err.data_ptr(), _stream(stream, seg_starts.device))
+    _check(rc, "sgmv_validate_pointers")
     return d_err
 
 

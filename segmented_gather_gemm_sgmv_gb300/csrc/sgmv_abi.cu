@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -35,54 +36,36 @@ struct KernelCache {  // per kernel instantiation
 };
 
 struct DeviceState {
-  bool init = false;
+  std::once_flag once;
+  int init_rc = SGMV_ECUDA;  // written once, under `once`
   int sms = 0;
   int* err = nullptr;
-  uint64_t wait_ns = kDefaultWaitNs;
-  int inject = 0;
-  KernelCache cache[3][3][4][2];  // dtype, mode, rank index, geometry (SGMV_LONG_BATCH)
+  std::atomic<uint64_t> wait_ns{kDefaultWaitNs};
+  std::atomic<int> inject{0};
+  KernelCache cache[3][3][4][2];  // dtype, mode, rank index, geometry (SGMV_LONG_BATCH); g_mu
 };
 
-std::mutex g_mu;
+std::mutex g_mu;  // guards the kernel caches
 DeviceState g_dev[kMaxDevices];
 
 constexpr int kMaxStages = 16;
 
-struct Tuning {
-  int stages = 0;     // 0: as many as shared memory holds
-  int stage_kb = 0;   // ring stage size in KB; 0: by rank (stage_kb_for)
-  int budget_kb = 0;  // 0: 112 KB (two CTAs per SM), else the per-CTA shared-memory budget
-  int tc_min_rows = 64;  // adapter groups of at least half a 128-row tile use the tensor
-                         // cores (measured: 64 beats 128 on the 70B mix, 16 and 32 tie)...
-  int xchg_kb = 64;      // cost of one partial-sum exchange in streamed KB (group size rule)
-  int tc_min_mb = 32;    // ...and whose CUDA-core items would re-read at least this many MB of
-                         // weights (ceil(rows / 4) items x the adapter's A and B)
-  int wide_threads = 1;  // SGMV_LONG_BATCH launches use the 416-thread kernel (0: 288 threads)
-};
+// Launch-geometry and routing constants (chosen by measurement on GB300; fixed at build time).
+// Adapter groups of at least half a 128-row tile may use the tensor cores (measured: 64 beats
+// 128 on the 70B mix, 16 and 32 tie) ...
+constexpr int kTcMinRows = 64;
+// ... when their CUDA-core items would re-read at least this many MB of weights (ceil(rows / 4)
+// items x the adapter's A and B bytes).
+constexpr int kTcMinMB = 32;
+// Cost of one partial-sum exchange through distributed shared memory, in streamed KB (the
+// group-size rule of the CUDA-core role).
+constexpr int kXchgKB = 64;
 
-Tuning read_tuning() {
-  Tuning t;
-  if (const char* s = std::getenv("SGMV_SMEM_KB")) t.budget_kb = std::max(0, std::atoi(s));
-  if (const char* s = std::getenv("SGMV_STAGES")) t.stages = std::max(0, std::atoi(s));
-  if (const char* s = std::getenv("SGMV_STAGE_KB")) t.stage_kb = std::max(4, std::atoi(s));
-  if (const char* s = std::getenv("SGMV_TC_MIN_ROWS")) t.tc_min_rows = std::max(16, std::atoi(s));
-  if (const char* s = std::getenv("SGMV_TC_MIN_MB")) t.tc_min_mb = std::max(0, std::atoi(s));
-  if (const char* s = std::getenv("SGMV_XCHG_KB")) t.xchg_kb = std::max(0, std::atoi(s));
-  if (const char* s = std::getenv("SGMV_WIDE_THREADS")) t.wide_threads = std::atoi(s) != 0;
-  return t;
-}
-const Tuning& tuning() {
-  static const Tuning t = read_tuning();
-  return t;
-}
 // Ring stage size.  Rank 16: 20 KB, i.e. an A chunk of 512 rows plus its x columns for four
 // rows, with five stages in the ring (24 KB stages hold the same 512-row chunks, four at a
 // time: measured 5.8 vs 6.4 us per chained decode call).  Larger ranks: 24 KB (measured on the
 // 70B mix, rank 64: 136 vs 138 us).
-int stage_kb_for(int r, const Tuning& tu) {
-  if (tu.stage_kb > 0) return tu.stage_kb;
-  return r <= 16 ? 20 : 24;
-}
+int stage_kb_for(int r) { return r <= 16 ? 20 : 24; }
 
 int rank_index(int r) {
   switch (r) {
@@ -138,18 +121,20 @@ bool encode_rows(sgmv::TmaMap* out, const void* base, int cols, int ld, int dtyp
 }
 size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Per-device state of the current device, set up once (thread-safe) on first use.
 int device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SGMV_ECUDA;
   DeviceState& st = g_dev[dev];
-  if (!st.init) {
-    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return SGMV_ECUDA;
+  std::call_once(st.once, [&st, dev] {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_sgmv_error) != cudaSuccess) return SGMV_ECUDA;
-    st.err = static_cast<int*>(p);
-    st.init = true;
-  }
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaGetSymbolAddress(&p, g_sgmv_error) == cudaSuccess) {
+      st.err = static_cast<int*>(p);
+      st.init_rc = SGMV_OK;
+    }
+  });
+  if (st.init_rc != SGMV_OK) return st.init_rc;
   *out = &st;
   return SGMV_OK;
 }
@@ -217,12 +202,11 @@ sgmv::MemberPlan member_plan(const Problem& pb, int E, int m, int kb, int wmax, 
 // Lays out shared memory and fills the geometry part of the kernel parameters.  The launch
 // cluster is kMaxGroup CTAs; the kernel itself picks how many of them share an item.
 int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* smem_out) {
-  const Tuning& tu = tuning();
   const int eb = pb.dtype == SGMV_F32 ? 4 : 2;
   const int vec = 16 / eb;
   const int C = sgmv::kMaxGroup;
   const int rmax = sgmv::kRowsMax;
-  const int stage_bytes = stage_kb_for(pb.r, tu) * 1024;
+  const int stage_bytes = stage_kb_for(pb.r) * 1024;
   // A rows per stage, followed by the same rows' columns of up to rmax x rows.
   const int kb = (stage_bytes / ((pb.r + rmax) * eb)) / 8 * 8;
   // Expand pass width: one thread per 16 bytes of a B row, and rmax y rows must fit a stage.
@@ -264,14 +248,13 @@ int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* sme
   if (p.off_ring + std::max<size_t>(scratch, 2 * static_cast<size_t>(stage_bytes)) > budget)
     return SGMV_EUNSUPPORTED;
   int nst = static_cast<int>((budget - p.off_ring) / stage_bytes);
-  nst = std::min(nst, tu.stages > 0 ? tu.stages : kMaxStages);
   nst = std::min(std::max(nst, 2), kMaxStages);
   const size_t ring = std::max<size_t>(static_cast<size_t>(nst) * stage_bytes, scratch);
   off = p.off_ring + ring;
   if (off > budget) return SGMV_EUNSUPPORTED;
 
   p.C = C;
-  p.xchg_bytes = tu.xchg_kb * 1024;
+  p.xchg_bytes = kXchgKB * 1024;
   p.nstages = nst;
   p.stage_bytes = stage_bytes;
   p.kb = kb;
@@ -286,11 +269,7 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   if (rc != SGMV_OK) return rc;
   size_t smem = 0;
   const bool wide = (flags & SGMV_LONG_BATCH) != 0;
-  const size_t base_smem = wide ? kMaxSmem : kPairSmem;
-  const size_t budget =
-      tuning().budget_kb > 0
-          ? std::min<size_t>(kMaxSmem, static_cast<size_t>(tuning().budget_kb) * 1024)
-          : base_smem;
+  const size_t budget = wide ? kMaxSmem : kPairSmem;
   rc = plan_geometry(pb, budget, p, &smem);
   if (rc == SGMV_EUNSUPPORTED) rc = plan_geometry(pb, kMaxSmem, p, &smem);
   if (rc != SGMV_OK) return rc;
@@ -300,14 +279,14 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   p.h_in = pb.h_in;
   p.h_out = pb.h_out;
   p.scale = pb.scale;
-  p.wait_limit_ns = st->wait_ns;
-  p.inject_stall = st->inject;
+  p.wait_limit_ns = st->wait_ns.load(std::memory_order_relaxed);
+  p.inject_stall = st->inject.load(std::memory_order_relaxed);
 
   // The 416-thread kernel (a second tensor-role epilogue warpgroup) measured faster where the
   // tensor role dominates (prefill_mixed, 8 segments: 61.1 -> 58.3 us) and slower on the
   // CUDA-core role (the 70B mix, 482 segments: 101.0 -> 105.6 us); a table of many segments
   // means many decode rows, so those keep the 288-thread kernel.
-  const bool wide_kernel = wide && tuning().wide_threads && pb.S <= kWideMaxSegments;
+  const bool wide_kernel = wide && pb.S <= kWideMaxSegments;
   const void* fn = kernel_for(pb.dtype, pb.mode, pb.r, wide_kernel);
   const int threads = wide_kernel ? sgmv::kThreadsWide : sgmv::kThreads;
   if (!fn) return SGMV_EUNSUPPORTED;
@@ -370,8 +349,12 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   p.tc_base = tc_base;
   const size_t xchg = pb.mode != sgmv::kExpand ? sgmv::kTcXchgBytes : 0;  // split-K buffers
   if (tc_capable && grid >= 2 * p.C && smem > tc_base + xchg) {
-    const int slots = std::min<int>(static_cast<int>((smem - tc_base - xchg) / sgmv::kTcSlot),
-                                    (2 * kMaxStages + sgmv::kNumFixedBars - sgmv::kTcNumFixed) / 2);
+    int slots = std::min<int>(static_cast<int>((smem - tc_base - xchg) / sgmv::kTcSlot),
+                              (2 * kMaxStages + sgmv::kNumFixedBars - sgmv::kTcNumFixed) / 2);
+    // Two epilogue groups take alternate n-tiles: with an even slot count the previous use of
+    // every slot within an m-tile belongs to the same group, so no group can wait on a slot
+    // whose previous fill (another group's) has not landed yet (parity waits see one phase).
+    if (wide_kernel) slots &= ~1;
     p.tc_xchg = tc_base + static_cast<uint32_t>(slots) * sgmv::kTcSlot;
     if (slots >= 3) {
       const bool need_x = pb.mode != sgmv::kExpand, need_y = pb.mode != sgmv::kShrink;
@@ -394,11 +377,11 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
       const double w = static_cast<double>(pb.r) * 2.0 *
                        ((pb.mode != sgmv::kExpand ? pb.h_in : 0) +
                         (pb.mode != sgmv::kShrink ? pb.h_out : 0));
-      const double items = std::ceil(tuning().tc_min_mb * 1048576.0 / w);
+      const double items = std::ceil(kTcMinMB * 1048576.0 / w);
       p.tc_min_rows = (flags & SGMV_TENSOR_CORES_ALWAYS)
                           ? 64
                           : static_cast<int>(std::min(
-                                1e9, std::max<double>(tuning().tc_min_rows, 4.0 * items)));
+                                1e9, std::max<double>(kTcMinRows, 4.0 * items)));
       p.tc_slots = slots;
     }
   }
@@ -477,6 +460,27 @@ __global__ void validate_kernel(const int32_t* ss, const int32_t* sa, int S, int
   if (i < S) {
     if (ss[i + 1] < ss[i]) bits |= 1;
     if (sa[i] >= num_adapters) bits |= 8;
+  }
+  if (bits) atomicOr(err, bits);
+}
+
+// Checks the weight pointers of every adapter a non-empty segment uses; see
+// sgmv_validate_pointers in include/sgmv.h.  Reads pointer values only, never what they point to.
+__global__ void validate_ptrs_kernel(const void* const* A_ptrs, const void* const* B_ptrs,
+                                     const int32_t* ss, const int32_t* sa, int S,
+                                     int num_adapters, int32_t* err) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= S) return;
+  const int k = sa[i];
+  if (k < 0 || k >= num_adapters || ss[i + 1] <= ss[i]) return;
+  int bits = 0;
+  if (A_ptrs) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(A_ptrs[k]);
+    if (a == 0 || (a & 15u)) bits |= 16;
+  }
+  if (B_ptrs) {
+    const uintptr_t b = reinterpret_cast<uintptr_t>(B_ptrs[k]);
+    if (b == 0 || (b & 15u)) bits |= 32;
   }
   if (bits) atomicOr(err, bits);
 }
@@ -623,6 +627,25 @@ int sgmv_validate(const int32_t* seg_starts, const int32_t* seg_adapter, int32_t
   return cudaGetLastError() == cudaSuccess ? SGMV_OK : SGMV_ECUDA;
 }
 
+int sgmv_validate_pointers(const void* const* A_ptrs, const void* const* B_ptrs,
+                           const int32_t* seg_starts, const int32_t* seg_adapter,
+                           int32_t num_segments, int32_t num_adapters, int32_t* d_err,
+                           sgmv_stream_t stream) {
+  if (num_segments < 0 || num_adapters < 0 || !seg_starts || !d_err ||
+      (num_segments > 0 && !seg_adapter) || (!A_ptrs && !B_ptrs))
+    return SGMV_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(A_ptrs) & 7u) || (reinterpret_cast<uintptr_t>(B_ptrs) & 7u))
+    return SGMV_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(d_err, 0, sizeof(int32_t), s) != cudaSuccess) return SGMV_ECUDA;
+  if (num_segments == 0) return SGMV_OK;
+  const int threads = 256;
+  const int blocks = (num_segments + threads - 1) / threads;
+  validate_ptrs_kernel<<<blocks, threads, 0, s>>>(A_ptrs, B_ptrs, seg_starts, seg_adapter,
+                                                  num_segments, num_adapters, d_err);
+  return cudaGetLastError() == cudaSuccess ? SGMV_OK : SGMV_ECUDA;
+}
+
 int sgmv_get_error(int32_t* host_err, int32_t clear, sgmv_stream_t stream) {
   if (!host_err) return SGMV_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -646,8 +669,8 @@ int sgmv_set_wait_limit(uint64_t limit_ns, int32_t inject_stall) {
   DeviceState* st = nullptr;
   const int rc = device_state(&st);
   if (rc != SGMV_OK) return rc;
-  st->wait_ns = limit_ns ? limit_ns : kDefaultWaitNs;
-  st->inject = inject_stall ? 1 : 0;
+  st->wait_ns.store(limit_ns ? limit_ns : kDefaultWaitNs, std::memory_order_relaxed);
+  st->inject.store(inject_stall ? 1 : 0, std::memory_order_relaxed);
   return SGMV_OK;
 }
 

@@ -273,7 +273,44 @@ struct Waiter {
     }
   }
   __device__ __forceinline__ bool ok() const { return *abort == 0; }
+
+  // Bounded wait until the shared counter *f reaches `target` (a monotonic counter cannot alias
+  // the way an mbarrier parity can).  All threads that call it see the same result only if
+  // the caller makes them agree (e.g. __all_sync).
+  __device__ __forceinline__ bool until(const volatile int* f, int target) const {
+    if (*f >= target) return true;
+    const uint64_t t0 = now_ns();
+    while (true) {
+      if (*f >= target) return true;
+      if (*abort) return false;
+      if (now_ns() - t0 > limit) {
+        *abort = 1;
+        atomicExch(err, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+
+  // After the CTA gave up: waits (bounded, ignoring the abort flag) until the phase of `bar`
+  // with this parity has completed, i.e. until the asynchronous copies counted on it have
+  // landed in this CTA's shared memory.  Returns false when the bound ran out (copies whose
+  // bytes were announced but never issued).
+  template <bool kCluster>
+  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+    const uint64_t t0 = now_ns();
+    while (!(kCluster ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)))
+      if (now_ns() - t0 > limit) return false;
+    return true;
+  }
 };
+
+// Shared-memory control words (ints at off_ctl): [0] abort flag, [1] TMEM address (tensor
+// role), [2..3] tensor_ctas sums, [4..23] scan scratch, and the drain records below.
+constexpr int kCtlIssued = 26;   // ring slots the producer ever filled (bit mask)
+constexpr int kCtlParity = 27;   // phase parity of each slot's last fill (bit mask)
+constexpr int kCtlPending = 28;  // 1 + parity of an armed exchange barrier not yet seen complete
+constexpr int kCtlPendBar = 29;  // which exchange barrier
+constexpr int kCtlTileGo = 30;   // tensor role: last m-tile whose shrink slots are all consumed
 
 // ---- stage layout ---------------------------------------------------------------------
 // The stages of one item, in ring order: [A chunks][pass 0: B chunks, y][pass 1: ...] (fused);
@@ -639,7 +676,8 @@ struct Kernel {
 
   // One stage into the current ring slot: wait for the slot (after the first round), announce
   // its bytes (weights and activations), copy the weights, and the activations when `acts`.
-  __device__ __forceinline__ static void issue_stage(const Params& p, const Smem& sm,
+  // Returns whether the stage's bytes were announced (false once the CTA has given up).
+  __device__ __forceinline__ static bool issue_stage(const Params& p, const Smem& sm,
                                                      const Waiter& w, int4 e, const RingPos& rp,
                                                      const T* Ak, const T* Bk, const int* d,
                                                      int nrow, bool acts, uint64_t pol_w,
@@ -664,22 +702,26 @@ struct Kernel {
         bulk_g2s(sm.stage_u32(s), Ak + static_cast<size_t>(e.y) * R,
                  static_cast<uint32_t>(rows * R * kEb), sm.full(s), pol_w);
     }
-    __syncwarp();
-    const bool ok = w.ok();
+    // every lane follows lane 0's decision, so that the bytes announced are the bytes copied
+    const bool ok = __shfl_sync(0xffffffffu, w.ok() ? 1 : 0, 0) != 0;
     if (kind == kChunkB && ok)
       for (int rr = lane; rr < rows; rr += 32)  // up to R (64) rows
         bulk_g2s(sm.stage_u32(s) + static_cast<uint32_t>(rr * b_row_stride(e.w, kEb)),
                  Bk + static_cast<size_t>(e.y + rr) * p.h_out + e.z,
                  static_cast<uint32_t>(e.w * kEb), sm.full(s), pol_w);
     if (acts) issue_acts(p, sm, ok, e, s, d, nrow, pol_a);
+    return ok;
   }
 
   __device__ __forceinline__ static void producer(const Params& p, const Smem& sm,
                                                   const Waiter& w, const Group& grp,
                                                   const MemberPlan& mp, const int* starts,
                                                   const int* adapters, const int* base,
-                                                  const int* gcnt, int4* tab, int n_my) {
+                                                  const int* gcnt, int4* tab, int n_my,
+                                                  int* ctl) {
     const int lane = threadIdx.x & 31;
+    uint32_t issued = 0, parity = 0;  // ring slots filled, parity of each one's last fill
+    uint32_t pre_ok = 0;  // stages issued before the wait on the previous kernel, bytes announced
     const uint64_t pol_w = policy_evict_first();  // weights: streamed once per call
     const uint64_t pol_a = policy_evict_last();   // activations: reused by the group
     const int NST = sm.nst;
@@ -710,19 +752,29 @@ struct Kernel {
           // the stages already issued (item 0 started at slot 0).
           pdl_wait_prior();
           prior_done = true;
-          const bool ok = w.ok();
-          for (int q = 0; q < t; ++q) issue_acts(p, sm, ok, tab[q], q, d, nrow, pol_a);
+          // the activation bytes of a stage were announced with its weights (or none were):
+          // copy exactly what was announced, so that every phase completes
+          for (int q = 0; q < t; ++q)
+            issue_acts(p, sm, (pre_ok >> q) & 1u, tab[q], q, d, nrow, pol_a);
         }
-        issue_stage(p, sm, w, tab[t], rp, Ak, Bk, d, nrow, prior_done, pol_w, pol_a);
+        const bool sok = issue_stage(p, sm, w, tab[t], rp, Ak, Bk, d, nrow, prior_done, pol_w,
+                                     pol_a);
+        if (!prior_done && sok) pre_ok |= 1u << t;
+        issued |= 1u << rp.s;
+        parity = (parity & ~(1u << rp.s)) | (rp.par << rp.s);
       }
       if (!prior_done) {
         pdl_wait_prior();
         prior_done = true;
-        const bool ok = w.ok();
-        for (int q = 0; q < total; ++q) issue_acts(p, sm, ok, tab[q], q, d, nrow, pol_a);
+        for (int q = 0; q < total; ++q)
+          issue_acts(p, sm, (pre_ok >> q) & 1u, tab[q], q, d, nrow, pol_a);
       }
     }
     if (!prior_done) pdl_wait_prior();
+    if (lane == 0) {  // for the drain of a CTA that gives up
+      ctl[kCtlIssued] = static_cast<int>(issued);
+      ctl[kCtlParity] = static_cast<int>(parity);
+    }
   }
 
   // --------------------------------------------------------------- consumer warps ----
@@ -730,7 +782,8 @@ struct Kernel {
   __device__ __forceinline__ static void consume_item(const Params& p, const Smem& sm,
                                                       const Waiter& w, const Group& grp,
                                                       const MemberPlan& mp, int li, bool last,
-                                                      RingPos& rp, const int* d, int nrow) {
+                                                      RingPos& rp, const int* d, int nrow,
+                                                      int* ctl) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NST = sm.nst;
     float acc[RB][kVec];
@@ -865,7 +918,11 @@ struct Kernel {
             st_async_f32(cluster_map(my_slot + 4u * t, grp.rank0 + j), s,
                          cluster_map(vready, grp.rank0 + j));
         }
-        w.wait<true>(vready, (li >> 1) & 1);
+        const bool got = w.wait<true>(vready, (li >> 1) & 1);
+        if (tid == 0 && !got) {  // peers' pushes may still land: drained before exit
+          ctl[kCtlPending] = 1 + ((li >> 1) & 1);
+          ctl[kCtlPendBar] = kVReady0 + (li & 1);
+        }
         for (int t = tid; t < nrow * R; t += kConsumers) {
           float s = 0.f;
           for (int j = 0; j < grp.size; ++j) s += sm.vpart(li & 1, j)[t];
@@ -970,7 +1027,7 @@ struct Kernel {
 
   __device__ __forceinline__ static void consumer(const Params& p, const Smem& sm,
                                                   const Waiter& w, const Group& grp,
-                                                  const MemberPlan& mp, int n_my) {
+                                                  const MemberPlan& mp, int n_my, int* ctl) {
     RingPos rp;
     rp.init();
     for (int li = 0; li < n_my; ++li) {
@@ -979,11 +1036,11 @@ struct Kernel {
       const int nrow = min(max(d[1], 0), kRowsMax);
       const bool last = li == n_my - 1;
       if (nrow <= 1)
-        consume_item<1>(p, sm, w, grp, mp, li, last, rp, d, nrow);
+        consume_item<1>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
       else if (nrow <= 2)
-        consume_item<2>(p, sm, w, grp, mp, li, last, rp, d, nrow);
+        consume_item<2>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
       else
-        consume_item<kRowsMax>(p, sm, w, grp, mp, li, last, rp, d, nrow);
+        consume_item<kRowsMax>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
     }
     // keep every thread's cluster barrier sequence: wait #1, arrive #2 (done per item above
     // when the group exchanges partial products)
@@ -1051,6 +1108,7 @@ struct Kernel {
 
     if (tid == 0) {  // CUDA-core role barriers (a tensor-role CTA invalidates them again)
       ctl[0] = 0;
+      for (int i = kCtlIssued; i <= kCtlPendBar; ++i) ctl[i] = 0;
       for (int s = 0; s < p.nstages; ++s) {
         mbar_init(sm.full(s), 1);
         mbar_init(sm.empty(s), kConsumerWarps);
@@ -1144,19 +1202,27 @@ struct Kernel {
     if (warp >= kConsumerWarps) {  // the producer, and the warps of the wide geometry that
       if (warp == kConsumerWarps)   // only the tensor role uses
         producer(p, sm, w, grp, mp, starts, adapters, base, gcnt,
-                 reinterpret_cast<int4*>(smem + p.off_stab), n_my);
+                 reinterpret_cast<int4*>(smem + p.off_stab), n_my, ctl);
       if (MODE != kExpand) {
         cluster_wait();
         cluster_arrive_relaxed();
       }
     } else {
-      consumer(p, sm, w, grp, mp, n_my);
+      consumer(p, sm, w, grp, mp, n_my, ctl);
     }
     __syncthreads();
-    if (!w.ok()) {  // gave up: let every bulk copy already issued land before the CTA exits
-      const uint64_t t0 = now_ns();
-      while (now_ns() - t0 < 200000ull) __nanosleep(1000);
+    if (!w.ok() && tid == 0) {
+      // Gave up: before the CTA exits, wait (bounded) for every asynchronous copy into its
+      // shared memory -- the last fill of each ring slot, and the partial products that peers
+      // of the cluster may still be pushing.  (Bulk stores were waited for as they were issued.)
+      const uint32_t issued = static_cast<uint32_t>(ctl[kCtlIssued]);
+      const uint32_t par = static_cast<uint32_t>(ctl[kCtlParity]);
+      for (int s = 0; s < sm.nst; ++s)
+        if ((issued >> s) & 1u) w.drain<false>(sm.full(s), (par >> s) & 1u);
+      if (ctl[kCtlPending])
+        w.drain<true>(sm.fixed(ctl[kCtlPendBar]), static_cast<uint32_t>(ctl[kCtlPending] - 1));
     }
+    __syncthreads();
     if (MODE != kExpand) cluster_wait();
   }
 };

@@ -188,8 +188,11 @@ struct TcRole {
   // the warp to the ring slot, not to the sequence number, keeps every use of a slot issued in
   // order by one warp: a parity wait on the slot's "empty" barrier can then never be satisfied
   // by a phase two uses old.
-  __device__ __forceinline__ static void loader(const Params& p, const Ctx& c, const Waiter& w,
-                                                TcWalk wk) {
+  // Returns, for the drain of a CTA that gives up, the ring slots this warp filled (low 16
+  // bits) and the phase parity of each one's last fill (high 16 bits).
+  __device__ __forceinline__ static uint32_t loader(const Params& p, const Ctx& c,
+                                                    const Waiter& w, TcWalk wk) {
+    uint32_t issued = 0, parity = 0;
     const int lt = threadIdx.x;  // 0..127
     const int warp = lt >> 5, lane = lt & 31;
     const T* x = static_cast<const T*>(p.x);
@@ -317,6 +320,8 @@ struct TcRole {
             cp_async16_zero(d, Ak);
         }
         cp_async_arrive(bar);
+        issued |= 1u << rg.s;
+        parity = (parity & ~(1u << rg.s)) | (rg.par << rg.s);
       }
       if (!ok) break;
       // expand slots: B rows [r x 64] + y rows [128 x 64]
@@ -354,11 +359,14 @@ struct TcRole {
           }
         }
         cp_async_arrive(bar);
+        issued |= 1u << rg.s;
+        parity = (parity & ~(1u << rg.s)) | (rg.par << rg.s);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(c.fx(kTcRtFree0 + par));
     }
     cp_async_wait_all();  // every copy lands before the CTA moves on
+    return issued | (parity << 16);
   }
 
   // ---------------------------------------------------------------------- MMA issuer ----
@@ -448,7 +456,7 @@ struct TcRole {
   // been read.
   __device__ __forceinline__ static bool exchange(const Params& p, const Ctx& c, const Waiter& w,
                                                   uint32_t tq, int q, int lane, int tok_row,
-                                                  uint32_t rnd) {
+                                                  uint32_t rnd, int* ctl) {
     const bool has_k = c.k_hi > c.k_lo;
     const uint32_t rs = c.xchg, ag = c.xchg + kTcHalfXchg;
     for (int j = 0; j < R / 16; ++j) {
@@ -483,6 +491,7 @@ struct TcRole {
         if (lane == 0) {
           mbar_arrive_expect_tx(c.fx(kTcRsFull), kTcHalfXchg);
           mbar_arrive_expect_tx(c.fx(kTcAgFull), MODE == kFused ? kTcHalfXchg : 3 * 4);
+          ctl[kCtlPending] = 1 + static_cast<int>(ph);  // both armed: drained if we give up
         }
         if (!wwait_cluster(w, c.fx(kTcRsFull), ph)) return false;
         float sum[16];
@@ -533,14 +542,24 @@ struct TcRole {
               st_async_f32(cluster_map(ag, pp), 0.f, cluster_map(c.fx(kTcAgFull), pp));
         }
         if (!wwait_cluster(w, c.fx(kTcAgFull), ph)) return false;
+        if (lane == 0) ctl[kCtlPending] = 0;
       }
     }
     return true;
   }
 
   // ------------------------------------------------------------------------ epilogue ----
+  // On every exit, normal or after a wait ran out, this thread's TMA stores have finished
+  // reading shared memory before it returns.
   __device__ __forceinline__ static void epilogue(const Params& p, const Ctx& c, const Waiter& w,
-                                                  TcWalk wk, uint32_t tm, int g) {
+                                                  TcWalk wk, uint32_t tm, int g, int* ctl) {
+    epilogue_tiles(p, c, w, wk, tm, g, ctl);
+    bulk_wait_read();
+  }
+
+  __device__ __forceinline__ static void epilogue_tiles(const Params& p, const Ctx& c,
+                                                        const Waiter& w, TcWalk wk, uint32_t tm,
+                                                        int g, int* ctl) {
     const int q = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;  // TMEM lane quarter, lane
     const int row = q * 32 + lane;                                   // tile row = TMEM lane
     const uint32_t tq = tm + (static_cast<uint32_t>(q * 32) << 16);
@@ -558,6 +577,16 @@ struct TcRole {
       if (!wwait(w, c.fx(kTcRtFull0 + par), (li >> 1) & 1)) return;
       const int* rt = c.rowtok + par * kTcRows;
       const int tok_row = rt[row];
+      volatile int* tile_go = ctl + kCtlTileGo;
+      if (kGroups == 2 && g == 1) {
+        // The second group skips the per-m-tile work below and would reach this m-tile's first
+        // expand slot while the ring is still cycling through its shrink fills: a parity wait
+        // on that slot could then see a shrink phase complete and pass two phases early.  It
+        // waits first until group 0 has seen every shrink MMA of the m-tile complete (a
+        // monotonic counter: no phase aliasing), after which the slot's next completed phase
+        // is its expand fill.
+        if (!__all_sync(0xffffffffu, w.until(tile_go, li))) return;
+      }
       if (g == 0) {  // the per-m-tile work: v into TMEM as hi / lo
         if constexpr (kDoShrink) {
           if (!wwait(w, c.fx(kTcVFull), li & 1)) return;
@@ -565,10 +594,11 @@ struct TcRole {
         if constexpr (kDoExpand) {
           if (!wwait(w, c.fx(kTcHFree), (li & 1) ^ 1)) return;
         }
+        if (kGroups == 2 && q == 0 && lane == 0) *tile_go = li;  // shrink slots all consumed
         tc_fence_after();
         if constexpr (kDoShrink) {
           if (c.split) {
-            if (!exchange(p, c, w, tq, q, lane, tok_row, rnd)) return;
+            if (!exchange(p, c, w, tq, q, lane, tok_row, rnd, ctl)) return;
             rnd += R / 16;
           } else {
 #pragma unroll
@@ -751,6 +781,8 @@ struct TcRole {
     }
     uint32_t* tslot = reinterpret_cast<uint32_t*>(ctl + 1);
     if (tid == 0) {
+      ctl[kCtlPending] = 0;
+      ctl[kCtlTileGo] = -1;
       for (int s = 0; s < c.slots; ++s) {
         mbar_init(c.full(s), 32 + 1);  // the filling warp's cp.async arrivals + TMA bytes
         mbar_init(c.empty(s), 1 + 4);
@@ -820,12 +852,13 @@ struct TcRole {
       wk.u1 = static_cast<int>(U * (unit + 1) / n_units);
     }
 
+    uint32_t filled = 0;  // loader warps: slots filled and their parities (drain)
     if (warp < 4) {
-      loader(p, c, w, wk);
+      filled = loader(p, c, w, wk);
     } else if (warp < kConsumerWarps) {
-      epilogue(p, c, w, wk, tm, 0);
+      epilogue(p, c, w, wk, tm, 0, ctl);
     } else if (kGroups == 2 && warp > kConsumerWarps) {
-      epilogue(p, c, w, wk, tm, 1);
+      epilogue(p, c, w, wk, tm, 1, ctl);
     } else if (warp == kConsumerWarps && (tid & 31) == 0) {
       issuer(p, c, w, wk, tm);
       // every MMA issued has completed before TMEM is released
@@ -837,6 +870,20 @@ struct TcRole {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (!w.ok()) {
+      // Gave up: before the CTA exits, wait (bounded) for every asynchronous copy into its
+      // shared memory -- the TMA loads of each slot's last fill (cp.async copies were waited
+      // for by their warps) and the exchange data that peers may still be pushing.
+      if (warp < 4 && (tid & 31) == 0)
+        for (int s = 0; s < c.slots; ++s)
+          if ((filled >> s) & 1u) w.drain<false>(c.full(s), (filled >> (16 + s)) & 1u);
+      if (tid == 0 && ctl[kCtlPending]) {
+        const uint32_t ph = static_cast<uint32_t>(ctl[kCtlPending] - 1);
+        w.drain<true>(c.fx(kTcRsFull), ph);
+        w.drain<true>(c.fx(kTcAgFull), ph);
+      }
+      __syncthreads();
+    }
     if (warp == kConsumerWarps) tmem_dealloc(tm, kTcCols);
     if (c.split) {  // no member leaves while a peer may still write to it (every incoming
       cluster_arrive_relaxed();  // byte was counted by a barrier this CTA waited on)

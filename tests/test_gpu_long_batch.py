@@ -119,3 +119,29 @@ def test_long_batch_unfused_forms():
         y_ref = oracle.sgmv_expand(c.y0.double().cpu().numpy(), v.double().cpu().numpy(), B, ss,
                                    sa, 0, w.scale)
         harness.assert_close(y.float().cpu().numpy(), y_ref, f"expand {mode}")
+
+
+@pytest.mark.parametrize("dtype,r", [("bf16", 64), ("f16", 16)])
+def test_long_batch_ring_reuse_across_shrink_and_expand(dtype, r):
+    """More shrink chunks per cluster member than the ring has slots (h_in = 3072: 12 chunks
+    per member over 8 slots), so every expand slot reuses a slot that held shrink data earlier
+    in the same m-tile, and many n-tiles per member for both epilogue groups of the 416-thread
+    kernel.  Fused and unfused forms against the oracle, every row."""
+    import oracle
+    from segmented_gather_gemm_sgmv_gb300 import sgmv_expand, sgmv_shrink
+    w = workloads.Workload("long_reuse", 3072, 2560, r, dtype, 4, 1)
+    ss, sa = _table([400, 200, 129, 300, 3], [0, 1, 2, 0, 3])
+    c = harness.make_case(w, ss, sa)
+    y = harness.run_apply(c, 0, tensor_cores="always", long_batch=True)
+    harness.assert_close(y.float().cpu().numpy(), harness.oracle_apply(c, 0),
+                         f"ring reuse {dtype} fused")
+    keys = harness.touched(sa, ss)
+    B = harness.oracle_blocks(c.B, keys, 0)
+    v = torch.zeros((c.M, r), device="cuda")
+    sgmv_shrink(v, c.x, c.A_ptrs, c.d_ss, c.d_sa, 0, r, tensor_cores="always", long_batch=True)
+    y = c.y0.clone()
+    sgmv_expand(y, v, c.B_ptrs, c.d_ss, c.d_sa, 0, r, w.scale, tensor_cores="always",
+                long_batch=True)
+    y_ref = oracle.sgmv_expand(c.y0.double().cpu().numpy(), v.double().cpu().numpy(), B, ss, sa,
+                               0, w.scale)
+    harness.assert_close(y.float().cpu().numpy(), y_ref, f"ring reuse {dtype} expand")

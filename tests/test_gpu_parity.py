@@ -370,3 +370,58 @@ def test_max_segments():
                    torch.as_tensor(ss2, device="cuda"), torch.as_tensor(sa2, device="cuda"), 0,
                    w.r, w.scale)
     assert e.value.status == -3
+
+
+def test_tensor_role_wait_timeout_reports_and_recovers():
+    """The bounded-wait path of the tensor-core role: long adapter groups (>= 64 rows, forced
+    onto tcgen05), a barrier that nothing completes, a short bound.  The error word reads
+    SGMV_ETIMEOUT, y is untouched, and the next call matches the oracle."""
+    from segmented_gather_gemm_sgmv_gb300 import sgmv_get_error, sgmv_set_wait_limit
+    for dtype, r, h_in, h_out in (("bf16", 64, 512, 640), ("f16", 16, 1024, 768)):
+        w = workloads.Workload("stall_tc", h_in, h_out, r, dtype, 3, 2)
+        ss = np.array([0, 150, 170, 420, 425], np.int32)
+        sa = np.array([0, 2, 1, 0], np.int32)
+        c = harness.make_case(w, ss, sa)
+        assert sgmv_get_error(clear=True) == 0
+        for long_batch in (False, True):
+            sgmv_set_wait_limit(2_000_000, inject_stall=True)  # 2 ms
+            try:
+                y = harness.run_apply(c, 1, tensor_cores="always", long_batch=long_batch)
+                torch.cuda.synchronize()
+            finally:
+                sgmv_set_wait_limit(0, inject_stall=False)
+            assert sgmv_get_error(clear=True) == -5
+            assert torch.equal(y, c.y0), "a timed-out call must not write y"
+            y = harness.run_apply(c, 1, tensor_cores="always", long_batch=long_batch)
+            harness.assert_close(y.float().cpu().numpy(), harness.oracle_apply(c, 1),
+                                 f"{dtype} r={r} after timeout (long_batch={long_batch})")
+            assert sgmv_get_error(clear=True) == 0
+
+
+def test_validate_pointers_matches_oracle():
+    """The pointer check flags null and misaligned weight pointers of the adapters a table
+    uses, exactly as the oracle does.  The bad tables go to the validator only, never to a
+    compute call."""
+    import oracle
+    from segmented_gather_gemm_sgmv_gb300 import sgmv_validate_pointers
+    rng = np.random.default_rng(3)
+    d_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for trial in range(30):
+        n = int(rng.integers(1, 40))
+        ss, sa = workloads.random_segments(rng, int(rng.integers(0, 300)), 4, n, p_empty=0.2)
+        sa = np.where(rng.random(len(sa)) < 0.1, -1, sa).astype(np.int32)
+        if len(sa) and rng.random() < 0.3:
+            sa[int(rng.integers(0, len(sa)))] = n + 2  # past the pool: skipped here
+        A = (0x7f0000000000 + 4096 * np.arange(n, dtype=np.uint64)).astype(np.uint64)
+        B = (0x7f1000000000 + 4096 * np.arange(n, dtype=np.uint64)).astype(np.uint64)
+        for arr in (A, B):
+            for j in rng.choice(n, size=int(rng.integers(0, 3)), replace=True):
+                arr[j] = 0 if rng.random() < 0.5 else arr[j] + np.uint64(8 * rng.integers(1, 2))
+        use_a, use_b = [(True, True), (True, False), (False, True)][trial % 3]
+        dA = torch.as_tensor(A.view(np.int64), device="cuda") if use_a else None
+        dB = torch.as_tensor(B.view(np.int64), device="cuda") if use_b else None
+        d_ss = torch.as_tensor(ss, device="cuda")
+        d_sa = torch.as_tensor(sa, device="cuda")
+        sgmv_validate_pointers(dA, dB, d_ss, d_sa, d_err)
+        want = oracle.validate_pointers(A if use_a else None, B if use_b else None, ss, sa, n)
+        assert int(d_err.item()) == want, (trial, int(d_err.item()), want)
