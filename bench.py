@@ -1,30 +1,43 @@
 #!/usr/bin/env python3
 """Benchmark of the fused SGMV LoRA apply (lora_apply) on one or more GB300s.
 
-One step = one lora_apply call: one batch of tokens through one LoRA layer (fused shrink +
-expand over every segment).  Default workload: decode_distinct -- Llama-7B projection
-h_in=h_out=4096, r=16, fp16, 64 tokens, each its own length-1 segment and its own adapter of a
-64-adapter pool stacked over 32 layers; the steps sweep layer_idx 0..31 and rotate 32 x/y buffer
-sets, so every step reads inputs that are not in L2 (the sweep touches ~0.55 GB > 129 MB L2).
+Step.  One step is one decode step's LoRA pass over every layer of the model for one
+projection: a layer sweep of lora_apply calls (one launch each) on one batch.  Headline
+workload: decode_distinct -- Llama-7B projection h_in=h_out=4096, r=16, fp16, 64 tokens, each
+its own length-1 segment and its own adapter of a 64-adapter pool stacked over 32 layers; a
+step is 32 calls (layer_idx 0..31), each on its own x / y buffer set, so every call reads
+weights and activations that are not in L2 (the sweep touches ~0.6 GB > 129 MB of L2).  The
+calls of a step are replayed from one CUDA graph and launched with SGMV_OVERLAP_PRIOR.
 
 Prints one JSON line (rank 0):
-  value      achieved algorithmic HBM GB/s (bytes: each distinct adapter's A and B once, x
-             once, y read + written), whole job, inputs resident in HBM, CUDA-graph replay,
-             CUDA events on the launching stream;
-  e2e        the same metric through the public API with pinned HOST buffers: every step copies
-             its x, y_in and segment table host->device and reads y back;
-  roofline   achieved / measured HBM copy bandwidth of the GB300s;
-  cpu_baseline  the fp64 oracle (single thread) on a bounded sample of the same workload.
+  value         algorithmic HBM GB/s, whole job (bytes per call: each distinct adapter's A
+                and B once, x once, y read + written once), inputs resident in HBM, CUDA events
+                on the launching stream around exactly K steps;
+  e2e           the same metric through the public API with pinned HOST buffers: every call of
+                a step copies its x, y_in and segment table host->device and reads y back;
+  roofline      achieved / measured HBM copy bandwidth (and the FLOP term beside it);
+  per_config    every named workload (decode_distinct, decode_zipf, decode_uniform,
+                decode_same, prefill_mixed, mixed_70b): us per call chained and isolated, the
+                unfused shrink + expand pair, GB/s, tokens/s, roofline fraction, clocks;
+  cpu_baseline  the fp64 oracle on all host cores (threads over disjoint segment ranges) on
+                one call of the headline batch.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+--gpus N without an external launcher re-launches this script through torch.distributed.run
+with N local ranks (one replica per GPU: the batches are independent, no collective on the data
+path; only the barriers and the max over ranks of the step time).
 """
 from __future__ import annotations
 
 import argparse
-import hashlib
+import concurrent.futures as cf
 import glob
+import hashlib
 import json
+import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -40,6 +53,12 @@ from segmented_gather_gemm_sgmv_gb300 import workloads  # noqa: E402
 
 METRIC = "SGMV shrink+expand achieved HBM GB/s & tokens/s at h=4096,r=16 (% roofline)"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1700.0  # sustained, the profiling recipe's fallback
+# FP32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (unit counts and the
+# maximum SM clock).
+FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+PER_CONFIG = ("decode_distinct", "decode_zipf", "decode_uniform", "decode_same", "prefill_mixed",
+              "mixed_70b")
 
 
 # ------------------------------------------------------------------ accounting ----
@@ -53,6 +72,26 @@ def algorithmic_bytes(w, ss, sa):
             D.add(int(k))
     eb = w.elem_bytes
     return len(D) * (w.h_in * w.r + w.r * w.h_out) * eb + M * w.h_in * eb + 2 * M * w.h_out * eb, M
+
+
+def group_rows(ss, sa):
+    rows = {}
+    for i, k in enumerate(sa):
+        n = int(ss[i + 1]) - int(ss[i])
+        if n > 0 and k >= 0:
+            rows[int(k)] = rows.get(int(k), 0) + n
+    return rows
+
+
+def tensor_core_rows(w, ss, sa, tensor_cores="auto"):
+    """Rows that the library's documented routing rule sends to the tensor cores (fp16 / bf16,
+    r >= 16, adapter groups of >= 64 rows whose CUDA-core items would re-read >= 32 MB of
+    weights; include/sgmv.h, lora_apply)."""
+    if w.dtype == "f32" or w.r < 16 or tensor_cores == "never":
+        return 0
+    wbytes = w.r * 2 * (w.h_in + w.h_out)
+    need = 64 if tensor_cores == "always" else max(64, 4 * math.ceil(32 * 1048576 / wbytes))
+    return sum(n for n in group_rows(ss, sa).values() if n >= need)
 
 
 def flops(w, M):
@@ -70,8 +109,9 @@ def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return (float(d["hbm_gbs"]), float(d.get("bf16_tflops_sustained", FALLBACK_BF16_TFLOPS)),
+                "measured")
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def recorded_traffic(workload):
@@ -86,9 +126,35 @@ def recorded_traffic(workload):
     return d.get("dram_bytes_per_launch")
 
 
+def roofline(w, ss, sa, us_per_call, tensor_cores="auto"):
+    """max(bytes / HBM, FLOPs / peak): the tensor-core FLOPs against the measured sustained
+    bf16 (= fp16) peak, the CUDA-core FLOPs against the FP32 peak; fraction = roofline time /
+    measured time."""
+    hbm, tc_peak, kind = measured_peaks()
+    nbytes, M = algorithmic_bytes(w, ss, sa)
+    m_tc = tensor_core_rows(w, ss, sa, tensor_cores)
+    f_tc, f_cc = flops(w, m_tc), flops(w, M - m_tc)
+    t_mem = nbytes / (hbm * 1e9)
+    t_flop = f_tc / (tc_peak * 1e12) + f_cc / (FP32_TFLOPS * 1e12)
+    per = us_per_call * 1e-6
+    achieved = nbytes / per / 1e9
+    bound = "hbm" if t_mem >= t_flop else ("tensor" if f_tc / tc_peak >= f_cc / FP32_TFLOPS
+                                          else "alu")
+    out = {"bound": bound, "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+           "frac": round(max(t_mem, t_flop) / per, 4), "peak_source": kind,
+           "t_mem_us": round(t_mem * 1e6, 3), "t_flop_us": round(t_flop * 1e6, 3),
+           "flop_peaks_tflops": {"tensor_bf16_sustained": tc_peak, "fp32_cuda_cores":
+                                 round(FP32_TFLOPS, 1)},
+           "flops_tensor": f_tc, "flops_cuda_cores": f_cc}
+    if bound != "hbm":  # the FLOP term dominates: report against its peak
+        out.update(achieved=round((f_tc + f_cc) / per / 1e12, 2), unit="TFLOP/s",
+                   peak=tc_peak if bound == "tensor" else round(FP32_TFLOPS, 1))
+    return out
+
+
 # ---------------------------------------------------------------------- clocks ----
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi sampling of SM clock and throttle reasons while a timed region runs."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -169,12 +235,32 @@ def barrier(world):
         dist.barrier()
 
 
-# ----------------------------------------------------------------- our arm ----
-class Setup:
-    """Device-resident inputs of the workload: pool, NB rotating x/y sets, segment table."""
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
 
-    def __init__(self, w, device, nbuf=32, seed=0, overlap=True, tensor_cores="auto",
-                 long_batch=False, strided=False):
+
+def relaunch_cmd(argv, n):
+    """The torch.distributed.run command that runs this script with n local ranks."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={n}", "--master-addr=127.0.0.1",
+            f"--master-port={_free_port()}", os.path.abspath(__file__)] + list(argv)
+
+
+# ----------------------------------------------------------------- our arm ----
+def sweep_len(w):
+    """Calls per step: every layer of the pool once (a single-layer pool: 20 repeats)."""
+    return w.layers if w.layers > 1 else 20
+
+
+class Setup:
+    """Device-resident inputs of the workload: pool, one x/y set per call of a step, table."""
+
+    def __init__(self, w, device, seed=0, overlap=True, tensor_cores="auto", long_batch=False,
+                 strided=False):
         import torch
         self.w = w
         self.overlap = overlap
@@ -187,10 +273,10 @@ class Setup:
         self.B_ptrs = workloads.pointer_table(self.B, device)
         self.d_ss = torch.as_tensor(self.ss, device=device)
         self.d_sa = torch.as_tensor(self.sa, device=device)
-        self.nbuf = nbuf
+        self.calls = sweep_len(w)
         self.x, self.y = [], []
         self.strided = strided
-        for i in range(nbuf):
+        for i in range(self.calls):
             x, y = workloads.make_activations(w, self.M, device, seed=seed + 100 + i)
             if strided:  # the middle third of 3x-wide rows, as q / k / v of a fused output
                 X = torch.zeros((self.M, 3 * w.h_in), dtype=x.dtype, device=device)
@@ -200,66 +286,129 @@ class Setup:
                 x, y = X[:, w.h_in:2 * w.h_in], Y[:, w.h_out:2 * w.h_out]
             self.x.append(x)
             self.y.append(y)
+        self.v = None
 
-    def call(self, step, stream=None):
+    def call(self, i, stream=None):
         from segmented_gather_gemm_sgmv_gb300 import lora_apply
-        i = step % self.nbuf
         lora_apply(self.y[i], self.x[i], self.A_ptrs, self.B_ptrs, self.d_ss, self.d_sa,
-                   step % self.w.layers, self.w.r, self.w.scale, stream=stream,
+                   i % self.w.layers, self.w.r, self.w.scale, stream=stream,
                    overlap_prior=self.overlap, tensor_cores=self.tensor_cores,
                    long_batch=self.long_batch)
 
+    def call_unfused(self, i, stream=None):
+        """The pages' two launches per layer: sgmv_shrink into v, then sgmv_expand."""
+        import torch
+        from segmented_gather_gemm_sgmv_gb300 import sgmv_expand, sgmv_shrink
+        if self.v is None:
+            self.v = torch.zeros((self.M, self.w.r), dtype=torch.float32, device=self.x[0].device)
+        kw = dict(stream=stream, tensor_cores=self.tensor_cores, long_batch=self.long_batch,
+                  overlap_prior=self.overlap)
+        sgmv_shrink(self.v, self.x[i], self.A_ptrs, self.d_ss, self.d_sa, i % self.w.layers,
+                    self.w.r, **kw)
+        sgmv_expand(self.y[i], self.v, self.B_ptrs, self.d_ss, self.d_sa, i % self.w.layers,
+                    self.w.r, self.w.scale, **kw)
 
-def capture(torch, fn, n, stream):
+    def flags_text(self):
+        t = ("lora_apply_ex(SGMV_OVERLAP_PRIOR): each call's weight prefetch overlaps the "
+             "previous call (programmatic dependent launch)" if self.overlap else
+             "lora_apply: each call starts after the previous one completes")
+        if self.long_batch:
+            t += "; SGMV_LONG_BATCH (a prefill batch: one CTA per SM, whole shared memory)"
+        return t
+
+
+def capture_step(torch, fn, n, stream):
+    """A CUDA graph of one step (n calls)."""
+    with torch.cuda.stream(stream):
+        for i in range(n):  # uncaptured first calls set the kernels' attributes
+            fn(i, stream)
+    torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for s in range(n):
-            fn(s)
+        for i in range(n):
+            fn(i, stream)
     return g
 
 
-def time_graph_steps(torch, setup, K, W, stream, world):
-    """Device time of K steps (graph replays of one layer sweep), CUDA events on `stream`."""
-    per = setup.w.layers * max(1, setup.nbuf // setup.w.layers)
-    per = max(per, setup.nbuf)
+def time_steps(torch, g, K, W, stream, world=1):
+    """Device time (ms) of exactly K replays of the step graph after W untimed ones; barrier +
+    synchronize on both sides; CUDA events on the launching stream."""
     with torch.cuda.stream(stream):
-        for s in range(per):  # uncaptured first calls set kernel attributes
-            setup.call(s, stream)
-    torch.cuda.synchronize()
-    g_full = capture(torch, lambda s: setup.call(s, stream), per, stream)
-    rem = K % per
-    g_rem = capture(torch, lambda s: setup.call(s, stream), rem, stream) if rem else None
-    with torch.cuda.stream(stream):  # replay() launches on the current stream
-        for _ in range(max(1, (W + per - 1) // per)):
-            g_full.replay()
+        for _ in range(W):
+            g.replay()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.nvtx.range_push("timed")
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(K // per):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
+        for _ in range(K):
+            g.replay()
         e1.record(stream)
-    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(world)
     return e0.elapsed_time(e1)
 
 
+def steps_for(torch, g, stream, seconds):
+    """How many replays of g fill about `seconds` (measured on a few replays)."""
+    ms = time_steps(torch, g, 3, 2, stream)
+    return max(5, int(seconds * 1e3 / max(ms / 3, 1e-3)))
+
+
+def measure_config(torch, name, device, stream, seconds, args):
+    """One per_config entry: chained, isolated and unfused us per call, with clocks."""
+    w = workloads.WORKLOADS[name]
+    long_batch = {"auto": w.prefill, "on": True, "off": False}[args.long_batch]
+    setup = Setup(w, device, tensor_cores=args.tensor_cores, long_batch=long_batch)
+    n = setup.calls
+    out = {"calls_per_step": n, "layers": w.layers}
+    nbytes, M = algorithmic_bytes(w, setup.ss, setup.sa)
+    for label, overlap, fn in (("isolated", False, setup.call), ("unfused", True,
+                                                                 setup.call_unfused),
+                               ("chained", True, setup.call)):
+        setup.overlap = overlap
+        g = capture_step(torch, fn, n, stream)
+        K = steps_for(torch, g, stream, seconds)
+        clocks = ClockSampler(torch.cuda.current_device()).start() if label == "chained" else None
+        ms = time_steps(torch, g, K, 3, stream)
+        us = ms * 1e3 / (K * n)
+        out[f"us_per_call_{label}"] = round(us, 3)
+        if clocks is not None:
+            out["clocks"] = clocks.stop()
+            out["timed_calls"] = K * n
+        del g
+    from segmented_gather_gemm_sgmv_gb300 import binding
+    if binding.sgmv_get_error(clear=True) != 0:
+        raise RuntimeError(f"{name}: a device-side wait ran out")
+    us = out["us_per_call_chained"]
+    out.update({
+        "launch": setup.flags_text(),
+        "unfused_launch": "sgmv_shrink_ex + sgmv_expand_ex (two launches per call, same flags)",
+        "GB_per_s": round(nbytes / us / 1e3, 2),
+        "tokens_per_s": round(M / us * 1e6, 1),
+        "bytes_per_call": nbytes, "flops_per_call": flops(w, M), "tokens": M,
+        "distinct_adapters": len(group_rows(setup.ss, setup.sa)),
+        "tensor_core_rows": tensor_core_rows(w, setup.ss, setup.sa, args.tensor_cores),
+        "roofline": roofline(w, setup.ss, setup.sa, us, args.tensor_cores),
+        "roofline_isolated_frac": roofline(w, setup.ss, setup.sa, out["us_per_call_isolated"],
+                                           args.tensor_cores)["frac"],
+    })
+    del setup
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_e2e(torch, setup, K, stream):
-    """Public-API path with pinned host buffers.  Per step: ONE host->device copy of the step's
+    """Public-API path with pinned host buffers.  Per call: ONE host->device copy of the call's
     inputs (x, y_in and the segment table packed in one pinned staging buffer), the lora_apply
-    call on views of the device copy, ONE device->host copy of y.  Steps alternate between two
-    streams and two device / host buffer sets, so that one step's copies overlap the other
-    stream's kernel; each stream runs its steps in order (a buffer set is reused only after
-    its previous step's copy back has completed)."""
+    call on views of the device copy, ONE device->host copy of y.  Calls alternate between two
+    streams and two device / host buffer sets, so that one call's copies overlap the other
+    stream's kernel; each stream runs its calls in order.  Returns seconds per step (one step =
+    the same number of calls as a device-timed step)."""
     w = setup.w
-    n = min(K, 2048)
     dt = workloads.torch_dtype(w.dtype)
     x0, y0 = setup.x[0], setup.y[0]
     eb = x0.element_size()
@@ -289,7 +438,7 @@ def time_e2e(torch, setup, K, stream):
                          out=torch.empty(y0.shape, dtype=dt).pin_memory()))
     from segmented_gather_gemm_sgmv_gb300 import lora_apply
 
-    def step(s):
+    def one(s):
         st, b = streams[s % 2], sets[s % 2]
         with torch.cuda.stream(st):
             b["dev"].copy_(host, non_blocking=True)
@@ -298,36 +447,26 @@ def time_e2e(torch, setup, K, stream):
                        tensor_cores=setup.tensor_cores, long_batch=setup.long_batch)
             b["out"].copy_(b["y"], non_blocking=True)
 
-    def sweep(n_steps):
+    def step():
         streams[1].wait_stream(streams[0])  # fork
-        for s in range(n_steps):
-            step(s)
+        for s in range(setup.calls):
+            one(s)
         streams[0].wait_stream(streams[1])  # join
 
-    per = w.layers if w.layers % 2 == 0 else 2 * w.layers
     with torch.cuda.stream(stream):
-        sweep(4)
+        step()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        sweep(per)
-    with torch.cuda.stream(stream):
-        g.replay()
-    torch.cuda.synchronize()
-    reps = max(1, n // per)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    return ms / (reps * per), total, ny, reps * per
+        step()
+    ms = time_steps(torch, g, K, 3, stream)
+    return ms / 1e3 / K, total * setup.calls, ny * setup.calls
 
 
 def cpu_baseline(w, setup, seconds=10.0):
-    """The fp64 oracle, single-threaded, on the full batch at layer 0, repeated for ~seconds."""
+    """The fp64 oracle on all host cores: the headline batch at layer 0 split into disjoint
+    segment ranges, one per thread (the oracle's C loop runs with the GIL released), repeated
+    for ~seconds; the single-thread figure is reported beside it."""
     import oracle
     keys = sorted({int(k) for i, k in enumerate(setup.sa)
                    if k >= 0 and setup.ss[i + 1] > setup.ss[i]})
@@ -336,22 +475,36 @@ def cpu_baseline(w, setup, seconds=10.0):
     for k in keys:
         A[k] = setup.A[k, 0:1].double().cpu().numpy()
         B[k] = setup.B[k, 0:1].double().cpu().numpy()
-    call = oracle.PreparedApply(setup.y[0].double().cpu().numpy(),
-                                setup.x[0].double().cpu().numpy(), A, B, setup.ss, setup.sa, 0,
-                                w.scale)
-    n, t0 = 0, time.perf_counter()
-    while True:
-        call()
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    nbytes, M = algorithmic_bytes(w, setup.ss, setup.sa)
-    per = el / n
-    return {"value": round(nbytes / per / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"oracle_lora_apply (fp64, 1 thread) on the whole {w.name} batch "
-                      f"({M} tokens, layer 0), {n} calls in {el:.1f} s",
-            "tokens_per_s": round(M / per, 2), "us_per_call": round(per * 1e6, 1)}
+    y = setup.y[0].double().cpu().numpy()
+    x = setup.x[0].double().cpu().numpy()
+    ss, sa = np.asarray(setup.ss), np.asarray(setup.sa)
+    nbytes, M = algorithmic_bytes(w, ss, sa)
+    cores = max(1, min(os.cpu_count() or 1, len(sa)))
+    parts = [p for p in np.array_split(np.arange(len(sa)), cores) if len(p)]
+    calls = [oracle.PreparedApply(y, x, A, B, ss[p[0]:p[-1] + 2], sa[p[0]:p[-1] + 1], 0, w.scale)
+             for p in parts]
+    single = oracle.PreparedApply(y, x, A, B, ss, sa, 0, w.scale)
+
+    def timed(fn, budget):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= budget:
+                return el / n, n, el
+
+    with cf.ThreadPoolExecutor(max_workers=len(calls)) as ex:
+        per, n, el = timed(lambda: list(ex.map(lambda c: c(), calls)), seconds)
+    per1, n1, _ = timed(single, min(seconds, 3.0))
+    return {"value": round(nbytes / per / 1e9, 4), "unit": "GB/s", "cores": len(calls),
+            "kind": "oracle",
+            "sample": f"oracle_lora_apply (fp64) on the whole {w.name} batch ({M} tokens, layer "
+                      f"0), split into {len(calls)} disjoint segment ranges on {len(calls)} "
+                      f"threads; {n} calls in {el:.1f} s",
+            "tokens_per_s": round(M / per, 2), "us_per_call": round(per * 1e6, 1),
+            "single_thread": {"value": round(nbytes / per1 / 1e9, 4), "unit": "GB/s",
+                              "us_per_call": round(per1 * 1e6, 1), "calls": n1}}
 
 
 def run_ours(args):
@@ -365,79 +518,99 @@ def run_ours(args):
     torch.cuda.set_device(device)
     from segmented_gather_gemm_sgmv_gb300 import binding
     binding.lib()
+    stream = torch.cuda.Stream(device)
+    K, W = args.steps, args.warmup
+
+    per_config = {}
+    if world == 1 and not args.no_per_config:
+        for name in PER_CONFIG:
+            per_config[name] = measure_config(torch, name, device, stream, args.config_seconds,
+                                              args)
+
     w = workloads.WORKLOADS[args.workload]
     long_batch = {"auto": w.prefill, "on": True, "off": False}[args.long_batch]
     setup = Setup(w, device, tensor_cores=args.tensor_cores, long_batch=long_batch,
                   strided=args.strided)
-    stream = torch.cuda.Stream(device)
     nbytes, M = algorithmic_bytes(w, setup.ss, setup.sa)
-    K, W = args.steps, args.warmup
+    n = setup.calls
 
-    # isolated calls (each kernel waits for the previous one to finish): context figure
-    setup.overlap = False
-    ms_iso = time_graph_steps(torch, setup, min(K, 6400), W, stream, world)
-    us_iso = ms_iso * 1e3 / min(K, 6400)
+    setup.overlap = False  # isolated calls (each kernel waits for the previous one to finish)
+    g_iso = capture_step(torch, setup.call, n, stream)
+    ms_iso = time_steps(torch, g_iso, max(K, 3), 3, stream, world)
+    us_iso = ms_iso * 1e3 / (max(K, 3) * n)
+    del g_iso
     setup.overlap = not args.no_overlap
+    g = capture_step(torch, setup.call, n, stream)
     clocks = ClockSampler(torch.cuda.current_device()).start()
-    time.sleep(0.3)
-    ms = time_graph_steps(torch, setup, K, W, stream, world)
+    ms = time_steps(torch, g, K, W, stream, world)
+    # nvidia-smi samples every 50 ms: a short timed region is extended, for the clock record
+    # only, by untimed replays of the same graph (the same load) for 0.3 s after it.
+    extra = 0
+    if ms < 300.0:
+        per_ms = max(ms / K, 1e-3)
+        extra = int(300.0 / per_ms) + 1
+        with torch.cuda.stream(stream):
+            for _ in range(extra):
+                g.replay()
+        torch.cuda.synchronize()
     clk = clocks.stop()
+    clk["window"] = ("the W warm-up replays, the K timed steps" +
+                     (f" and {extra} untimed replays of the same step after them" if extra else ""))
     ms = reduce_max(ms, world, device)
     if binding.sgmv_get_error(clear=True) != 0:
         raise RuntimeError("a device-side wait ran out during the timed region")
-    per = ms / 1e3 / K
-    e2e_s, h2d, d2h, e2e_n = time_e2e(torch, setup, K, stream)
-    e2e_s = reduce_max(e2e_s, world, device) / 1e3
+    per_step = ms / 1e3 / K
+    us_call = per_step / n * 1e6
+    e2e_s, h2d, d2h = time_e2e(torch, setup, max(3, min(K, 200)), stream)
+    e2e_s = reduce_max(e2e_s, world, device)
     if rank != 0:
         dist_finish(world)
         return
-    hbm, peak_kind = measured_peaks()
-    achieved = nbytes / per / 1e9
     line = {
         "metric": METRIC,
-        "value": round(job_value(world, nbytes, per), 2),
+        "value": round(job_value(world, nbytes * n, per_step), 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": K,
         "warmup": W,
-        "ms_per_step": round(per * 1e3, 6),
+        "ms_per_step": round(per_step * 1e3, 6),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic",
         "impl": "ours",
-        "tokens_per_s": round(world * M / per, 1),
-        "us_per_call": round(per * 1e6, 3),
+        "tokens_per_s": round(world * M / (us_call * 1e-6), 1),
+        "us_per_call": round(us_call, 3),
         "us_per_call_isolated": round(us_iso, 3),
-        "launch": ("lora_apply_ex(SGMV_OVERLAP_PRIOR): each call's weight prefetch overlaps the "
-                   "previous call (programmatic dependent launch)" if setup.overlap else
-                   "lora_apply: each call starts after the previous one completes") +
-                  ("; SGMV_LONG_BATCH (a prefill batch: one CTA per SM, whole shared memory)"
-                   if setup.long_batch else ""),
+        "launch": setup.flags_text(),
         "config": {"workload": w.name, "h_in": w.h_in, "h_out": w.h_out, "r": w.r,
                    "tokens": M, "segments": int(len(setup.sa)),
-                   "distinct_adapters": int(len({int(k) for k in setup.sa})),
+                   "distinct_adapters": len(group_rows(setup.ss, setup.sa)),
                    "pool_adapters": w.num_adapters, "layers": w.layers,
+                   "calls_per_step": n,
+                   "step": f"one layer sweep: {n} lora_apply calls (layer_idx 0..{w.layers - 1}"
+                           f"{', repeated' if w.layers == 1 else ''}), each on its own x / y "
+                           "set, replayed from one CUDA graph",
                    "bytes_per_call": nbytes, "flops_per_call": flops(w, M),
-                   "timing": "CUDA graph of one 32-layer sweep replayed; CUDA events on the "
-                             "launching stream",
-                   "l2": "inputs larger than L2: each step reads another layer's weights and "
-                         "another x/y set (sweep footprint > 129 MB)",
+                   "timing": "CUDA events on the launching stream around exactly K graph "
+                             "replays, after W untimed ones",
+                   "l2": "inputs larger than L2: each call reads another layer's weights and "
+                         "another x/y set (the footprint of a step is > 129 MB)",
                    "layout": ("x, y: middle column third of rows 3 h apart (lora_apply_strided)"
                               if setup.strided else "x [M][h_in], y [M][h_out] dense"),
                    "parallelism": f"replica x{world}"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
-                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "traffic": None if setup.strided else recorded_traffic(w.name),
-                     "peak_source": peak_kind,
-                     "kernel": "sgmv_kernel<fused> (lora_apply)"},
-        "e2e": {"value": round(job_value(world, nbytes, e2e_s), 2), "unit": "GB/s",
+        "roofline": dict(roofline(w, setup.ss, setup.sa, us_call, args.tensor_cores),
+                         traffic=None if setup.strided else recorded_traffic(w.name),
+                         kernel="sgmv_kernel<fused> (lora_apply)"),
+        "e2e": {"value": round(job_value(world, nbytes * n, e2e_s), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_n, "us_per_step": round(e2e_s * 1e6, 3)},
-        "gpu_launches": K,
+                "us_per_call": round(e2e_s / n * 1e6, 3)},
+        "gpu_launches": K * n,
         "clocks": clk,
     }
+    if per_config:
+        line["per_config"] = per_config
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, setup, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -453,8 +626,9 @@ def dist_finish(world):
 
 # ------------------------------------------------------------ reference arm ----
 def run_reference(args):
-    """The fp64 oracle timed on the host cores, on this arm's workload: each step is one token
-    of the batch (a length-1 segment with its adapter, layer 0), cycling over the batch."""
+    """The fp64 oracle timed on the host cores, on this arm's workload and step: one step is the
+    same layer sweep (the batch once per layer), every call split into disjoint segment ranges
+    over all host cores.  Rank 0 only."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
@@ -462,54 +636,67 @@ def run_reference(args):
     w = workloads.WORKLOADS[args.workload]
     ss, sa = workloads.make_segments(w.name, 0)
     rng = np.random.default_rng(0)
+    n_calls = sweep_len(w)
+    layers = min(w.layers, 2)  # the work of a call does not depend on the layer's values
     keys = sorted({int(k) for i, k in enumerate(sa) if k >= 0 and ss[i + 1] > ss[i]})
     A = [None] * w.num_adapters
     B = [None] * w.num_adapters
     for k in keys:
-        A[k] = rng.uniform(-1, 1, (1, w.h_in, w.r)) / np.sqrt(w.h_in)
-        B[k] = rng.standard_normal((1, w.r, w.h_out)) / np.sqrt(w.r)
+        A[k] = rng.uniform(-1, 1, (layers, w.h_in, w.r)) / np.sqrt(w.h_in)
+        B[k] = rng.standard_normal((layers, w.r, w.h_out)) / np.sqrt(w.r)
     M = int(ss[-1])
     x = rng.standard_normal((M, w.h_in))
     y = rng.standard_normal((M, w.h_out))
-    rows = [(int(ss[i]), int(k)) for i, k in enumerate(sa) if ss[i + 1] > ss[i] and k >= 0]
-    calls = []
-    for t, k in rows:
-        calls.append(oracle.PreparedApply(y[t:t + 1], x[t:t + 1], A, B, [0, 1], [k], 0, w.scale))
-    for s in range(args.warmup):
-        calls[s % len(calls)]()
-    t0 = time.perf_counter()
-    for s in range(args.steps):
-        calls[s % len(calls)]()
-    el = time.perf_counter() - t0
+    cores = max(1, min(os.cpu_count() or 1, len(sa)))
+    parts = [p for p in np.array_split(np.arange(len(sa)), cores) if len(p)]
+    calls = [oracle.PreparedApply(y, x, A, B, ss[p[0]:p[-1] + 2], sa[p[0]:p[-1] + 1], 0, w.scale)
+             for p in parts]
+    with cf.ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        def step():
+            for i in range(n_calls):
+                list(ex.map(lambda c: c(i % layers), calls))
+        for _ in range(args.warmup):
+            step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step()
+        el = time.perf_counter() - t0
     per = el / args.steps
-    eb = w.elem_bytes
-    nbytes = (w.h_in * w.r + w.r * w.h_out) * eb + w.h_in * eb + 2 * w.h_out * eb
-    val = nbytes / per / 1e9
+    nbytes, _ = algorithmic_bytes(w, ss, sa)
+    val = nbytes * n_calls / per / 1e9
     line = {"metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": w.name, "h_in": w.h_in, "h_out": w.h_out, "r": w.r,
-                       "step": "one token of the batch (its own adapter, layer 0)"},
-            "tokens_per_s": round(1.0 / per, 2),
-            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1,
+                       "tokens": M, "calls_per_step": n_calls,
+                       "step": f"one layer sweep: the whole batch through {n_calls} oracle "
+                               f"calls (fp64; layers alternate over {layers} weight layers), "
+                               "each split over the host cores"},
+            "tokens_per_s": round(M * n_calls / per, 2),
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": len(parts),
                              "kind": "oracle",
-                             "sample": f"{args.steps} single-token oracle_lora_apply calls "
-                                       f"(fp64, 1 thread) cycling over the {w.name} batch"},
+                             "sample": f"{args.steps} steps of {n_calls} oracle_lora_apply "
+                                       f"calls on the {w.name} batch, {len(parts)} threads over "
+                                       "disjoint segment ranges"},
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def main():
+def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100000)
-    ap.add_argument("--warmup", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_distinct", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config sweep of every named workload")
+    ap.add_argument("--config-seconds", type=float, default=0.4,
+                    help="timed seconds per per_config measurement")
     ap.add_argument("--tensor-cores", choices=["auto", "never", "always"], default="auto",
                     help="which adapter groups use the tensor cores (lora_apply_ex flags)")
     ap.add_argument("--long-batch", choices=["auto", "on", "off"], default="auto",
@@ -520,9 +707,17 @@ def main():
                          "(lora_apply_strided; the e2e figure stays on dense copies)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain lora_apply launches (no programmatic dependent launch)")
-    args = ap.parse_args()
+    argv = sys.argv[1:] if argv is None else argv
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" in os.environ:
+        if int(os.environ["WORLD_SIZE"]) != args.gpus:
+            ap.error(f"--gpus {args.gpus} disagrees with WORLD_SIZE={os.environ['WORLD_SIZE']}")
+    elif args.gpus > 1:  # one process per GPU: re-launch with N local ranks
+        sys.exit(subprocess.call(relaunch_cmd(argv, args.gpus)))
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -245,7 +245,9 @@ class PreparedApply:
                      self.ss.ctypes.data, self.sa.ctypes.data, len(self.sa), int(layer_idx),
                      self.x.shape[1], self.y.shape[1], _rank(A_blocks), float(scale))
 
-    def __call__(self):
-        rc = self._lib.oracle_lora_apply(*self.args)
+    def __call__(self, layer_idx=None):
+        args = self.args if layer_idx is None else (
+            self.args[:7] + (int(layer_idx),) + self.args[8:])
+        rc = self._lib.oracle_lora_apply(*args)
         if rc != 0:
             raise MemoryError("oracle_lora_apply failed")
