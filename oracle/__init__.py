@@ -116,6 +116,8 @@ class OracleLib:
         lib.oracle_validate.restype = ctypes.c_int32
         lib.oracle_validate_pointers.argtypes = [dp, dp, dp, dp, i32, i32]
         lib.oracle_validate_pointers.restype = ctypes.c_int32
+        lib.oracle_plan.argtypes = [dp, dp, i32, i32, dp, dp, dp]
+        lib.oracle_plan.restype = ctypes.c_int32
         self.lib = lib
         self.path = lib_path
 
@@ -192,6 +194,23 @@ class OracleLib:
                                                      int(num_adapters)))
 
 
+    def plan(self, seg_starts, seg_adapter, max_rows):
+        """The adapter grouping of a table: (g_starts[G+1], g_adapter[G], rows[n]) as int32
+        arrays, or None when more than max_rows rows would be listed."""
+        ss, sa = _i32(seg_starts), _i32(seg_adapter)
+        if len(ss) != len(sa) + 1:
+            raise ValueError("seg_starts must hold num_segments + 1 offsets")
+        S = len(sa)
+        gs = np.zeros(S + 1, np.int32)
+        ga = np.zeros(max(S, 1), np.int32)
+        rows = np.zeros(max(int(max_rows), 1), np.int32)
+        G = int(self.lib.oracle_plan(ss.ctypes.data, sa.ctypes.data, S, int(max_rows),
+                                     gs.ctypes.data, ga.ctypes.data, rows.ctypes.data))
+        if G < 0:
+            return None
+        return gs[:G + 1].copy(), ga[:G].copy(), rows[:gs[G]].copy()
+
+
 def _load() -> OracleLib:
     global _lib
     with _lock:
@@ -220,11 +239,16 @@ def validate_pointers(*args, **kw):
     return _load().validate_pointers(*args, **kw)
 
 
+def plan(*args, **kw):
+    return _load().plan(*args, **kw)
+
+
 lora_apply.__doc__ = OracleLib.lora_apply.__doc__
 sgmv_shrink.__doc__ = OracleLib.sgmv_shrink.__doc__
 sgmv_expand.__doc__ = OracleLib.sgmv_expand.__doc__
 validate.__doc__ = OracleLib.validate.__doc__
 validate_pointers.__doc__ = OracleLib.validate_pointers.__doc__
+plan.__doc__ = OracleLib.plan.__doc__
 
 
 class PreparedApply:

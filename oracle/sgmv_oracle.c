@@ -164,3 +164,39 @@ int32_t oracle_validate_pointers(const uint64_t *A_addr, const uint64_t *B_addr,
     }
     return bits;
 }
+
+/* The adapter grouping that a plan of the table holds ("Punica Guide: Multi-Tenant LoRA Serving
+ * with SGMV", section "Hardware-Level Optimizations in SGMV": segment descriptors pre-sorted so
+ * that each adapter's weights are streamed once; section "Mathematical Modeling: Throughput
+ * Scaling and Kernel Launch Bounds", part 2: the work list is built once and reused by every
+ * layer's launches).  Groups are the distinct adapter ids >= 0 of non-empty segments, in the
+ * order of their first segment; a group's rows are its segments' rows, segment after segment,
+ * each segment's rows in increasing order.  Writes g_starts[G+1] (row offsets of the groups in
+ * rows[]), g_adapter[G] and rows[] (token indices); returns G, or -1 when more than max_rows
+ * rows would be listed. */
+int32_t oracle_plan(const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,
+                    int32_t max_rows, int32_t *g_starts, int32_t *g_adapter, int32_t *rows)
+{
+    int32_t G = 0, n = 0;
+    for (int32_t i = 0; i < num_segments; ++i) {
+        const int32_t k = seg_adapter[i];
+        if (k < 0 || seg_starts[i + 1] <= seg_starts[i]) continue;
+        int32_t seen = 0;
+        for (int32_t g = 0; g < G; ++g)
+            if (g_adapter[g] == k) seen = 1;
+        if (seen) continue;
+        /* first segment of adapter k: collect every segment of k from here on, in order */
+        g_adapter[G] = k;
+        g_starts[G] = n;
+        for (int32_t j = i; j < num_segments; ++j) {
+            if (seg_adapter[j] != k) continue;
+            for (int32_t t = seg_starts[j]; t < seg_starts[j + 1]; ++t) {
+                if (n >= max_rows) return -1;
+                rows[n++] = t;
+            }
+        }
+        ++G;
+    }
+    g_starts[G] = n;
+    return G;
+}

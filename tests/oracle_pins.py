@@ -249,7 +249,40 @@ def check_validate_pointers(o):
     assert o.validate_pointers(good, good, [0], [], 4) == 0                      # no segments
 
 
+def check_plan(o):
+    """The grouping: hand-worked tables, and on random tables the invariants that fix it --
+    every row of a non-empty segment with an adapter listed exactly once, under its adapter,
+    groups in order of first appearance, rows of a group in segment order then row order."""
+    # segment 0 (rows 0,1) and segment 3 (rows 3..6) use adapter 5, segment 1 (row 2) adapter 1,
+    # segment 2 is empty, segment 4 has no adapter
+    gs, ga, rows = o.plan([0, 2, 3, 3, 7, 8], [5, 1, 4, 5, -1], 100)
+    assert ga.tolist() == [5, 1] and gs.tolist() == [0, 6, 7]
+    assert rows.tolist() == [0, 1, 3, 4, 5, 6, 2]
+    assert o.plan([0, 2, 3, 3, 7, 8], [5, 1, 4, 5, -1], 6) is None      # 7 rows > 6
+    gs, ga, rows = o.plan([0], [], 0)
+    assert gs.tolist() == [0] and len(ga) == 0 and len(rows) == 0
+    gs, ga, rows = o.plan([4, 9], [0], 5)                               # rows need not start at 0
+    assert ga.tolist() == [0] and rows.tolist() == [4, 5, 6, 7, 8]
+    rng = np.random.default_rng(11)
+    for _ in range(40):
+        S = int(rng.integers(1, 60))
+        lens = rng.integers(0, 5, size=S)
+        ss = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        sa = rng.integers(-1, 8, size=S).astype(np.int32)
+        gs, ga, rows = o.plan(ss, sa, int(ss[-1]))
+        want = sorted(t for i in range(S) if sa[i] >= 0 for t in range(ss[i], ss[i + 1]))
+        assert sorted(rows.tolist()) == want                            # each row exactly once
+        firsts = []
+        for i in range(S):
+            if sa[i] >= 0 and lens[i] > 0 and sa[i] not in firsts:
+                firsts.append(int(sa[i]))
+        assert ga.tolist() == firsts                                    # order of first use
+        for g, k in enumerate(ga):
+            expect = [t for i in range(S) if sa[i] == k for t in range(ss[i], ss[i + 1])]
+            assert rows[gs[g]:gs[g + 1]].tolist() == expect
+
+
 ALL_CHECKS = [check_hand_example, check_merged_weights, check_per_request_gemv,
               check_single_adapter_dense, check_zero_adapter, check_permutation,
               check_brute_force, check_layer_selection, check_shrink_expand,
-              check_untouched_rows, check_validate, check_validate_pointers]
+              check_untouched_rows, check_validate, check_validate_pointers, check_plan]

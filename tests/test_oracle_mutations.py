@@ -36,6 +36,11 @@ MUTATIONS = [
      ") continue;", None),
     ("pointer_check_b_alignment_dropped", "B_addr[k] == 0 || B_addr[k] % 16 != 0",
      "B_addr[k] == 0", None),
+    ("plan_groups_empty_segments",
+     "if (k < 0 || seg_starts[i + 1] <= seg_starts[i]) continue;\n        int32_t seen",
+     "if (k < 0) continue;\n        int32_t seen", None),
+    ("plan_rows_reversed", "rows[n++] = t;",
+     "rows[n++] = seg_starts[j + 1] - 1 - (t - seg_starts[j]);", None),
 ]
 
 
