@@ -53,6 +53,7 @@
 #ifndef SGMV_GB300_H
 #define SGMV_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -74,7 +75,8 @@ typedef enum {
     SGMV_EALIGN = -2,        /* pointer not 16-byte aligned, h_in/h_out not multiples of 8  */
     SGMV_EUNSUPPORTED = -3,  /* rank not in {8,16,32,64}, sizes past the documented limits  */
     SGMV_ECUDA = -4,         /* a CUDA runtime call or launch failed                        */
-    SGMV_ETIMEOUT = -5       /* a bounded device-side wait ran out (see sgmv_get_error)     */
+    SGMV_ETIMEOUT = -5,      /* a bounded device-side wait ran out (see sgmv_get_error)     */
+    SGMV_EPLAN = -6          /* a planned call read an invalid plan (see sgmv_get_error)    */
 } sgmv_status_t;
 
 /* Largest num_segments one call accepts (the segment table is staged on chip). */
@@ -83,6 +85,8 @@ typedef enum {
 #define SGMV_MAX_HIDDEN 65536
 /* Largest row stride (elements) of x or y that the _strided entry points accept. */
 #define SGMV_MAX_LD (1 << 24)
+/* Largest number of projections of one lora_apply_multi call. */
+#define SGMV_MAX_PROJECTIONS 4
 
 /*
  * lora_apply -- the fused path: y[t] += scale * (x[t] . A_k) . B_k for every segment row.
@@ -243,6 +247,106 @@ int sgmv_expand_strided(void *y, int32_t ldy, const float *v, const void *const 
                         float scale, sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream);
 
 /*
+ * ---- Plans: the segment table grouped once, reused by every layer and projection ----------
+ * Source: section "Mathematical Modeling: Throughput Scaling and Kernel Launch Bounds", part 2
+ * (every layer's adapter work in a fixed number of launches) and section "Hardware-Level
+ * Optimizations in SGMV" (segment descriptors pre-sorted by adapter so that each adapter's
+ * weights are streamed once).  The grouping of a batch's table by adapter does not depend on
+ * the layer or on the projection; the unplanned calls above redo it in every CTA of every call.
+ * sgmv_plan does it once, on the device, into a buffer the caller owns; the *_planned calls and
+ * lora_apply_multi read it instead of the table.
+ *
+ * Plan contents (int32 words; the buffer is opaque to callers but its layout is fixed):
+ * a 16-word header (magic, status, num_segments, groups G, rows listed, max_rows), the group
+ * row offsets [num_segments + 1], the group adapters [num_segments] and the row list
+ * [max_rows].  Groups are the distinct adapter ids >= 0 of the non-empty segments, in the
+ * order of their first segment; a group's rows are its segments' rows, segment after segment.
+ * Negative ids and empty segments are dropped (their rows are never touched).
+ */
+
+/* Bytes of a plan for a table of num_segments segments holding at most max_rows rows (0 for
+ * negative sizes or num_segments > SGMV_MAX_SEGMENTS). */
+size_t sgmv_plan_size(int32_t num_segments, int32_t max_rows);
+
+/*
+ * sgmv_plan -- groups the device segment table into `plan` (one kernel launch of one CTA,
+ * asynchronous on `stream`).
+ *   seg_starts, seg_adapter  in   device table as for lora_apply (validate untrusted tables
+ *                                 first: decreasing offsets count as empty segments here)
+ *   num_segments                  0 <= num_segments <= SGMV_MAX_SEGMENTS
+ *   max_rows                      capacity of the row list (>= the rows of the table that have
+ *                                 an adapter; the caller knows M and passes it)
+ *   plan                     out  device buffer of plan_bytes >= sgmv_plan_size(), 16-byte
+ *                                 aligned, owned by the caller; valid until overwritten
+ * A table with more than max_rows rows yields a plan marked invalid (status word 1): every
+ * planned call that reads it returns without touching y or v and sets the library's device
+ * error word to SGMV_EPLAN.  Returns SGMV_OK, SGMV_EINVAL (null pointers, negative sizes,
+ * plan_bytes too small), SGMV_EALIGN, SGMV_EUNSUPPORTED or SGMV_ECUDA.
+ * Ordering: a planned call launched with SGMV_OVERLAP_PRIOR reads the plan before it waits for
+ * the kernel enqueued just before it, so that kernel must not be the sgmv_plan that writes the
+ * plan (the same rule as for the segment table); without the flag any order on one stream is
+ * fine.
+ */
+int sgmv_plan(const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,
+              int32_t max_rows, void *plan, size_t plan_bytes, sgmv_stream_t stream);
+
+/*
+ * lora_apply_planned -- lora_apply_strided with the segment table replaced by a plan.
+ *   plan           in   from sgmv_plan (device, 16-byte aligned)
+ *   num_segments        the num_segments the plan was built with (its capacity; checked
+ *                       against the plan on the device: a mismatch is SGMV_EPLAN)
+ * Other arguments, flags, layout and errors: as for lora_apply_strided (x and y rows ldx and
+ * ldy elements apart; ldx = h_in and ldy = h_out for dense activations).  The results equal
+ * the unplanned call's within rounding (the same routing rule and chunking; the rows of a group
+ * are visited in the plan's order).
+ */
+int lora_apply_planned(void *y, int32_t ldy, const void *x, int32_t ldx,
+                       const void *const *A_ptrs, const void *const *B_ptrs, const void *plan,
+                       int32_t num_segments, int32_t layer_idx, int32_t h_in, int32_t h_out,
+                       int32_t r, float scale, sgmv_dtype_t dtype, uint32_t flags,
+                       sgmv_stream_t stream);
+
+/* sgmv_shrink_strided with a plan (arguments as for lora_apply_planned). */
+int sgmv_shrink_planned(float *v, const void *x, int32_t ldx, const void *const *A_ptrs,
+                        const void *plan, int32_t num_segments, int32_t layer_idx, int32_t h_in,
+                        int32_t r, sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream);
+
+/* sgmv_expand_strided with a plan (arguments as for lora_apply_planned). */
+int sgmv_expand_planned(void *y, int32_t ldy, const float *v, const void *const *B_ptrs,
+                        const void *plan, int32_t num_segments, int32_t layer_idx, int32_t r,
+                        int32_t h_out, float scale, sgmv_dtype_t dtype, uint32_t flags,
+                        sgmv_stream_t stream);
+
+/* One projection of lora_apply_multi: the arguments of lora_apply_planned that differ between
+ * projections (device pointers; ldx / ldy in elements). */
+typedef struct {
+    void *y;
+    const void *x;
+    const void *const *A_ptrs;
+    const void *const *B_ptrs;
+    int32_t ldy, ldx;
+    int32_t h_in, h_out;
+    float scale;
+    int32_t reserved;  /* 0 */
+} sgmv_projection_t;
+
+/*
+ * lora_apply_multi -- the fused LoRA term of up to SGMV_MAX_PROJECTIONS projections of one
+ * layer (for example q, k and v of an attention block, or gate and up of an MLP) in ONE
+ * kernel launch over one plan: proj[q] gets y_q[t] += scale_q * (x_q[t] . A_{q,k}) . B_{q,k}.
+ * Each projection has its own x, y, weights, h_in, h_out and scale; all share the plan (the
+ * batch), the layer, the rank r and the element type.  The grid is divided between the
+ * projections in proportion to an estimate of their bytes.  proj is a HOST array of num_proj
+ * entries, read during the call.  Projections must not write overlapping y rows.
+ * Flags, layout and errors as for lora_apply_planned (SGMV_EUNSUPPORTED when num_proj >
+ * SGMV_MAX_PROJECTIONS).  Each projection's result equals lora_apply_planned's on its own
+ * within rounding.
+ */
+int lora_apply_multi(const sgmv_projection_t *proj, int32_t num_proj, const void *plan,
+                     int32_t num_segments, int32_t layer_idx, int32_t r, sgmv_dtype_t dtype,
+                     uint32_t flags, sgmv_stream_t stream);
+
+/*
  * sgmv_validate -- checks a segment table on the device and writes an OR of these bits to
  * *d_err (device int32, overwritten; 0 = valid):
  *   1  seg_starts decreases somewhere          2  seg_starts[0] < 0
@@ -283,7 +387,7 @@ int sgmv_validate_pointers(const void *const *A_ptrs, const void *const *B_ptrs,
 
 /*
  * sgmv_get_error -- synchronises `stream`, copies the current device's library error word to
- * *host_err (a host int32: 0 or a negative sgmv_status_t such as SGMV_ETIMEOUT) and, when
+ * *host_err (a host int32: 0 or a negative sgmv_status_t: SGMV_ETIMEOUT, SGMV_EPLAN) and, when
  * clear != 0, resets it to 0.  Returns SGMV_OK or SGMV_ECUDA.
  */
 int sgmv_get_error(int32_t *host_err, int32_t clear, sgmv_stream_t stream);

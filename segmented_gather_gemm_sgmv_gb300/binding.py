@@ -17,6 +17,9 @@ _lock = threading.Lock()
 _lib = None
 
 SGMV_OK, SGMV_EINVAL, SGMV_EALIGN, SGMV_EUNSUPPORTED, SGMV_ECUDA, SGMV_ETIMEOUT = 0, -1, -2, -3, -4, -5
+SGMV_EPLAN = -6
+SGMV_MAX_PROJECTIONS = 4
+PLAN_HEADER = 16  # int32 words before a plan's group table (include/sgmv.h)
 SGMV_MAX_SEGMENTS = 4096
 SGMV_MAX_HIDDEN = 65536
 SGMV_OVERLAP_PRIOR = 1
@@ -27,7 +30,16 @@ SGMV_MAX_LD = 1 << 24
 SYMBOLS = ("lora_apply", "lora_apply_ex", "lora_apply_strided", "sgmv_shrink", "sgmv_shrink_ex",
            "sgmv_shrink_strided", "sgmv_expand", "sgmv_expand_ex", "sgmv_expand_strided",
            "sgmv_validate", "sgmv_validate_pointers", "sgmv_get_error", "sgmv_set_wait_limit",
-           "sgmv_status_string", "sgmv_version")
+           "sgmv_status_string", "sgmv_version", "sgmv_plan_size", "sgmv_plan",
+           "lora_apply_planned", "sgmv_shrink_planned", "sgmv_expand_planned", "lora_apply_multi")
+
+
+class Projection(ctypes.Structure):
+    """sgmv_projection_t of include/sgmv.h."""
+    _fields_ = [("y", ctypes.c_void_p), ("x", ctypes.c_void_p), ("A_ptrs", ctypes.c_void_p),
+                ("B_ptrs", ctypes.c_void_p), ("ldy", ctypes.c_int32), ("ldx", ctypes.c_int32),
+                ("h_in", ctypes.c_int32), ("h_out", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("reserved", ctypes.c_int32)]
 
 
 class SgmvError(RuntimeError):
@@ -68,13 +80,24 @@ def lib(build_if_stale: bool = True) -> ctypes.CDLL:
                                           ctypes.c_int, ctypes.c_uint32, vp]
         L.sgmv_validate.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         L.sgmv_validate_pointers.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp]
+        u32, ci = ctypes.c_uint32, ctypes.c_int
+        L.sgmv_plan_size.argtypes = [i32, i32]
+        L.sgmv_plan_size.restype = ctypes.c_size_t
+        L.sgmv_plan.argtypes = [vp, vp, i32, i32, vp, ctypes.c_size_t, vp]
+        L.lora_apply_planned.argtypes = [vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32,
+                                         f32, ci, u32, vp]
+        L.sgmv_shrink_planned.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, i32, ci, u32, vp]
+        L.sgmv_expand_planned.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, i32, f32, ci, u32,
+                                          vp]
+        L.lora_apply_multi.argtypes = [ctypes.POINTER(Projection), i32, vp, i32, i32, i32, ci,
+                                       u32, vp]
         L.sgmv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
         L.sgmv_set_wait_limit.argtypes = [ctypes.c_uint64, i32]
         L.sgmv_status_string.argtypes = [ctypes.c_int]
         L.sgmv_status_string.restype = ctypes.c_char_p
         L.sgmv_version.argtypes = []
         for name in SYMBOLS:
-            if name != "sgmv_status_string":
+            if name not in ("sgmv_status_string", "sgmv_plan_size"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
         return L
@@ -328,3 +351,136 @@ def sgmv_set_wait_limit(limit_ns: int, inject_stall: bool = False):
 
 def sgmv_version() -> int:
     return int(lib().sgmv_version())
+
+
+# ---------------------------------------------------------------------------- plans ----
+class Plan:
+    """A device plan (sgmv_plan): the segment table grouped by adapter once, for reuse by
+    every planned call of the batch.  `buf` is the caller-side device allocation (torch int32);
+    num_segments is the plan's capacity, which every planned call passes back."""
+
+    def __init__(self, buf, num_segments, max_rows):
+        self.buf = buf
+        self.num_segments = int(num_segments)
+        self.max_rows = int(max_rows)
+
+    @property
+    def device(self):
+        return self.buf.device
+
+    def groups(self):
+        """(g_starts, g_adapter, rows) as host numpy arrays, or None for an invalid plan
+        (synchronises)."""
+        import numpy as np
+        h = self.buf.cpu().numpy()
+        S = self.num_segments
+        if int(h[1]) != 0:
+            return None
+        G, n = int(h[3]), int(h[4])
+        gs = h[PLAN_HEADER:PLAN_HEADER + G + 1].astype(np.int32)
+        ga = h[PLAN_HEADER + S + 1:PLAN_HEADER + S + 1 + G].astype(np.int32)
+        rows = h[PLAN_HEADER + 2 * S + 1:PLAN_HEADER + 2 * S + 1 + n].astype(np.int32)
+        return gs, ga, rows
+
+
+def sgmv_plan_size(num_segments, max_rows) -> int:
+    return int(lib().sgmv_plan_size(int(num_segments), int(max_rows)))
+
+
+def sgmv_plan(seg_starts, seg_adapter, max_rows, stream=None, out=None) -> Plan:
+    """Groups the device segment table by adapter into a plan (a torch int32 device buffer the
+    binding allocates unless `out` is given); max_rows: capacity of the row list (>= the rows
+    with an adapter, e.g. M)."""
+    import torch
+    S = _table(seg_starts, seg_adapter)
+    nbytes = sgmv_plan_size(S, max_rows)
+    if nbytes == 0:
+        raise ValueError("bad plan size arguments")
+    if out is None:
+        out = torch.empty((nbytes + 3) // 4, dtype=torch.int32, device=seg_starts.device)
+    _cuda(out, "out")
+    with _on(seg_starts, seg_adapter, out):
+        rc = lib().sgmv_plan(seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(max_rows),
+                             out.data_ptr(), out.numel() * out.element_size(),
+                             _stream(stream, seg_starts.device))
+    _check(rc, "sgmv_plan")
+    return Plan(out, S, max_rows)
+
+
+def lora_apply_planned(y, x, A_ptrs, B_ptrs, plan: Plan, layer_idx, r, scale, stream=None,
+                       overlap_prior=False, tensor_cores="auto", long_batch=False):
+    """lora_apply with a plan instead of the segment table (x, y may be column slices)."""
+    ldy, ldx = _rows(y, "y"), _rows(x, "x")
+    if x.dtype != y.dtype or x.shape[0] != y.shape[0]:
+        raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
+    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    with _on(x, y, A_ptrs, B_ptrs, plan.buf):
+        rc = lib().lora_apply_planned(
+            y.data_ptr(), ldy, x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
+            plan.buf.data_ptr(), plan.num_segments, int(layer_idx), x.shape[1], y.shape[1],
+            int(r), float(scale), _dtype_code(x), flags, _stream(stream, x.device))
+    _check(rc, "lora_apply_planned")
+    return y
+
+
+def sgmv_shrink_planned(v, x, A_ptrs, plan: Plan, layer_idx, r, stream=None,
+                        tensor_cores="auto", long_batch=False, overlap_prior=False):
+    import torch
+    _cuda(v, "v")
+    ldx = _rows(x, "x")
+    if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != x.shape[0]:
+        raise ValueError("v must be float32 [M, r]")
+    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    with _on(x, v, A_ptrs, plan.buf):
+        rc = lib().sgmv_shrink_planned(v.data_ptr(), x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"),
+                                       plan.buf.data_ptr(), plan.num_segments, int(layer_idx),
+                                       x.shape[1], int(r), _dtype_code(x), flags,
+                                       _stream(stream, x.device))
+    _check(rc, "sgmv_shrink_planned")
+    return v
+
+
+def sgmv_expand_planned(y, v, B_ptrs, plan: Plan, layer_idx, r, scale, stream=None,
+                        tensor_cores="auto", long_batch=False, overlap_prior=False):
+    import torch
+    _cuda(v, "v")
+    ldy = _rows(y, "y")
+    if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != y.shape[0]:
+        raise ValueError("v must be float32 [M, r]")
+    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    with _on(y, v, B_ptrs, plan.buf):
+        rc = lib().sgmv_expand_planned(y.data_ptr(), ldy, v.data_ptr(), _ptrs(B_ptrs, "B_ptrs"),
+                                       plan.buf.data_ptr(), plan.num_segments, int(layer_idx),
+                                       int(r), y.shape[1], float(scale), _dtype_code(y), flags,
+                                       _stream(stream, y.device))
+    _check(rc, "sgmv_expand_planned")
+    return y
+
+
+def lora_apply_multi(projections, plan: Plan, layer_idx, r, stream=None, overlap_prior=False,
+                     tensor_cores="auto", long_batch=False):
+    """One launch over several projections: projections is a list of
+    (y, x, A_ptrs, B_ptrs, scale) tuples sharing the plan, layer, rank and dtype."""
+    if not 1 <= len(projections) <= SGMV_MAX_PROJECTIONS:
+        raise ValueError(f"1 to {SGMV_MAX_PROJECTIONS} projections")
+    arr = (Projection * len(projections))()
+    dt = None
+    tensors = []
+    for q, (y, x, A_ptrs, B_ptrs, scale) in enumerate(projections):
+        ldy, ldx = _rows(y, "y"), _rows(x, "x")
+        if x.dtype != y.dtype or x.shape[0] != y.shape[0]:
+            raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
+        if dt is not None and x.dtype != dt:
+            raise ValueError("all projections share one dtype")
+        dt = x.dtype
+        arr[q] = Projection(y.data_ptr(), x.data_ptr(), _ptrs(A_ptrs, "A_ptrs"),
+                            _ptrs(B_ptrs, "B_ptrs"), ldy, ldx, x.shape[1], y.shape[1],
+                            float(scale), 0)
+        tensors += [y, x, A_ptrs, B_ptrs]
+    x0 = projections[0][1]
+    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    with _on(x0, plan.buf, *tensors):
+        rc = lib().lora_apply_multi(arr, len(projections), plan.buf.data_ptr(), plan.num_segments,
+                                    int(layer_idx), int(r), _dtype_code(x0), flags,
+                                    _stream(stream, x0.device))
+    _check(rc, "lora_apply_multi")

@@ -42,7 +42,9 @@ struct DeviceState {
   int* err = nullptr;
   std::atomic<uint64_t> wait_ns{kDefaultWaitNs};
   std::atomic<int> inject{0};
-  KernelCache cache[3][3][4][2];  // dtype, mode, rank index, geometry (SGMV_LONG_BATCH); g_mu
+  // dtype, mode (fused, shrink, expand, multi-projection fused), rank index, geometry
+  // (SGMV_LONG_BATCH); guarded by g_mu
+  KernelCache cache[3][4][4][2];
 };
 
 std::mutex g_mu;  // guards the kernel caches
@@ -144,6 +146,15 @@ const void* kernel_for(int dtype, int mode, int r, bool wide) {
     case SGMV_F32: return sgmv::kernel_f32(mode, r, wide);
     case SGMV_F16: return sgmv::kernel_f16(mode, r, wide);
     case SGMV_BF16: return sgmv::kernel_bf16(mode, r, wide);
+    default: return nullptr;
+  }
+}
+
+const void* multi_kernel_for(int dtype, int r, bool wide) {
+  switch (dtype) {
+    case SGMV_F32: return sgmv::kernel_multi_f32(r, wide);
+    case SGMV_F16: return sgmv::kernel_multi_f16(r, wide);
+    case SGMV_BF16: return sgmv::kernel_multi_bf16(r, wide);
     default: return nullptr;
   }
 }
@@ -263,14 +274,19 @@ int plan_geometry(const Problem& pb, size_t budget, sgmv::Params& p, size_t* sme
   return SGMV_OK;
 }
 
-int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stream) {
-  DeviceState* st = nullptr;
-  int rc = device_state(&st);
-  if (rc != SGMV_OK) return rc;
+// ---- launch set-up, shared by the single, planned and multi-projection entry points ----
+
+bool tensor_capable(const Problem& pb, uint32_t flags) {
+  return pb.dtype != SGMV_F32 && pb.r >= 16 && !(flags & SGMV_NO_TENSOR_CORES);
+}
+
+// Shared-memory layout and the per-problem kernel parameters that do not depend on the grid.
+// Returns the bytes of dynamic shared memory this problem needs in this geometry.
+int setup_problem(const DeviceState* st, const Problem& pb, sgmv::Params& p, uint32_t flags,
+                  size_t* smem_out) {
+  const size_t budget = (flags & SGMV_LONG_BATCH) ? kMaxSmem : kPairSmem;
   size_t smem = 0;
-  const bool wide = (flags & SGMV_LONG_BATCH) != 0;
-  const size_t budget = wide ? kMaxSmem : kPairSmem;
-  rc = plan_geometry(pb, budget, p, &smem);
+  int rc = plan_geometry(pb, budget, p, &smem);
   if (rc == SGMV_EUNSUPPORTED) rc = plan_geometry(pb, kMaxSmem, p, &smem);
   if (rc != SGMV_OK) return rc;
   p.err = st->err;
@@ -281,81 +297,80 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   p.scale = pb.scale;
   p.wait_limit_ns = st->wait_ns.load(std::memory_order_relaxed);
   p.inject_stall = st->inject.load(std::memory_order_relaxed);
-
-  // The 416-thread kernel (a second tensor-role epilogue warpgroup) measured faster where the
-  // tensor role dominates (prefill_mixed, 8 segments: 61.1 -> 58.3 us) and slower on the
-  // CUDA-core role (the 70B mix, 482 segments: 101.0 -> 105.6 us); a table of many segments
-  // means many decode rows, so those keep the 288-thread kernel.
-  const bool wide_kernel = wide && pb.S <= kWideMaxSegments;
-  const void* fn = kernel_for(pb.dtype, pb.mode, pb.r, wide_kernel);
-  const int threads = wide_kernel ? sgmv::kThreadsWide : sgmv::kThreads;
-  if (!fn) return SGMV_EUNSUPPORTED;
-  const bool clustered = pb.mode != sgmv::kExpand;
   // Tensor role (16-bit types, r >= 16; every mode): it uses none of the CUDA-core scratch
   // areas, so its row table sits at off_vpart and its ring of 24 KB slots right after it, up to
   // the end of the budget (the launch then always takes the whole budget).
-  const uint32_t tc_base = static_cast<uint32_t>(
+  p.tc_base = static_cast<uint32_t>(
       up(p.off_vpart + (2 * sgmv::kTcRows + 4) * sizeof(int), 1024));
-  const bool tc_capable = pb.dtype != SGMV_F32 && pb.r >= 16 && !(flags & SGMV_NO_TENSOR_CORES);
-  if (tc_capable && smem <= budget) smem = budget;  // the tensor ring takes the whole budget
-  int grid = 0;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    KernelCache& kc = st->cache[pb.dtype][pb.mode][rank_index(pb.r)][wide_kernel ? 1 : 0];
-    if (kc.smem_set < smem) {
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem)) != cudaSuccess)
-        return SGMV_ECUDA;
-      if (clustered && p.C > 8 &&
-          cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-              cudaSuccess)
-        return SGMV_ECUDA;
-      kc.smem_set = smem;
-    }
-    if (kc.cluster != p.C || kc.smem_q != smem) {
-      int n = 0;
-      if (clustered) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        cfg.gridDim = dim3(static_cast<unsigned>(p.C * st->sms), 1, 1);
-        cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
-        cfg.dynamicSmemBytes = smem;
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) return SGMV_ECUDA;
-      } else {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) !=
-            cudaSuccess)
-          return SGMV_ECUDA;
-        n = per_sm * st->sms / p.C;
-      }
-      n = std::min(n, std::max(1, st->sms / p.C));  // one CTA per SM per kernel
-      if (n <= 0) return SGMV_EUNSUPPORTED;
-      kc.cluster = p.C;
-      kc.smem_q = smem;
-      kc.max_clusters = n;
-    }
-    grid = kc.max_clusters * p.C;
-  }
+  if (tensor_capable(pb, flags) && smem <= budget) smem = budget;
+  *smem_out = smem;
+  return SGMV_OK;
+}
 
-  // Tensor role: at least three ring slots and two clusters in the grid.
+// Clusters of C CTAs that fit at once for this kernel and shared-memory size (one CTA per SM
+// per kernel), cached per instantiation.  Also sets the kernel's attributes.
+int grid_for(DeviceState* st, KernelCache& kc, const void* fn, int threads, size_t smem,
+             bool clustered, int C, int* grid) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (kc.smem_set < smem) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return SGMV_ECUDA;
+    if (clustered && C > 8 &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+      return SGMV_ECUDA;
+    kc.smem_set = smem;
+  }
+  if (kc.cluster != C || kc.smem_q != smem) {
+    int n = 0;
+    if (clustered) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      cfg.gridDim = dim3(static_cast<unsigned>(C * st->sms), 1, 1);
+      cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) return SGMV_ECUDA;
+    } else {
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) !=
+          cudaSuccess)
+        return SGMV_ECUDA;
+      n = per_sm * st->sms / C;
+    }
+    n = std::min(n, std::max(1, st->sms / C));  // one CTA per SM per kernel
+    if (n <= 0) return SGMV_EUNSUPPORTED;
+    kc.cluster = C;
+    kc.smem_q = smem;
+    kc.max_clusters = n;
+  }
+  *grid = kc.max_clusters * C;
+  return SGMV_OK;
+}
+
+// The grid-dependent part of a problem's parameters: its CTA range and the tensor role (ring
+// slots, tensor maps, routing threshold), which needs at least two clusters and three slots.
+int finish_problem(const Problem& pb, sgmv::Params& p, uint32_t flags, size_t smem, int cta0,
+                   int nctas, bool wide_kernel) {
+  p.cta0 = cta0;
+  p.nctas = nctas;
   p.tc_min_rows = 0x7fffffff;
   p.tc_slots = 0;
-  p.tc_base = tc_base;
   const size_t xchg = pb.mode != sgmv::kExpand ? sgmv::kTcXchgBytes : 0;  // split-K buffers
-  if (tc_capable && grid >= 2 * p.C && smem > tc_base + xchg) {
-    int slots = std::min<int>(static_cast<int>((smem - tc_base - xchg) / sgmv::kTcSlot),
+  if (tensor_capable(pb, flags) && nctas >= 2 * p.C && smem > p.tc_base + xchg) {
+    int slots = std::min<int>(static_cast<int>((smem - p.tc_base - xchg) / sgmv::kTcSlot),
                               (2 * kMaxStages + sgmv::kNumFixedBars - sgmv::kTcNumFixed) / 2);
     // Two epilogue groups take alternate n-tiles: with an even slot count the previous use of
     // every slot within an m-tile belongs to the same group, so no group can wait on a slot
     // whose previous fill (another group's) has not landed yet (parity waits see one phase).
     if (wide_kernel) slots &= ~1;
-    p.tc_xchg = tc_base + static_cast<uint32_t>(slots) * sgmv::kTcSlot;
+    p.tc_xchg = p.tc_base + static_cast<uint32_t>(slots) * sgmv::kTcSlot;
     if (slots >= 3) {
       const bool need_x = pb.mode != sgmv::kExpand, need_y = pb.mode != sgmv::kShrink;
       if ((need_x && (!encode_rows(&p.tmap_x128, p.x, pb.h_in, p.ldx, pb.dtype, 128) ||
@@ -385,7 +400,11 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
       p.tc_slots = slots;
     }
   }
+  return SGMV_OK;
+}
 
+int launch_kernel(const void* fn, int grid, int threads, size_t smem, bool clustered, int C,
+                  uint32_t flags, void* arg, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -395,7 +414,7 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   unsigned na = 0;
   if (clustered) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = static_cast<unsigned>(p.C);
+    attr[na].val.clusterDim.x = static_cast<unsigned>(C);
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;
@@ -407,9 +426,36 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   }
   cfg.attrs = na ? attr : nullptr;
   cfg.numAttrs = na;
-  void* args[] = {&p};
-  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SGMV_ECUDA;
-  return SGMV_OK;
+  void* args[] = {arg};
+  return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? SGMV_OK : SGMV_ECUDA;
+}
+
+// The 416-thread kernel (a second tensor-role epilogue warpgroup) measured faster where the
+// tensor role dominates (prefill_mixed, 8 segments: 61.1 -> 58.3 us) and slower on the
+// CUDA-core role (the 70B mix, 482 segments: 101.0 -> 105.6 us); a table of many segments
+// means many decode rows, so those keep the 288-thread kernel.
+bool use_wide_kernel(const Problem& pb, uint32_t flags) {
+  return (flags & SGMV_LONG_BATCH) && pb.S <= kWideMaxSegments;
+}
+
+// One problem, one launch.
+int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stream) {
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != SGMV_OK) return rc;
+  size_t smem = 0;
+  if ((rc = setup_problem(st, pb, p, flags, &smem)) != SGMV_OK) return rc;
+  const bool wide_kernel = use_wide_kernel(pb, flags);
+  const void* fn = kernel_for(pb.dtype, pb.mode, pb.r, wide_kernel);
+  const int threads = wide_kernel ? sgmv::kThreadsWide : sgmv::kThreads;
+  if (!fn) return SGMV_EUNSUPPORTED;
+  const bool clustered = pb.mode != sgmv::kExpand;
+  int grid = 0;
+  rc = grid_for(st, st->cache[pb.dtype][pb.mode][rank_index(pb.r)][wide_kernel ? 1 : 0], fn,
+                threads, smem, clustered, p.C, &grid);
+  if (rc != SGMV_OK) return rc;
+  if ((rc = finish_problem(pb, p, flags, smem, 0, grid, wide_kernel)) != SGMV_OK) return rc;
+  return launch_kernel(fn, grid, threads, smem, clustered, p.C, flags, &p, stream);
 }
 
 bool flags_ok(uint32_t flags) {
@@ -614,6 +660,192 @@ int sgmv_expand_strided(void* y, int32_t ldy, const float* v, const void* const*
   return launch(pb, p, flags, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ---- planned calls (a plan from sgmv_plan instead of the segment table) ----------------
+
+namespace {
+int check_plan_args(const void* plan, int32_t num_segments) {
+  if (!plan || num_segments < 0) return SGMV_EINVAL;
+  if (num_segments > SGMV_MAX_SEGMENTS) return SGMV_EUNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(plan) & 15u) return SGMV_EALIGN;
+  return SGMV_OK;
+}
+
+// Points the kernel at the plan's group table (one segment per adapter group) and row list.
+void use_plan(sgmv::Params& p, const void* plan, int32_t S) {
+  const int32_t* h = static_cast<const int32_t*>(plan);
+  p.plan_hdr = h;
+  p.seg_starts = h + sgmv::kPlanHeader;
+  p.seg_adapter = h + sgmv::kPlanHeader + S + 1;
+  p.rowmap = h + sgmv::kPlanHeader + 2 * S + 1;
+}
+}  // namespace
+
+int lora_apply_planned(void* y, int32_t ldy, const void* x, int32_t ldx,
+                       const void* const* A_ptrs, const void* const* B_ptrs, const void* plan,
+                       int32_t num_segments, int32_t layer_idx, int32_t h_in, int32_t h_out,
+                       int32_t r, float scale, sgmv_dtype_t dtype, uint32_t flags,
+                       sgmv_stream_t stream) {
+  if (!flags_ok(flags)) return SGMV_EINVAL;
+  int rc = check_plan_args(plan, num_segments);
+  if (rc != SGMV_OK) return rc;
+  if ((rc = check_common(num_segments, plan, plan, layer_idx, r, dtype)) != SGMV_OK) return rc;
+  if (!y || !x || !A_ptrs || !B_ptrs) return SGMV_EINVAL;
+  if ((rc = check_hidden(h_in)) != SGMV_OK || (rc = check_hidden(h_out)) != SGMV_OK) return rc;
+  if ((rc = check_ld(ldx, h_in)) != SGMV_OK || (rc = check_ld(ldy, h_out)) != SGMV_OK) return rc;
+  if (!aligned16(y) || !aligned16(x) || (reinterpret_cast<uintptr_t>(A_ptrs) & 7u) ||
+      (reinterpret_cast<uintptr_t>(B_ptrs) & 7u))
+    return SGMV_EALIGN;
+  if (num_segments == 0) return SGMV_OK;
+  sgmv::Params p = {};
+  p.y = y;
+  p.x = x;
+  p.ldx = ldx;
+  p.ldy = ldy;
+  p.A_ptrs = A_ptrs;
+  p.B_ptrs = B_ptrs;
+  use_plan(p, plan, num_segments);
+  const Problem pb{sgmv::kFused, dtype, r, num_segments, layer_idx, h_in, h_out, scale};
+  return launch(pb, p, flags, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgmv_shrink_planned(float* v, const void* x, int32_t ldx, const void* const* A_ptrs,
+                        const void* plan, int32_t num_segments, int32_t layer_idx, int32_t h_in,
+                        int32_t r, sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream) {
+  if (!flags_ok(flags)) return SGMV_EINVAL;
+  int rc = check_plan_args(plan, num_segments);
+  if (rc != SGMV_OK) return rc;
+  if ((rc = check_common(num_segments, plan, plan, layer_idx, r, dtype)) != SGMV_OK) return rc;
+  if (!v || !x || !A_ptrs) return SGMV_EINVAL;
+  if ((rc = check_hidden(h_in)) != SGMV_OK) return rc;
+  if ((rc = check_ld(ldx, h_in)) != SGMV_OK) return rc;
+  if (!aligned16(v) || !aligned16(x) || (reinterpret_cast<uintptr_t>(A_ptrs) & 7u))
+    return SGMV_EALIGN;
+  if (num_segments == 0) return SGMV_OK;
+  sgmv::Params p = {};
+  p.x = x;
+  p.ldx = ldx;
+  p.ldy = 8;
+  p.v_out = v;
+  p.A_ptrs = A_ptrs;
+  use_plan(p, plan, num_segments);
+  const Problem pb{sgmv::kShrink, dtype, r, num_segments, layer_idx, h_in, 8, 1.0f};
+  return launch(pb, p, flags, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgmv_expand_planned(void* y, int32_t ldy, const float* v, const void* const* B_ptrs,
+                        const void* plan, int32_t num_segments, int32_t layer_idx, int32_t r,
+                        int32_t h_out, float scale, sgmv_dtype_t dtype, uint32_t flags,
+                        sgmv_stream_t stream) {
+  if (!flags_ok(flags)) return SGMV_EINVAL;
+  int rc = check_plan_args(plan, num_segments);
+  if (rc != SGMV_OK) return rc;
+  if ((rc = check_common(num_segments, plan, plan, layer_idx, r, dtype)) != SGMV_OK) return rc;
+  if (!y || !v || !B_ptrs) return SGMV_EINVAL;
+  if ((rc = check_hidden(h_out)) != SGMV_OK) return rc;
+  if ((rc = check_ld(ldy, h_out)) != SGMV_OK) return rc;
+  if (!aligned16(y) || !aligned16(v) || (reinterpret_cast<uintptr_t>(B_ptrs) & 7u))
+    return SGMV_EALIGN;
+  if (num_segments == 0) return SGMV_OK;
+  sgmv::Params p = {};
+  p.y = y;
+  p.ldx = 8;
+  p.ldy = ldy;
+  p.v_in = v;
+  p.B_ptrs = B_ptrs;
+  use_plan(p, plan, num_segments);
+  const Problem pb{sgmv::kExpand, dtype, r, num_segments, layer_idx, 8, h_out, scale};
+  return launch(pb, p, flags, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lora_apply_multi(const sgmv_projection_t* proj, int32_t num_proj, const void* plan,
+                     int32_t num_segments, int32_t layer_idx, int32_t r, sgmv_dtype_t dtype,
+                     uint32_t flags, sgmv_stream_t stream) {
+  if (!flags_ok(flags) || !proj || num_proj < 1) return SGMV_EINVAL;
+  if (num_proj > SGMV_MAX_PROJECTIONS) return SGMV_EUNSUPPORTED;
+  int rc = check_plan_args(plan, num_segments);
+  if (rc != SGMV_OK) return rc;
+  if ((rc = check_common(num_segments, plan, plan, layer_idx, r, dtype)) != SGMV_OK) return rc;
+  for (int q = 0; q < num_proj; ++q) {
+    const sgmv_projection_t& j = proj[q];
+    if (!j.y || !j.x || !j.A_ptrs || !j.B_ptrs) return SGMV_EINVAL;
+    if ((rc = check_hidden(j.h_in)) != SGMV_OK || (rc = check_hidden(j.h_out)) != SGMV_OK)
+      return rc;
+    if ((rc = check_ld(j.ldx, j.h_in)) != SGMV_OK || (rc = check_ld(j.ldy, j.h_out)) != SGMV_OK)
+      return rc;
+    if (!aligned16(j.y) || !aligned16(j.x) || (reinterpret_cast<uintptr_t>(j.A_ptrs) & 7u) ||
+        (reinterpret_cast<uintptr_t>(j.B_ptrs) & 7u))
+      return SGMV_EALIGN;
+  }
+  if (num_segments == 0) return SGMV_OK;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != SGMV_OK) return rc;
+  static_assert(sgmv::kMaxProblems == SGMV_MAX_PROJECTIONS, "projection limit");
+  sgmv::MultiParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  mp.P = num_proj;
+  Problem pbs[sgmv::kMaxProblems];
+  size_t smem = 0;
+  for (int q = 0; q < num_proj; ++q) {
+    const sgmv_projection_t& j = proj[q];
+    sgmv::Params& p = mp.prob[q];
+    p.y = j.y;
+    p.x = j.x;
+    p.ldx = j.ldx;
+    p.ldy = j.ldy;
+    p.A_ptrs = j.A_ptrs;
+    p.B_ptrs = j.B_ptrs;
+    use_plan(p, plan, num_segments);
+    pbs[q] = Problem{sgmv::kFused, dtype, r, num_segments, layer_idx, j.h_in, j.h_out, j.scale};
+    size_t sq = 0;
+    if ((rc = setup_problem(st, pbs[q], p, flags, &sq)) != SGMV_OK) return rc;
+    smem = std::max(smem, sq);
+  }
+  const bool wide_kernel = use_wide_kernel(pbs[0], flags);
+  const void* fn = multi_kernel_for(dtype, r, wide_kernel);
+  if (!fn) return SGMV_EUNSUPPORTED;
+  const int threads = wide_kernel ? sgmv::kThreadsWide : sgmv::kThreads;
+  const int C = mp.prob[0].C;
+  int grid = 0;
+  rc = grid_for(st, st->cache[dtype][3][rank_index(r)][wide_kernel ? 1 : 0], fn, threads, smem,
+                true, C, &grid);
+  if (rc != SGMV_OK) return rc;
+  // Clusters per projection, in proportion to an estimate of its bytes: the weights of an
+  // adapter ((h_in + h_out) r) plus the activations of its rows (h_in + 2 h_out per row; ~4 rows
+  // per adapter, ~128 for SGMV_LONG_BATCH launches), at least one cluster each.
+  const int clusters = grid / C;
+  if (clusters < num_proj) return SGMV_EUNSUPPORTED;
+  const double rows = (flags & SGMV_LONG_BATCH) ? 128.0 : 4.0;
+  double cost[sgmv::kMaxProblems], total = 0.0;
+  for (int q = 0; q < num_proj; ++q) {
+    cost[q] = static_cast<double>(pbs[q].h_in + pbs[q].h_out) * r +
+              rows * (pbs[q].h_in + 2.0 * pbs[q].h_out);
+    total += cost[q];
+  }
+  int share[sgmv::kMaxProblems], given = 0;
+  for (int q = 0; q < num_proj; ++q) {
+    share[q] = std::max(1, static_cast<int>((clusters - num_proj) * cost[q] / total) + 1);
+    given += share[q];
+  }
+  for (int q = 0; given > clusters; q = (q + 1) % num_proj)  // trim (never below one)
+    if (share[q] > 1) {
+      --share[q];
+      --given;
+    }
+  for (int q = 0; given < clusters; q = (q + 1) % num_proj) {  // hand out the remainder
+    ++share[q];
+    ++given;
+  }
+  int cta0 = 0;
+  for (int q = 0; q < num_proj; ++q) {
+    if ((rc = finish_problem(pbs[q], mp.prob[q], flags, smem, cta0, share[q] * C,
+                             wide_kernel)) != SGMV_OK)
+      return rc;
+    cta0 += share[q] * C;
+  }
+  return launch_kernel(fn, grid, threads, smem, true, C, flags, &mp,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
 int sgmv_validate(const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
                   int32_t num_adapters, int32_t M, int32_t* d_err, sgmv_stream_t stream) {
   if (num_segments < 0 || !seg_starts || !d_err || (num_segments > 0 && !seg_adapter))
@@ -682,10 +914,11 @@ const char* sgmv_status_string(int status) {
     case SGMV_EUNSUPPORTED: return "SGMV_EUNSUPPORTED: rank or size outside the supported range";
     case SGMV_ECUDA: return "SGMV_ECUDA: CUDA runtime error";
     case SGMV_ETIMEOUT: return "SGMV_ETIMEOUT: a device-side wait ran out";
+    case SGMV_EPLAN: return "SGMV_EPLAN: a planned call was given an invalid plan";
     default: return "unknown status";
   }
 }
 
-int sgmv_version(void) { return 100; }
+int sgmv_version(void) { return 200; }
 
 }  // extern "C"

@@ -51,6 +51,10 @@ constexpr int kThreads = kConsumers + 32;  // + one producer warp (two CTAs per 
 // Long-batch launches (one CTA per SM): + four warps, a second tensor-role epilogue warpgroup.
 constexpr int kThreadsWide = kThreads + 128;
 constexpr int kStatusTimeout = -5;         // SGMV_ETIMEOUT
+constexpr int kStatusBadPlan = -6;         // SGMV_EPLAN
+constexpr int kPlanMagic = 0x504d4753;     // plan header word 0
+constexpr int kPlanHeader = 16;            // ints before the group table
+constexpr int kMaxProblems = 4;            // projections of one lora_apply_multi launch
 constexpr int kRowsMax = 4;                // rows per CUDA-core work item
 
 enum Mode : int { kFused = 0, kShrink = 1, kExpand = 2 };
@@ -110,6 +114,13 @@ struct Params {
   uint32_t tc_xchg;     // tensor-role split-K exchange buffers (after the ring)
   int32_t xchg_bytes;   // cost of one partial-sum exchange, in streamed bytes (group size rule)
   MemberPlan plan[kPlanSlots];
+  // A plan built by sgmv_plan (nullptr: the segment table is grouped by every CTA).  With a
+  // plan, seg_starts / seg_adapter point at its group table (one segment per adapter group,
+  // S = capacity, the group count in the plan header) and the rows of group segment g are
+  // rowmap[seg_starts[g] .. seg_starts[g + 1]).
+  const int32_t* plan_hdr;
+  const int32_t* rowmap;
+  int32_t cta0, nctas;  // this problem's CTAs in the grid (a multiple of C)
   // Tensor role: x [rows][h_in] and y [rows][h_out] with the 128-byte swizzle, boxes of
   // 64 elements x 128 rows (a whole m-tile) and 64 x 8 rows (one swizzle atom).
   TmaMap tmap_x128, tmap_x8, tmap_y128, tmap_y8;
@@ -430,11 +441,11 @@ static __device__ __forceinline__ uint32_t hash_slot(int k, int mask) {
 // gcnt[lead] holds the group's row count.
 // `scratch` (transient) holds slot[S] and the hash table (3 * hash_slots ints).
 template <int NT>
-static __device__ __forceinline__ void build_schedule(const Params& p, int* starts, int* adapters,
-                                                      int* base, int* gcnt, int* tbase,
-                                                      int* scratch, int* wsum) {
+static __device__ __forceinline__ void build_schedule(const Params& p, int S, int* starts,
+                                                      int* adapters, int* base, int* gcnt,
+                                                      int* tbase, int* scratch, int* wsum) {
   const int tid = threadIdx.x;
-  const int S = p.S, HS = p.hash_slots;
+  const int HS = p.hash_slots;
   int* slot = scratch;
   int* hkey = slot + S;
   int* hlead = hkey + HS;
@@ -464,7 +475,15 @@ static __device__ __forceinline__ void build_schedule(const Params& p, int* star
     if (i < S) adapters[i] = __ldg(p.seg_adapter + i);
   }
   __syncthreads();
-  for (int i = tid; i < S; i += NT) {
+  // A plan's group table is already grouped: every segment is its own group's lead.
+  if (p.plan_hdr) {
+    for (int i = tid; i < S; i += NT) {
+      slot[i] = i;
+      hlead[i] = i;
+      hcnt[i] = starts[i + 1] - starts[i];
+    }
+  }
+  for (int i = tid; i < S && !p.plan_hdr; i += NT) {
     const int k = adapters[i];
     const int len = starts[i + 1] - starts[i];
     int h = -1;
@@ -503,12 +522,16 @@ static __device__ __forceinline__ void build_schedule(const Params& p, int* star
   __syncthreads();
 }
 
+// Token index of (virtual) row v: with a plan, rows are listed group by group in its row map.
+static __device__ __forceinline__ int row_of(const Params& p, int v) {
+  return p.rowmap ? __ldg(p.rowmap + v) : v;
+}
+
 // One warp: turns item t into {adapter, rows, row ids...} in d (d[0]=k, d[1]=R, d[2..]=rows).
-static __device__ __forceinline__ void decode_item(const Params& p, int t, const int* starts,
-                                                   const int* adapters, const int* base,
-                                                   const int* gcnt, int* d) {
+static __device__ __forceinline__ void decode_item(const Params& p, int S, int t,
+                                                   const int* starts, const int* adapters,
+                                                   const int* base, const int* gcnt, int* d) {
   const int lane = threadIdx.x & 31;
-  const int S = p.S;
   int lo = 0, hi = S - 1;  // largest i with base[i] <= t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -531,7 +554,7 @@ static __device__ __forceinline__ void decode_item(const Params& p, int t, const
     }
     const int seg_lo = pos + incl - len;
     const int a = max(seg_lo, p_lo), b = min(pos + incl, p_hi);
-    for (int q = a; q < b; ++q) d[2 + q - p_lo] = starts[j] + (q - seg_lo);
+    for (int q = a; q < b; ++q) d[2 + q - p_lo] = row_of(p, starts[j] + (q - seg_lo));
     pos += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (lane == 0) {
@@ -718,7 +741,7 @@ struct Kernel {
                                                   const MemberPlan& mp, const int* starts,
                                                   const int* adapters, const int* base,
                                                   const int* gcnt, int4* tab, int n_my,
-                                                  int* ctl) {
+                                                  int* ctl, int S) {
     const int lane = threadIdx.x & 31;
     uint32_t issued = 0, parity = 0;  // ring slots filled, parity of each one's last fill
     uint32_t pre_ok = 0;  // stages issued before the wait on the previous kernel, bytes announced
@@ -734,7 +757,7 @@ struct Kernel {
       if (li >= 2 && lane == 0) w.wait<false>(sm.fixed(kDescFree0 + b), ((li >> 1) - 1) & 1);
       __syncwarp();
       int* d = sm.desc(b);
-      decode_item(p, grp.gid + li * grp.ng, starts, adapters, base, gcnt, d);
+      decode_item(p, S, grp.gid + li * grp.ng, starts, adapters, base, gcnt, d);
       if (lane == 0) mbar_arrive(sm.fixed(kDescFull0 + b));
       const int k = d[0];
       const int nrow = min(max(d[1], 0), kRowsMax);
@@ -1055,7 +1078,7 @@ struct Kernel {
   // Number of CTAs (a multiple of the cluster size) that take the tensor role: all of them
   // when every group is long, else a share proportional to the estimated bytes of each side,
   // leaving at least one cluster to each.  Every CTA computes the same value.
-  __device__ __forceinline__ static int tensor_ctas(const Params& p, const int* gcnt,
+  __device__ __forceinline__ static int tensor_ctas(const Params& p, int S, const int* gcnt,
                                                     int n_items, int n_mt, int N, int* ctl) {
     if (n_mt == 0) return 0;
     if (n_items == 0) return N;
@@ -1066,7 +1089,7 @@ struct Kernel {
     }
     __syncthreads();
     int a = 0, b = 0;
-    for (int i = tid; i < p.S; i += NT) {
+    for (int i = tid; i < S; i += NT) {
       const int g = gcnt[i];
       if (g >= p.tc_min_rows) a += g; else b += g;
     }
@@ -1097,9 +1120,21 @@ struct Kernel {
   __device__ __forceinline__ static void run(const Params& p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     pdl_launch_dependents();  // the next kernel of the stream may start its weight prefetch
+    const int tid = threadIdx.x, warp = tid >> 5;
+    // Segments to schedule: the table's, or the group count of a plan (its header is checked:
+    // every CTA reads the same words, so a bad plan makes the whole grid return here).
+    int S = p.S;
+    if (p.plan_hdr) {
+      const int magic = __ldg(p.plan_hdr), status = __ldg(p.plan_hdr + 1);
+      S = __ldg(p.plan_hdr + 3);
+      if (magic != kPlanMagic || status != 0 || __ldg(p.plan_hdr + 2) != p.S || S < 0 ||
+          S > p.S) {
+        if (tid == 0 && blockIdx.x == p.cta0) atomicExch(p.err, kStatusBadPlan);
+        return;
+      }
+    }
     Smem sm;
     sm.init(smem, p);
-    const int tid = threadIdx.x, warp = tid >> 5;
     int* ctl = reinterpret_cast<int*>(smem + p.off_ctl);
     int* starts = reinterpret_cast<int*>(smem + p.off_tab);
     int* adapters = starts + (p.S + 1);
@@ -1120,15 +1155,16 @@ struct Kernel {
       mbar_init(sm.fixed(kNever), 1);
     }
     int* tbase = gcnt + p.S;
-    build_schedule<NT>(p, starts, adapters, base, gcnt, tbase,
-                   reinterpret_cast<int*>(smem + p.off_ring), ctl + 4);
-    const int n_items = base[p.S];
-    const int N = static_cast<int>(gridDim.x);
+    build_schedule<NT>(p, S, starts, adapters, base, gcnt, tbase,
+                       reinterpret_cast<int*>(smem + p.off_ring), ctl + 4);
+    const int n_items = base[S];
+    const int N = p.nctas;                                 // this problem's CTAs...
+    const int bx = static_cast<int>(blockIdx.x) - p.cta0;  // ...and this CTA among them
     // Long groups go to the tensor role: the first n_tc CTAs (whole clusters).
     int n_tc = 0;
     if constexpr (kTensorRole) {
-      if (p.tc_min_rows < 0x7fffffff) n_tc = tensor_ctas(p, gcnt, n_items, tbase[p.S], N, ctl);
-      if (static_cast<int>(blockIdx.x) < n_tc) {
+      if (p.tc_min_rows < 0x7fffffff) n_tc = tensor_ctas(p, S, gcnt, n_items, tbase[S], N, ctl);
+      if (bx < n_tc) {
         if (tid == 0) {  // the barrier words are re-initialised by the tensor role
           for (int s = 0; s < p.nstages; ++s) {
             mbar_inval(sm.full(s));
@@ -1140,8 +1176,8 @@ struct Kernel {
         fence_proxy_async();  // the ring held the hash table
         // (the tensor role makes its own cluster barriers: one after its barriers are
         // initialised, one before exit)
-        TcRole<T, R, MODE, NT>::run(p, smem, starts, adapters, gcnt, tbase, ctl,
-                                static_cast<int>(blockIdx.x), n_tc, tbase[p.S]);
+        TcRole<T, R, MODE, NT>::run(p, S, smem, starts, adapters, gcnt, tbase, ctl, bx, n_tc,
+                                    tbase[S]);
         return;
       }
     }
@@ -1150,7 +1186,7 @@ struct Kernel {
     if constexpr (kTensorRole) {
       if (warp == kConsumerWarps) tmem_relinquish();
     }
-    const int bid = static_cast<int>(blockIdx.x) - n_tc;  // index among the CUDA-core CTAs
+    const int bid = bx - n_tc;  // index among the CUDA-core CTAs
     const int Nc = N - n_tc;
     // Group size E: each item (one adapter's weights, W bytes) is split over E CTAs so that
     // the busiest CTA finishes first: minimise ceil(n_items E / Nc) x (W / E + X [E > 1]),
@@ -1177,7 +1213,7 @@ struct Kernel {
     grp.m = bid & (grp.size - 1);
     grp.gid = bid >> lg;
     grp.ng = Nc >> lg;
-    grp.rank0 = (static_cast<int>(blockIdx.x) & (p.C - 1)) & ~(grp.size - 1);
+    grp.rank0 = (bx & (p.C - 1)) & ~(grp.size - 1);  // cta0 is a multiple of C
     if (tid == 0) {
       mbar_init(sm.fixed(kVReady0), 1);  // the member's own expect_tx arrival + E partials' bytes
       mbar_init(sm.fixed(kVReady1), 1);
@@ -1202,7 +1238,7 @@ struct Kernel {
     if (warp >= kConsumerWarps) {  // the producer, and the warps of the wide geometry that
       if (warp == kConsumerWarps)   // only the tensor role uses
         producer(p, sm, w, grp, mp, starts, adapters, base, gcnt,
-                 reinterpret_cast<int4*>(smem + p.off_stab), n_my, ctl);
+                 reinterpret_cast<int4*>(smem + p.off_stab), n_my, ctl, S);
       if (MODE != kExpand) {
         cluster_wait();
         cluster_arrive_relaxed();
@@ -1238,6 +1274,36 @@ template <typename T, int R, int MODE>
 __global__ void __launch_bounds__(kThreadsWide, 1)
     sgmv_kernel_wide(const __grid_constant__ Params p) {
   Kernel<T, R, MODE, kThreadsWide>::run(p);
+}
+
+// Several projections in one launch (lora_apply_multi): problem q runs on CTAs
+// [prob[q].cta0, prob[q].cta0 + prob[q].nctas), each with its own weights, activations and
+// shared-memory layout, all with the same element type and rank.
+struct MultiParams {
+  int32_t P;
+  Params prob[kMaxProblems];
+};
+
+template <typename T, int R>
+__global__ void __launch_bounds__(kThreads, 2)
+    sgmv_kernel_multi(const __grid_constant__ MultiParams mp) {
+  int q = 0;
+  while (q + 1 < mp.P && static_cast<int>(blockIdx.x) >= mp.prob[q + 1].cta0) ++q;
+  Kernel<T, R, kFused, kThreads>::run(mp.prob[q]);
+}
+
+template <typename T, int R>
+__global__ void __launch_bounds__(kThreadsWide, 1)
+    sgmv_kernel_multi_wide(const __grid_constant__ MultiParams mp) {
+  int q = 0;
+  while (q + 1 < mp.P && static_cast<int>(blockIdx.x) >= mp.prob[q + 1].cta0) ++q;
+  Kernel<T, R, kFused, kThreadsWide>::run(mp.prob[q]);
+}
+
+template <typename T, int R>
+static const void* multi_kernel_ptr(bool wide) {
+  return wide ? reinterpret_cast<const void*>(&sgmv_kernel_multi_wide<T, R>)
+              : reinterpret_cast<const void*>(&sgmv_kernel_multi<T, R>);
 }
 
 // Host-side handle of one instantiation (for the launch).

@@ -24,4 +24,14 @@ const void* kernel_bf16(int mode, int r, bool wide) {
   }
 }
 
+const void* kernel_multi_bf16(int r, bool wide) {
+  switch (r) {
+    case 8: return multi_kernel_ptr<__nv_bfloat16, 8>(wide);
+    case 16: return multi_kernel_ptr<__nv_bfloat16, 16>(wide);
+    case 32: return multi_kernel_ptr<__nv_bfloat16, 32>(wide);
+    case 64: return multi_kernel_ptr<__nv_bfloat16, 64>(wide);
+    default: return nullptr;
+  }
+}
+
 }  // namespace sgmv

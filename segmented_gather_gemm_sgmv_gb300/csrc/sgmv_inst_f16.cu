@@ -24,4 +24,14 @@ const void* kernel_f16(int mode, int r, bool wide) {
   }
 }
 
+const void* kernel_multi_f16(int r, bool wide) {
+  switch (r) {
+    case 8: return multi_kernel_ptr<__half, 8>(wide);
+    case 16: return multi_kernel_ptr<__half, 16>(wide);
+    case 32: return multi_kernel_ptr<__half, 32>(wide);
+    case 64: return multi_kernel_ptr<__half, 64>(wide);
+    default: return nullptr;
+  }
+}
+
 }  // namespace sgmv

@@ -12,4 +12,9 @@ const void* kernel_f32(int mode, int r, bool wide);
 const void* kernel_f16(int mode, int r, bool wide);
 const void* kernel_bf16(int mode, int r, bool wide);
 
+// The fused kernel over several projections in one launch (lora_apply_multi).
+const void* kernel_multi_f32(int r, bool wide);
+const void* kernel_multi_f16(int r, bool wide);
+const void* kernel_multi_bf16(int r, bool wide);
+
 }  // namespace sgmv

@@ -68,8 +68,9 @@ static __device__ __forceinline__ uint32_t sw128(int m, int c) {
 
 // One warp: the token index of each of the 128 rows of m-tile [p0, p0 + 128) of the group led
 // by segment `lead` (-1 past the group's end).
-static __device__ __forceinline__ void tile_rows(const int* starts, const int* adapters, int S,
-                                                 int lead, int p0, int p_hi, int* out) {
+static __device__ __forceinline__ void tile_rows(const Params& p, const int* starts,
+                                                 const int* adapters, int S, int lead, int p0,
+                                                 int p_hi, int* out) {
   const int lane = threadIdx.x & 31;
   const int k = adapters[lead];
   for (int q = lane; q < kTcRows; q += 32) out[q] = -1;
@@ -87,7 +88,7 @@ static __device__ __forceinline__ void tile_rows(const int* starts, const int* a
     }
     const int seg_lo = pos + incl - len;
     const int a = max(seg_lo, p0), b = min(pos + incl, p_hi);
-    for (int q = a; q < b; ++q) out[q - p0] = starts[j] + (q - seg_lo);
+    for (int q = a; q < b; ++q) out[q - p0] = row_of(p, starts[j] + (q - seg_lo));
     pos += __shfl_sync(0xffffffffu, incl, 31);
   }
   __syncwarp();
@@ -149,6 +150,7 @@ struct TcRole {
     uint32_t xchg;   // split-K exchange buffers
     int cr, split;   // cluster member, split-K shrink on
     int k_lo, k_hi;  // this CTA's shrink chunks
+    int S;           // segments (or plan groups) in the table
     int* tmask;   // [2]: 8-row blocks moved as one TMA box
     const int *starts, *adapters, *gcnt, *tbase;
     __device__ __forceinline__ uint32_t full(int s) const { return bars + 8u * s; }
@@ -203,11 +205,11 @@ struct TcRole {
     for (int li = 0; ok && wk.next(); ++li) {
       const int par = li & 1;
       int lead, p0, nrow;
-      c.tile(p.S, wk.mi, lead, p0, nrow);
+      c.tile(c.S, wk.mi, lead, p0, nrow);
       int* rt = c.rowtok + par * kTcRows;
       if (warp == 0) {
         if (!wwait(w, c.fx(kTcRtFree0 + par), ((li >> 1) & 1) ^ 1)) break;
-        tile_rows(c.starts, c.adapters, p.S, lead, p0, p0 + nrow, rt);
+        tile_rows(p, c.starts, c.adapters, c.S, lead, p0, p0 + nrow, rt);
         // Rows of consecutive tokens move by TMA: the whole tile as one 128-row box when all
         // 128 rows are consecutive, else each 8-row block of consecutive tokens as one box
         // (one 1024-byte swizzle atom); every other row by cp.async.
@@ -754,10 +756,10 @@ struct TcRole {
 
   // ----------------------------------------------------------------------------- run ----
   // rank / n_tc: this CTA among the tensor CTAs.  n_mt: m-tiles of all long groups.
-  __device__ __forceinline__ static void run(const Params& p, uint8_t* smem, const int* starts,
-                                             const int* adapters, const int* gcnt,
-                                             const int* tbase, int* ctl, int rank, int n_tc,
-                                             int n_mt) {
+  __device__ __forceinline__ static void run(const Params& p, int S, uint8_t* smem,
+                                             const int* starts, const int* adapters,
+                                             const int* gcnt, const int* tbase, int* ctl,
+                                             int rank, int n_tc, int n_mt) {
     const int tid = threadIdx.x, warp = tid >> 5;
     Ctx c;
     c.bars = smem_addr(smem + p.off_bars);
@@ -769,6 +771,7 @@ struct TcRole {
     c.adapters = adapters;
     c.gcnt = gcnt;
     c.tbase = tbase;
+    c.S = S;
     c.xchg = smem_addr(smem + p.tc_xchg);
     // Split-K shrink over the 4 CTAs of a cluster (fused and shrink forms): member cr shrinks
     // chunks [nk cr / 4, nk (cr + 1) / 4) of h_in.

@@ -16,7 +16,8 @@ HEADER = os.path.join(ROOT, "include", "sgmv.h")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:int|const char \*)\s*\**\s*(\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char \*)\s*\**\s*(\w+)\s*\(", text,
+                                 flags=re.M)))
 
 
 @pytest.fixture(scope="module")
@@ -40,14 +41,15 @@ def test_header_constants_match_binding():
     assert f"#define SGMV_TENSOR_CORES_ALWAYS {binding.SGMV_TENSOR_CORES_ALWAYS}u" in text
     assert f"#define SGMV_LONG_BATCH {binding.SGMV_LONG_BATCH}u" in text
     assert "#define SGMV_MAX_LD (1 << 24)" in text and binding.SGMV_MAX_LD == 1 << 24
+    assert f"#define SGMV_MAX_PROJECTIONS {binding.SGMV_MAX_PROJECTIONS}" in text
     for name, val in [("SGMV_EINVAL", -1), ("SGMV_EALIGN", -2), ("SGMV_EUNSUPPORTED", -3),
-                      ("SGMV_ECUDA", -4), ("SGMV_ETIMEOUT", -5)]:
+                      ("SGMV_ECUDA", -4), ("SGMV_ETIMEOUT", -5), ("SGMV_EPLAN", -6)]:
         assert re.search(rf"{name}\s*=\s*{val}\b", text), name
 
 
 def test_version_and_strings(L):
-    assert L.sgmv_version() == 100
-    for s in (0, -1, -2, -3, -4, -5):
+    assert L.sgmv_version() == 200
+    for s in (0, -1, -2, -3, -4, -5, -6):
         assert binding.status_string(s).startswith("SGMV_")
 
 
@@ -168,3 +170,63 @@ def test_binding_row_stride(shape, stride, ld):
 def test_binding_rejects_unusable_layouts(m):
     with pytest.raises(ValueError):
         binding._rows(m, "x")
+
+
+def test_plan_size_and_host_checks(L):
+    """The plan's size formula (16 header words, group offsets and adapters, the row list) and
+    the host checks of sgmv_plan and the planned calls (num_segments = 0: checks only)."""
+    assert L.sgmv_plan_size(64, 64) == 4 * (16 + 2 * 64 + 1 + 64)
+    assert L.sgmv_plan_size(0, 0) == 4 * 17
+    assert L.sgmv_plan_size(-1, 5) == 0 and L.sgmv_plan_size(5, -1) == 0
+    assert L.sgmv_plan_size(4097, 5) == 0
+    a = OK_ARGS
+    plan = P + 0x60000
+    n = L.sgmv_plan_size(8, 100)
+    assert L.sgmv_plan(a["ss"], a["sa"], 8, 100, plan, n - 4, None) == -1   # too small
+    assert L.sgmv_plan(a["ss"], a["sa"], 8, 100, None, n, None) == -1
+    assert L.sgmv_plan(a["ss"], a["sa"], 8, 100, plan + 4, n, None) == -2  # plan misaligned
+    assert L.sgmv_plan(a["ss"], a["sa"], 4097, 100, plan, 1 << 30, None) == -3
+    assert L.sgmv_plan(a["ss"], a["sa"], -1, 100, plan, n, None) == -1
+
+    def planned(plan=plan, S=0, flags=0, r=16, ldx=4096, ldy=4096):
+        return L.lora_apply_planned(a["y"], ldy, a["x"], ldx, a["A"], a["B"], plan, S, 0, 4096,
+                                    4096, r, 1.0, 1, flags, None)
+    assert planned() == 0
+    assert planned(plan=None) == -1
+    assert planned(plan=plan + 8) == -2
+    assert planned(S=4097) == -3
+    assert planned(r=12) == -3
+    assert planned(flags=6) == -1
+    assert planned(ldx=4088, S=4) == -1
+    assert L.sgmv_shrink_planned(a["y"], a["x"], 4096, a["A"], None, 4, 0, 4096, 16, 1, 0,
+                                 None) == -1
+    assert L.sgmv_shrink_planned(a["y"], a["x"], 4096, a["A"], plan, 0, 0, 4096, 16, 1, 0,
+                                 None) == 0
+    assert L.sgmv_expand_planned(a["y"], 4096, a["x"], a["B"], plan, 4, 0, 16, 4090, 1.0, 1, 0,
+                                 None) == -2
+    assert L.sgmv_expand_planned(a["y"], 4096, a["x"], a["B"], plan, 0, 0, 16, 4096, 1.0, 1, 0,
+                                 None) == 0
+
+
+def test_multi_host_checks(L):
+    a = OK_ARGS
+    plan = P + 0x60000
+
+    def proj(**kw):
+        d = dict(y=a["y"], x=a["x"], A_ptrs=a["A"], B_ptrs=a["B"], ldy=4096, ldx=4096, h_in=4096,
+                 h_out=4096, scale=1.0, reserved=0)
+        d.update(kw)
+        return binding.Projection(**d)
+
+    def multi(projs, S=0, plan=plan, r=16, flags=0):
+        arr = (binding.Projection * max(1, len(projs)))(*projs)
+        return L.lora_apply_multi(arr, len(projs), plan, S, 0, r, 1, flags, None)
+    assert multi([proj(), proj(h_out=1024, ldy=1024)]) == 0
+    assert multi([]) == -1
+    assert multi([proj()] * 5) == -3
+    assert multi([proj(), proj(y=None)]) == -1
+    assert multi([proj(), proj(h_out=1020, ldy=1020)]) == -2
+    assert multi([proj(x=P + 0x10008)]) == -2
+    assert multi([proj()], plan=None) == -1
+    assert multi([proj()], r=24) == -3
+    assert multi([proj()], flags=16) == -1
