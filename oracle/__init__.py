@@ -117,6 +117,9 @@ class OracleLib:
         lib.oracle_validate_pointers.argtypes = [dp, dp, dp, dp, i32, i32]
         lib.oracle_validate_pointers.restype = ctypes.c_int32
         lib.oracle_plan.argtypes = [dp, dp, i32, i32, dp, dp, dp]
+        lib.oracle_lora_apply_ranked.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i32, i32, i32,
+                                                 i32]
+        lib.oracle_lora_apply_ranked.restype = ctypes.c_int
         lib.oracle_plan.restype = ctypes.c_int32
         self.lib = lib
         self.path = lib_path
@@ -194,6 +197,31 @@ class OracleLib:
                                                      int(num_adapters)))
 
 
+    def lora_apply_ranked(self, y, x, A_blocks, B_blocks, rank, scale, seg_starts, seg_adapter,
+                          layer_idx):
+        """Return y + scale[k] * (x A_k) B_k per segment (fp64), adapter k of rank rank[k]:
+        A_blocks[k] (L, h_in, rank[k]) and B_blocks[k] (L, rank[k], h_out), or None for an
+        adapter no segment uses.  y is not modified."""
+        y = _f64(y).copy()
+        x = _f64(x)
+        ss, sa = _i32(seg_starts), _i32(seg_adapter)
+        _check_segments(ss, sa, len(A_blocks), y.shape[0])
+        rk = _i32(rank)
+        sc = _f64(scale)
+        if len(rk) < len(A_blocks) or len(sc) < len(A_blocks):
+            raise ValueError("rank and scale need one entry per adapter")
+        for k, (a, b) in enumerate(zip(A_blocks, B_blocks)):
+            if a is not None and (np.shape(a)[-1] != rk[k] or np.shape(b)[-2] != rk[k]):
+                raise ValueError(f"adapter {k}: blocks do not have rank {rk[k]}")
+        At, Bt = _PtrTable(A_blocks), _PtrTable(B_blocks)
+        rc = self.lib.oracle_lora_apply_ranked(y.ctypes.data, x.ctypes.data, At.ptr, Bt.ptr,
+                                               rk.ctypes.data, sc.ctypes.data, ss.ctypes.data,
+                                               sa.ctypes.data, len(sa), int(layer_idx),
+                                               x.shape[1], y.shape[1])
+        if rc != 0:
+            raise MemoryError("oracle_lora_apply_ranked failed")
+        return y
+
     def plan(self, seg_starts, seg_adapter, max_rows):
         """The adapter grouping of a table: (g_starts[G+1], g_adapter[G], rows[n]) as int32
         arrays, or None when more than max_rows rows would be listed."""
@@ -243,12 +271,17 @@ def plan(*args, **kw):
     return _load().plan(*args, **kw)
 
 
+def lora_apply_ranked(*args, **kw):
+    return _load().lora_apply_ranked(*args, **kw)
+
+
 lora_apply.__doc__ = OracleLib.lora_apply.__doc__
 sgmv_shrink.__doc__ = OracleLib.sgmv_shrink.__doc__
 sgmv_expand.__doc__ = OracleLib.sgmv_expand.__doc__
 validate.__doc__ = OracleLib.validate.__doc__
 validate_pointers.__doc__ = OracleLib.validate_pointers.__doc__
 plan.__doc__ = OracleLib.plan.__doc__
+lora_apply_ranked.__doc__ = OracleLib.lora_apply_ranked.__doc__
 
 
 class PreparedApply:

@@ -200,3 +200,47 @@ int32_t oracle_plan(const int32_t *seg_starts, const int32_t *seg_adapter, int32
     g_starts[G] = n;
     return G;
 }
+
+/* y[t] += scale_k * (x[t] A_k) B_k with a rank and a scale of its own for every adapter
+ * ("Punica Guide: Multi-Tenant LoRA Serving with SGMV", section "The Heterogeneous Batching
+ * Bottleneck", the y_i equation with alpha/r taken per adapter, A_k of shape d_in x r_k and B_k
+ * of shape r_k x d_out; section "Operational Checklist", rank standardisation: batches whose
+ * adapters differ in rank).  A[k] is adapter k's block [L][h_in][rank[k]], B[k] its block
+ * [L][rank[k]][h_out]; scale[k] multiplies its term.  Same per-row loop as oracle_lora_apply. */
+int oracle_lora_apply_ranked(double *y, const double *x, const double *const *A,
+                             const double *const *B, const int32_t *rank, const double *scale,
+                             const int32_t *seg_starts, const int32_t *seg_adapter,
+                             int32_t num_segments, int32_t layer_idx, int32_t h_in,
+                             int32_t h_out)
+{
+    int32_t r_max = 1;
+    for (int32_t i = 0; i < num_segments; ++i)
+        if (seg_adapter[i] >= 0 && rank[seg_adapter[i]] > r_max) r_max = rank[seg_adapter[i]];
+    double *v = (double *)malloc(sizeof(double) * (size_t)r_max);
+    if (!v) return -1;
+    for (int32_t i = 0; i < num_segments; ++i) {
+        const int32_t k = seg_adapter[i];
+        if (k < 0) continue;
+        const int32_t r = rank[k];
+        const double *Ak = A[k] + (size_t)layer_idx * (size_t)h_in * (size_t)r;
+        const double *Bk = B[k] + (size_t)layer_idx * (size_t)r * (size_t)h_out;
+        for (int32_t t = seg_starts[i]; t < seg_starts[i + 1]; ++t) {
+            const double *xt = x + (size_t)t * (size_t)h_in;
+            double *yt = y + (size_t)t * (size_t)h_out;
+            for (int32_t c = 0; c < r; ++c) {
+                double s = 0.0;
+                for (int32_t j = 0; j < h_in; ++j)
+                    s += xt[j] * Ak[(size_t)j * (size_t)r + (size_t)c];
+                v[c] = s;
+            }
+            for (int32_t n = 0; n < h_out; ++n) {
+                double s = 0.0;
+                for (int32_t c = 0; c < r; ++c)
+                    s += v[c] * Bk[(size_t)c * (size_t)h_out + (size_t)n];
+                yt[n] += scale[k] * s;
+            }
+        }
+    }
+    free(v);
+    return 0;
+}

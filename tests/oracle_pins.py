@@ -282,7 +282,52 @@ def check_plan(o):
             assert rows[gs[g]:gs[g + 1]].tolist() == expect
 
 
+def check_ranked(o):
+    """Per-adapter rank and scale, pinned three ways: a hand-worked two-adapter case; per-row
+    GEMV chains through numpy with each adapter's own shapes (a library matmul, not this
+    loop); and zero-padding -- an adapter of rank r_k gives exactly what the same weights
+    padded with zero columns of A and zero rows of B to a larger rank give."""
+    # hand-worked: h_in = h_out = 2; adapter 0 of rank 1, adapter 1 of rank 2
+    x = np.array([[1.0, 2.0], [3.0, -1.0], [0.5, 0.5]])
+    y = np.array([[10.0, 20.0], [30.0, 40.0], [50.0, 60.0]])
+    A0 = np.array([[[1.0], [1.0]]])               # (1, 2, 1): v = x0 + x1
+    B0 = np.array([[[2.0, -1.0]]])                # (1, 1, 2)
+    A1 = np.array([[[1.0, 0.0], [0.0, 1.0]]])     # identity
+    B1 = np.array([[[1.0, 1.0], [0.0, 1.0]]])
+    got = o.lora_apply_ranked(y, x, [A0, A1], [B0, B1], [1, 2], [0.5, 2.0], [0, 1, 3], [0, 1], 0)
+    # row 0, adapter 0: v = 3 -> 0.5 * [6, -3] = [3, -1.5]
+    # rows 1, 2, adapter 1: v = x -> v B1 = [x0, x0 + x1] -> *2
+    want = np.array([[13.0, 18.5], [36.0, 44.0], [51.0, 62.0]])
+    assert np.array_equal(got, want), got
+    rng = np.random.default_rng(19)
+    h_in, h_out, L = 24, 40, 2
+    ranks = [8, 16, 24, 8, 32]
+    A = [rng.standard_normal((L, h_in, r)) for r in ranks]
+    B = [rng.standard_normal((L, r, h_out)) for r in ranks]
+    scale = rng.uniform(0.1, 3.0, size=len(ranks))
+    ss = np.array([0, 3, 4, 9, 9, 12], np.int32)
+    sa = np.array([2, 0, 4, 1, 2], np.int32)
+    x = rng.standard_normal((12, h_in))
+    y = rng.standard_normal((12, h_out))
+    got = o.lora_apply_ranked(y, x, A, B, ranks, scale, ss, sa, 1)
+    want = y.copy()
+    for i, k in enumerate(sa):
+        for t in range(ss[i], ss[i + 1]):
+            want[t] += scale[k] * (x[t:t + 1] @ A[k][1] @ B[k][1])[0]
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    # zero padding to rank 32 through the uniform-rank entry point, one adapter at a time
+    for k in range(len(ranks)):
+        Ap = np.zeros((L, h_in, 32))
+        Bp = np.zeros((L, 32, h_out))
+        Ap[:, :, :ranks[k]] = A[k]
+        Bp[:, :ranks[k], :] = B[k]
+        one = o.lora_apply_ranked(y, x, [A[k]], [B[k]], [ranks[k]], [scale[k]], [0, 12], [0], 1)
+        pad = o.lora_apply(y, x, [Ap], [Bp], [0, 12], [0], 1, scale[k])
+        assert np.allclose(one, pad, rtol=1e-12, atol=1e-12)
+
+
 ALL_CHECKS = [check_hand_example, check_merged_weights, check_per_request_gemv,
               check_single_adapter_dense, check_zero_adapter, check_permutation,
               check_brute_force, check_layer_selection, check_shrink_expand,
-              check_untouched_rows, check_validate, check_validate_pointers, check_plan]
+              check_untouched_rows, check_validate, check_validate_pointers, check_plan,
+              check_ranked]

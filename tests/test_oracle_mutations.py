@@ -39,6 +39,10 @@ MUTATIONS = [
     ("plan_groups_empty_segments",
      "if (k < 0 || seg_starts[i + 1] <= seg_starts[i]) continue;\n        int32_t seen",
      "if (k < 0) continue;\n        int32_t seen", None),
+    ("ranked_scale_of_first_adapter", "yt[n] += scale[k] * s;", "yt[n] += scale[0] * s;",
+     None),
+    ("ranked_transposed_B", "(size_t)layer_idx * (size_t)h_in * (size_t)r;\n        const double *Bk = B[k] + (size_t)layer_idx * (size_t)r * (size_t)h_out;\n        for (int32_t t = seg_starts[i]; t < seg_starts[i + 1]; ++t) {\n            const double *xt = x + (size_t)t * (size_t)h_in;\n            double *yt = y + (size_t)t * (size_t)h_out;\n            for (int32_t c = 0; c < r; ++c) {\n                double s = 0.0;\n                for (int32_t j = 0; j < h_in; ++j)\n                    s += xt[j] * Ak[(size_t)j * (size_t)r + (size_t)c];\n                v[c] = s;\n            }\n            for (int32_t n = 0; n < h_out; ++n) {\n                double s = 0.0;\n                for (int32_t c = 0; c < r; ++c)\n                    s += v[c] * Bk[(size_t)c * (size_t)h_out + (size_t)n];\n                yt[n] += scale[k] * s;",
+     "(size_t)layer_idx * (size_t)h_in * (size_t)r;\n        const double *Bk = B[k] + (size_t)layer_idx * (size_t)r * (size_t)h_out;\n        for (int32_t t = seg_starts[i]; t < seg_starts[i + 1]; ++t) {\n            const double *xt = x + (size_t)t * (size_t)h_in;\n            double *yt = y + (size_t)t * (size_t)h_out;\n            for (int32_t c = 0; c < r; ++c) {\n                double s = 0.0;\n                for (int32_t j = 0; j < h_in; ++j)\n                    s += xt[j] * Ak[(size_t)j * (size_t)r + (size_t)c];\n                v[c] = s;\n            }\n            for (int32_t n = 0; n < h_out; ++n) {\n                double s = 0.0;\n                for (int32_t c = 0; c < r; ++c)\n                    s += v[c] * Bk[(size_t)n * (size_t)r + (size_t)c];\n                yt[n] += scale[k] * s;", None),
     ("plan_rows_reversed", "rows[n++] = t;",
      "rows[n++] = seg_starts[j + 1] - 1 - (t - seg_starts[j]);", None),
 ]
