@@ -287,6 +287,21 @@ class Setup:
             self.x.append(x)
             self.y.append(y)
         self.v = None
+        self.plan = None
+
+    def make_plan(self):
+        """The batch's plan (sgmv_plan), built once and reused by every planned call."""
+        import torch
+        from segmented_gather_gemm_sgmv_gb300 import sgmv_plan
+        self.plan = sgmv_plan(self.d_ss, self.d_sa, self.M)
+        torch.cuda.synchronize()
+
+    def call_planned(self, i, stream=None):
+        from segmented_gather_gemm_sgmv_gb300 import lora_apply_planned
+        lora_apply_planned(self.y[i], self.x[i], self.A_ptrs, self.B_ptrs, self.plan,
+                           i % self.w.layers, self.w.r, self.w.scale, stream=stream,
+                           overlap_prior=self.overlap, tensor_cores=self.tensor_cores,
+                           long_batch=self.long_batch)
 
     def call(self, i, stream=None):
         from segmented_gather_gemm_sgmv_gb300 import lora_apply
@@ -365,8 +380,11 @@ def measure_config(torch, name, device, stream, seconds, args):
     n = setup.calls
     out = {"calls_per_step": n, "layers": w.layers}
     nbytes, M = algorithmic_bytes(w, setup.ss, setup.sa)
+    setup.make_plan()
     for label, overlap, fn in (("isolated", False, setup.call), ("unfused", True,
                                                                  setup.call_unfused),
+                               ("planned_isolated", False, setup.call_planned),
+                               ("planned_chained", True, setup.call_planned),
                                ("chained", True, setup.call)):
         setup.overlap = overlap
         g = capture_step(torch, fn, n, stream)
@@ -394,8 +412,114 @@ def measure_config(torch, name, device, stream, seconds, args):
         "roofline": roofline(w, setup.ss, setup.sa, us, args.tensor_cores),
         "roofline_isolated_frac": roofline(w, setup.ss, setup.sa, out["us_per_call_isolated"],
                                            args.tensor_cores)["frac"],
+        "roofline_planned_frac": roofline(w, setup.ss, setup.sa, out["us_per_call_planned_chained"],
+                                          args.tensor_cores)["frac"],
+        "planned_launch": "sgmv_plan once per batch, then lora_apply_planned (same flags)",
     })
     del setup
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_multi(torch, device, stream, seconds):
+    """q, k and v of a Llama-7B attention block (h = 4096, r = 16, fp16, the decode_distinct
+    batch and pool shape, each projection its own pool): one lora_apply_multi launch per layer
+    against three lora_apply_planned launches per layer, over a 32-layer step."""
+    from segmented_gather_gemm_sgmv_gb300 import lora_apply_multi, lora_apply_planned
+    w = workloads.WORKLOADS["decode_distinct"]
+    setups = [Setup(w, device, seed=s) for s in (0, 10, 20)]
+    for st in setups:
+        st.overlap = True
+    setups[0].make_plan()
+    plan = setups[0].plan
+    n = setups[0].calls
+
+    def multi(i, stream=None):
+        lora_apply_multi([(st.y[i], st.x[i], st.A_ptrs, st.B_ptrs, w.scale) for st in setups],
+                         plan, i % w.layers, w.r, stream=stream, overlap_prior=True)
+
+    def three(i, stream=None):
+        for st in setups:
+            lora_apply_planned(st.y[i], st.x[i], st.A_ptrs, st.B_ptrs, plan, i % w.layers, w.r,
+                               w.scale, stream=stream, overlap_prior=True)
+
+    nbytes, M = algorithmic_bytes(w, setups[0].ss, setups[0].sa)
+    out = {"projections": 3, "workload": "decode_distinct x 3 (q, k, v)",
+           "bytes_per_layer": 3 * nbytes}
+    for label, fn in (("multi", multi), ("three_planned", three)):
+        g = capture_step(torch, fn, n, stream)
+        K = steps_for(torch, g, stream, seconds)
+        ms = time_steps(torch, g, K, 3, stream)
+        us = ms * 1e3 / (K * n)
+        out[f"us_per_layer_{label}"] = round(us, 3)
+        out[f"GB_per_s_{label}"] = round(3 * nbytes / us / 1e3, 2)
+        del g
+    out["launch"] = ("lora_apply_multi (one launch per layer for q, k, v) vs three "
+                     "lora_apply_planned launches, SGMV_OVERLAP_PRIOR")
+    del setups
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_ranked(torch, device, stream, seconds):
+    """Mixed ranks in one decode batch: the decode_distinct batch (64 one-token segments, h =
+    4096, fp16, 32 layers) with adapter k of rank (8, 16, 32, 64)[k % 4], each stored at its own
+    rank, through lora_apply_ranked (r_max = 64); beside it the same batch with every adapter
+    padded to rank 64 through lora_apply."""
+    from segmented_gather_gemm_sgmv_gb300 import lora_apply, lora_apply_ranked
+    w = workloads.WORKLOADS["decode_distinct"]
+    ranks = [(8, 16, 32, 64)[k % 4] for k in range(w.num_adapters)]
+    ss, sa = workloads.make_segments(w.name, 0)
+    M, L = int(ss[-1]), w.layers
+    g = torch.Generator(device=device).manual_seed(5)
+    A = [torch.randn((L, w.h_in, r), generator=g, device=device, dtype=torch.float16)
+         for r in ranks]
+    B = [torch.randn((L, r, w.h_out), generator=g, device=device, dtype=torch.float16)
+         for r in ranks]
+    A_ptrs = torch.tensor([a.data_ptr() for a in A], dtype=torch.int64, device=device)
+    B_ptrs = torch.tensor([b.data_ptr() for b in B], dtype=torch.int64, device=device)
+    Ap = torch.randn((w.num_adapters, L, w.h_in, 64), generator=g, device=device,
+                     dtype=torch.float16)
+    Bp = torch.randn((w.num_adapters, L, 64, w.h_out), generator=g, device=device,
+                     dtype=torch.float16)
+    Ap_ptrs, Bp_ptrs = workloads.pointer_table(Ap, device), workloads.pointer_table(Bp, device)
+    d_rank = torch.tensor(ranks, dtype=torch.int32, device=device)
+    d_scale = torch.tensor([16.0 / r for r in ranks], dtype=torch.float32, device=device)
+    d_ss, d_sa = torch.as_tensor(ss, device=device), torch.as_tensor(sa, device=device)
+    acts = [workloads.make_activations(w, M, device, seed=300 + i) for i in range(L)]
+
+    def ranked(i, stream=None):
+        x, y = acts[i]
+        lora_apply_ranked(y, x, A_ptrs, B_ptrs, d_rank, d_scale, i, 64, seg_starts=d_ss,
+                          seg_adapter=d_sa, stream=stream, overlap_prior=True)
+
+    def padded(i, stream=None):
+        x, y = acts[i]
+        lora_apply(y, x, Ap_ptrs, Bp_ptrs, d_ss, d_sa, i, 64, 0.25, stream=stream,
+                   overlap_prior=True)
+
+    eb = 2
+    act = M * w.h_in * eb + 2 * M * w.h_out * eb
+    nbytes = sum((w.h_in + w.h_out) * ranks[int(k)] * eb for k in set(sa.tolist())) + act
+    nbytes_padded = len(set(sa.tolist())) * (w.h_in + w.h_out) * 64 * eb + act
+    out = {"workload": "decode_distinct batch, adapter ranks (8, 16, 32, 64) cycling, r_max 64",
+           "bytes_per_call": nbytes, "bytes_per_call_padded": nbytes_padded}
+    for label, fn, nb in (("ranked", ranked, nbytes), ("padded_r64", padded, nbytes_padded)):
+        gr = capture_step(torch, fn, L, stream)
+        K = steps_for(torch, gr, stream, seconds)
+        ms = time_steps(torch, gr, K, 3, stream)
+        us = ms * 1e3 / (K * L)
+        out[f"us_per_call_{label}"] = round(us, 3)
+        out[f"GB_per_s_{label}"] = round(nb / us / 1e3, 2)
+        del gr
+    hbm, _, kind = measured_peaks()
+    out["roofline_frac_ranked"] = round(nbytes / (hbm * 1e9) / (out["us_per_call_ranked"] * 1e-6),
+                                        4)
+    out["launch"] = ("lora_apply_ranked (each adapter read at its own rank) vs lora_apply on "
+                     "rank-64 copies, SGMV_OVERLAP_PRIOR, 32-layer steps")
+    del A, B, Ap, Bp, acts
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return out
@@ -526,6 +650,8 @@ def run_ours(args):
         for name in PER_CONFIG:
             per_config[name] = measure_config(torch, name, device, stream, args.config_seconds,
                                               args)
+        per_config["qkv_multi"] = measure_multi(torch, device, stream, args.config_seconds)
+        per_config["mixed_rank"] = measure_ranked(torch, device, stream, args.config_seconds)
 
     w = workloads.WORKLOADS[args.workload]
     long_batch = {"auto": w.prefill, "on": True, "off": False}[args.long_batch]

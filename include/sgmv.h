@@ -347,6 +347,35 @@ int lora_apply_multi(const sgmv_projection_t *proj, int32_t num_proj, const void
                      uint32_t flags, sgmv_stream_t stream);
 
 /*
+ * lora_apply_ranked -- the fused LoRA term with a rank and a scale of its own for every
+ * adapter: y[t] += adapter_scale[k] * (x[t] . A_k) . B_k, where adapter k has rank
+ * r_k = adapter_rank[k] and its blocks are A_k [L][h_in][r_k] and B_k [L][r_k][h_out]
+ * (row-major; layer l at l*h_in*r_k and l*r_k*h_out).  Source: the y_i equation of section
+ * "The Heterogeneous Batching Bottleneck" with alpha/r taken per adapter, and section
+ * "Operational Checklist" (rank standardisation): a batch can hold adapters of several ranks,
+ * and each is read at its own size, not padded.
+ *   adapter_rank   in   device int32 [num_adapters]: r_k, a multiple of 8 in [8, r_max].  An
+ *                       entry outside that set makes its adapter a no-op (its rows are left
+ *                       unchanged): the kernels never read more of a block than its entry
+ *                       declares.
+ *   adapter_scale  in   device float [num_adapters]: the factor of adapter k's term (alpha_k /
+ *                       r_k in the equation)
+ *   seg_starts, seg_adapter  the table (as for lora_apply), or null when `plan` is given
+ *   plan           in   a plan from sgmv_plan (as for lora_apply_planned), or null
+ *   r_max          8, 16, 32 or 64: the largest rank the call may meet (the kernels' capacity)
+ * Other arguments, flags, layout and errors: as for lora_apply_strided.  With every rank equal
+ * to r_max and every scale equal to `scale` the result equals lora_apply_strided's bit for bit.
+ * On the tensor cores the columns of v past r_k are exact zeros; on the CUDA cores B rows past
+ * r_k are never read.
+ */
+int lora_apply_ranked(void *y, int32_t ldy, const void *x, int32_t ldx,
+                      const void *const *A_ptrs, const void *const *B_ptrs,
+                      const int32_t *adapter_rank, const float *adapter_scale,
+                      const int32_t *seg_starts, const int32_t *seg_adapter, const void *plan,
+                      int32_t num_segments, int32_t layer_idx, int32_t h_in, int32_t h_out,
+                      int32_t r_max, sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream);
+
+/*
  * sgmv_validate -- checks a segment table on the device and writes an OR of these bits to
  * *d_err (device int32, overwritten; 0 = valid):
  *   1  seg_starts decreases somewhere          2  seg_starts[0] < 0

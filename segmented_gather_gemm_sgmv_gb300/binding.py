@@ -31,7 +31,8 @@ SYMBOLS = ("lora_apply", "lora_apply_ex", "lora_apply_strided", "sgmv_shrink", "
            "sgmv_shrink_strided", "sgmv_expand", "sgmv_expand_ex", "sgmv_expand_strided",
            "sgmv_validate", "sgmv_validate_pointers", "sgmv_get_error", "sgmv_set_wait_limit",
            "sgmv_status_string", "sgmv_version", "sgmv_plan_size", "sgmv_plan",
-           "lora_apply_planned", "sgmv_shrink_planned", "sgmv_expand_planned", "lora_apply_multi")
+           "lora_apply_planned", "sgmv_shrink_planned", "sgmv_expand_planned", "lora_apply_multi",
+           "lora_apply_ranked")
 
 
 class Projection(ctypes.Structure):
@@ -91,6 +92,8 @@ def lib(build_if_stale: bool = True) -> ctypes.CDLL:
                                           vp]
         L.lora_apply_multi.argtypes = [ctypes.POINTER(Projection), i32, vp, i32, i32, i32, ci,
                                        u32, vp]
+        L.lora_apply_ranked.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                        i32, i32, i32, ci, u32, vp]
         L.sgmv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
         L.sgmv_set_wait_limit.argtypes = [ctypes.c_uint64, i32]
         L.sgmv_status_string.argtypes = [ctypes.c_int]
@@ -484,3 +487,35 @@ def lora_apply_multi(projections, plan: Plan, layer_idx, r, stream=None, overlap
                                     int(layer_idx), int(r), _dtype_code(x0), flags,
                                     _stream(stream, x0.device))
     _check(rc, "lora_apply_multi")
+
+
+def lora_apply_ranked(y, x, A_ptrs, B_ptrs, adapter_rank, adapter_scale, layer_idx, r_max,
+                      seg_starts=None, seg_adapter=None, plan: Plan = None, stream=None,
+                      overlap_prior=False, tensor_cores="auto", long_batch=False):
+    """y[t] += adapter_scale[k] (x[t] A_k) B_k with adapter k of rank adapter_rank[k] (device
+    int32 and float32 tensors, one entry per adapter); the table, or a plan."""
+    import torch
+    ldy, ldx = _rows(y, "y"), _rows(x, "x")
+    if x.dtype != y.dtype or x.shape[0] != y.shape[0]:
+        raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
+    _cuda(adapter_rank, "adapter_rank")
+    _cuda(adapter_scale, "adapter_scale")
+    if adapter_rank.dtype != torch.int32 or adapter_scale.dtype != torch.float32:
+        raise TypeError("adapter_rank must be int32 and adapter_scale float32")
+    if (plan is None) == (seg_starts is None):
+        raise ValueError("pass either the segment table or a plan")
+    if plan is None:
+        S = _table(seg_starts, seg_adapter)
+        ss, sa, pl = seg_starts.data_ptr(), seg_adapter.data_ptr(), None
+        extra = (seg_starts, seg_adapter)
+    else:
+        S, ss, sa, pl = plan.num_segments, None, None, plan.buf.data_ptr()
+        extra = (plan.buf,)
+    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    with _on(x, y, A_ptrs, B_ptrs, adapter_rank, adapter_scale, *extra):
+        rc = lib().lora_apply_ranked(
+            y.data_ptr(), ldy, x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
+            adapter_rank.data_ptr(), adapter_scale.data_ptr(), ss, sa, pl, S, int(layer_idx),
+            x.shape[1], y.shape[1], int(r_max), _dtype_code(x), flags, _stream(stream, x.device))
+    _check(rc, "lora_apply_ranked")
+    return y

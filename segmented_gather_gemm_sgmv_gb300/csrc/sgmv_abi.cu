@@ -846,6 +846,51 @@ int lora_apply_multi(const sgmv_projection_t* proj, int32_t num_proj, const void
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+int lora_apply_ranked(void* y, int32_t ldy, const void* x, int32_t ldx,
+                      const void* const* A_ptrs, const void* const* B_ptrs,
+                      const int32_t* adapter_rank, const float* adapter_scale,
+                      const int32_t* seg_starts, const int32_t* seg_adapter, const void* plan,
+                      int32_t num_segments, int32_t layer_idx, int32_t h_in, int32_t h_out,
+                      int32_t r_max, sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream) {
+  if (!flags_ok(flags)) return SGMV_EINVAL;
+  if (!adapter_rank || !adapter_scale) return SGMV_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(adapter_rank) & 3u) ||
+      (reinterpret_cast<uintptr_t>(adapter_scale) & 3u))
+    return SGMV_EALIGN;
+  int rc = SGMV_OK;
+  if (plan) {
+    if ((rc = check_plan_args(plan, num_segments)) != SGMV_OK) return rc;
+    rc = check_common(num_segments, plan, plan, layer_idx, r_max, dtype);
+  } else {
+    rc = check_common(num_segments, seg_starts, seg_adapter, layer_idx, r_max, dtype);
+  }
+  if (rc != SGMV_OK) return rc;
+  if (!y || !x || !A_ptrs || !B_ptrs) return SGMV_EINVAL;
+  if ((rc = check_hidden(h_in)) != SGMV_OK || (rc = check_hidden(h_out)) != SGMV_OK) return rc;
+  if ((rc = check_ld(ldx, h_in)) != SGMV_OK || (rc = check_ld(ldy, h_out)) != SGMV_OK) return rc;
+  if (!aligned16(y) || !aligned16(x) || (reinterpret_cast<uintptr_t>(A_ptrs) & 7u) ||
+      (reinterpret_cast<uintptr_t>(B_ptrs) & 7u))
+    return SGMV_EALIGN;
+  if (num_segments == 0) return SGMV_OK;
+  sgmv::Params p = {};
+  p.y = y;
+  p.x = x;
+  p.ldx = ldx;
+  p.ldy = ldy;
+  p.A_ptrs = A_ptrs;
+  p.B_ptrs = B_ptrs;
+  p.adapter_rank = adapter_rank;
+  p.adapter_scale = adapter_scale;
+  if (plan) {
+    use_plan(p, plan, num_segments);
+  } else {
+    p.seg_starts = seg_starts;
+    p.seg_adapter = seg_adapter;
+  }
+  const Problem pb{sgmv::kFused, dtype, r_max, num_segments, layer_idx, h_in, h_out, 1.0f};
+  return launch(pb, p, flags, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int sgmv_validate(const int32_t* seg_starts, const int32_t* seg_adapter, int32_t num_segments,
                   int32_t num_adapters, int32_t M, int32_t* d_err, sgmv_stream_t stream) {
   if (num_segments < 0 || !seg_starts || !d_err || (num_segments > 0 && !seg_adapter))

@@ -120,6 +120,12 @@ struct Params {
   // rowmap[seg_starts[g] .. seg_starts[g + 1]).
   const int32_t* plan_hdr;
   const int32_t* rowmap;
+  // Per-adapter rank and scale (lora_apply_ranked; nullptr: every adapter has rank R and
+  // `scale`).  Adapter k's blocks are [L][h_in][r_k] and [L][r_k][h_out] (rank_of).  The
+  // kernels keep R (the call's r_max) as their capacity: columns of v past r_k stay exactly
+  // zero and B rows past r_k are never read.
+  const int32_t* adapter_rank;
+  const float* adapter_scale;
   int32_t cta0, nctas;  // this problem's CTAs in the grid (a multiple of C)
   // Tensor role: x [rows][h_in] and y [rows][h_out] with the 128-byte swizzle, boxes of
   // 64 elements x 128 rows (a whole m-tile) and 64 x 8 rows (one swizzle atom).
@@ -522,6 +528,19 @@ static __device__ __forceinline__ void build_schedule(const Params& p, int S, in
   __syncthreads();
 }
 
+// Rank of adapter k: R in an unranked call; in a ranked call its entry when that is a multiple
+// of 8 in [8, R], else 0 -- the adapter is then skipped (its rows get exactly + 0), so that no
+// entry can make the kernel read past the block size the caller declared.
+template <int R>
+static __device__ __forceinline__ int rank_of(const Params& p, int k) {
+  if (!p.adapter_rank) return R;
+  const int v = __ldg(p.adapter_rank + k);
+  return (v >= 8 && v <= R && (v & 7) == 0) ? v : 0;
+}
+static __device__ __forceinline__ float scale_of(const Params& p, int k) {
+  return p.adapter_scale ? __ldg(p.adapter_scale + k) : p.scale;
+}
+
 // Token index of (virtual) row v: with a plan, rows are listed group by group in its row map.
 static __device__ __forceinline__ int row_of(const Params& p, int v) {
   return p.rowmap ? __ldg(p.rowmap + v) : v;
@@ -541,6 +560,15 @@ static __device__ __forceinline__ void decode_item(const Params& p, int S, int t
   const int k = adapters[lead];
   const int p_lo = (t - base[lead]) * kRowsMax;
   const int p_hi = min(p_lo + kRowsMax, gcnt[lead]);  // stop once the chunk's rows are found
+  if (p.rowmap) {  // a plan's group is one segment: its rows are consecutive in the row map
+    if (lane < p_hi - p_lo) d[2 + lane] = __ldg(p.rowmap + starts[lead] + p_lo + lane);
+    if (lane == 0) {
+      d[0] = k;
+      d[1] = max(0, p_hi - p_lo);
+    }
+    __syncwarp();
+    return;
+  }
   int pos = 0;
   for (int jb = lead; jb < S && pos < p_hi; jb += 32) {
     const int j = jb + lane;
@@ -699,21 +727,23 @@ struct Kernel {
 
   // One stage into the current ring slot: wait for the slot (after the first round), announce
   // its bytes (weights and activations), copy the weights, and the activations when `acts`.
-  // Returns whether the stage's bytes were announced (false once the CTA has given up).
+  // Returns whether the stage's bytes were announced (false once the CTA has given up).  rk:
+  // the item's adapter rank (A rows are rk elements; B rows past rk are not copied).
   __device__ __forceinline__ static bool issue_stage(const Params& p, const Smem& sm,
                                                      const Waiter& w, int4 e, const RingPos& rp,
                                                      const T* Ak, const T* Bk, const int* d,
                                                      int nrow, bool acts, uint64_t pol_w,
-                                                     uint64_t pol_a) {
+                                                     uint64_t pol_a, int rk) {
     const int lane = threadIdx.x & 31;
     const int s = rp.s;
-    const int kind = e.x & 15, rows = e.x >> 4;
+    const int kind = e.x & 15;
+    const int rows = kind == kChunkB ? max(0, min(e.x >> 4, rk - e.y)) : (e.x >> 4);
     if (lane == 0) {
       if (rp.wrapped) w.wait<false>(sm.empty(s), rp.par ^ 1u);
       const bool ok = w.ok();
       uint32_t bytes;
       if (kind == kChunkA)
-        bytes = static_cast<uint32_t>((R + nrow) * rows * kEb);
+        bytes = static_cast<uint32_t>((rk + nrow) * rows * kEb);
       else if (kind == kChunkB)
         bytes = static_cast<uint32_t>(rows * e.w * kEb);
       else if (kind == kChunkY)
@@ -721,9 +751,9 @@ struct Kernel {
       else
         bytes = static_cast<uint32_t>(nrow * R * 4);
       mbar_arrive_expect_tx(sm.full(s), ok ? bytes : 0u);
-      if (kind == kChunkA && ok)
-        bulk_g2s(sm.stage_u32(s), Ak + static_cast<size_t>(e.y) * R,
-                 static_cast<uint32_t>(rows * R * kEb), sm.full(s), pol_w);
+      if (kind == kChunkA && ok && rk > 0)
+        bulk_g2s(sm.stage_u32(s), Ak + static_cast<size_t>(e.y) * rk,
+                 static_cast<uint32_t>(rows * rk * kEb), sm.full(s), pol_w);
     }
     // every lane follows lane 0's decision, so that the bytes announced are the bytes copied
     const bool ok = __shfl_sync(0xffffffffu, w.ok() ? 1 : 0, 0) != 0;
@@ -758,15 +788,21 @@ struct Kernel {
       __syncwarp();
       int* d = sm.desc(b);
       decode_item(p, S, grp.gid + li * grp.ng, starts, adapters, base, gcnt, d);
-      if (lane == 0) mbar_arrive(sm.fixed(kDescFull0 + b));
+      if (lane == 0) {  // the adapter's rank and scale travel with the item
+        d[6] = rank_of<R>(p, d[0]);
+        d[7] = __float_as_int(scale_of(p, d[0]));
+        mbar_arrive(sm.fixed(kDescFull0 + b));
+      }
+      __syncwarp();
       const int k = d[0];
+      const int rk = d[6];
       const int nrow = min(max(d[1], 0), kRowsMax);
       const T* Ak = nullptr;
       const T* Bk = nullptr;
       if (MODE != kExpand)
-        Ak = static_cast<const T*>(p.A_ptrs[k]) + static_cast<size_t>(p.layer) * p.h_in * R;
+        Ak = static_cast<const T*>(p.A_ptrs[k]) + static_cast<size_t>(p.layer) * p.h_in * rk;
       if (MODE != kShrink)
-        Bk = static_cast<const T*>(p.B_ptrs[k]) + static_cast<size_t>(p.layer) * R * p.h_out;
+        Bk = static_cast<const T*>(p.B_ptrs[k]) + static_cast<size_t>(p.layer) * rk * p.h_out;
       if (li == 0) build_table(mp, tab);  // the plan is the same for every item of this CTA
       for (int t = 0; t < total; ++t, rp.next(NST)) {
         if (!prior_done && rp.wrapped) {
@@ -781,7 +817,7 @@ struct Kernel {
             issue_acts(p, sm, (pre_ok >> q) & 1u, tab[q], q, d, nrow, pol_a);
         }
         const bool sok = issue_stage(p, sm, w, tab[t], rp, Ak, Bk, d, nrow, prior_done, pol_w,
-                                     pol_a);
+                                     pol_a, rk);
         if (!prior_done && sok) pre_ok |= 1u << t;
         issued |= 1u << rp.s;
         parity = (parity & ~(1u << rp.s)) | (rp.par << rp.s);
@@ -809,6 +845,11 @@ struct Kernel {
                                                       int* ctl) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NST = sm.nst;
+    // The item's adapter rank (R unless ranked) and the scale of its term.  Clamped like nrow:
+    // a CTA that has given up no longer waits for the descriptor, and whatever it then reads
+    // must still index inside its own stages.
+    const int rk = min(max(d[6], 0), R) & ~7;
+    const float sk = __int_as_float(d[7]);
     float acc[RB][kVec];
     float* vfull = sm.vfull_p;
     const uint32_t vfull_u32 = smem_addr(vfull);
@@ -817,7 +858,7 @@ struct Kernel {
       // ------------------------------------------------------------- v rows of the item
       w.wait<false>(sm.full(rp.s), rp.par);
       const float* vs = reinterpret_cast<const float*>(sm.stage(rp.s));
-      for (int t = tid; t < nrow * R; t += kConsumers) vfull[t] = p.scale * vs[t];
+      for (int t = tid; t < nrow * R; t += kConsumers) vfull[t] = sk * vs[t];
       named_bar(1, kConsumers);
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.empty(rp.s));
@@ -829,6 +870,7 @@ struct Kernel {
 #pragma unroll
         for (int e = 0; e < kVec; ++e) acc[i][e] = 0.f;
       const int cc = tid % kCpr, kl = tid / kCpr;  // compile-time divisors
+      const bool col_ok = cc * kVec < rk;          // columns past the rank read as zero
       const int xrow = p.kb * kEb;
       const int xoff = p.kb * R * kEb;
       int rows = min(mp.kbe, mp.kc);
@@ -845,7 +887,8 @@ struct Kernel {
             for (int u = 0; u < U; ++u) {
               const int kk = kk0 + u * kKLanes;
               if (kk < rows) {
-                a[u] = lds128(st + (kk * R + cc * kVec) * kEb);
+                a[u] = col_ok ? lds128(st + (kk * rk + cc * kVec) * kEb)
+                              : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int i = 0; i < RB; ++i)
                   xv[u][i] = static_cast<uint16_t>(lds16(xs + i * xrow + kk * kEb));
@@ -873,8 +916,13 @@ struct Kernel {
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const int kk = kk0 + u * kKLanes;
-            if (kk < rows) {
-              E::lds(st + (kk * R + cc * kVec) * kEb, a[u]);
+            if (kk < rows && col_ok) {
+              E::lds(st + (kk * rk + cc * kVec) * kEb, a[u]);
+#pragma unroll
+              for (int i = 0; i < RB; ++i) xv[u][i] = E::lds1(xs + i * xrow + kk * kEb);
+            } else if (kk < rows) {
+#pragma unroll
+              for (int e = 0; e < kVec; ++e) a[u][e] = 0.f;
 #pragma unroll
               for (int i = 0; i < RB; ++i) xv[u][i] = E::lds1(xs + i * xrow + kk * kEb);
             } else {
@@ -916,7 +964,7 @@ struct Kernel {
 #pragma unroll
           for (int ww = 0; ww < kConsumerWarps; ++ww) s += red[ww * kRowsMax * R + t];
           if (MODE == kFused) {
-            vfull[t] = s * p.scale;
+            vfull[t] = s * sk;
           } else if (w.ok()) {
             p.v_out[static_cast<size_t>(d[2 + t / R]) * R + (t % R)] = s;
           }
@@ -950,7 +998,7 @@ struct Kernel {
           float s = 0.f;
           for (int j = 0; j < grp.size; ++j) s += sm.vpart(li & 1, j)[t];
           if (MODE == kFused) {
-            vfull[t] = s * p.scale;
+            vfull[t] = s * sk;
           } else if ((t / R) % grp.size == grp.m && w.ok()) {
             p.v_out[static_cast<size_t>(d[2 + t / R]) * R + (t % R)] = s;
           }
@@ -978,7 +1026,7 @@ struct Kernel {
 #pragma unroll
           for (int e = 0; e < kVec; ++e) acc[i][e] = 0.f;
         for (int c0 = 0; c0 < R; c0 += cb, rp.next(NST)) {
-          const int rows = min(cb, R - c0);
+          const int rows = max(0, min(cb, rk - c0));  // B rows past the rank were not copied
           w.wait<false>(sm.full(rp.s), rp.par);
           if (active) {
             const uint32_t st = sm.stage_u32(rp.s) + my_ch * 16;

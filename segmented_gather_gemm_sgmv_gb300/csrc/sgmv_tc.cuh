@@ -73,6 +73,12 @@ static __device__ __forceinline__ void tile_rows(const Params& p, const int* sta
                                                  int p_hi, int* out) {
   const int lane = threadIdx.x & 31;
   const int k = adapters[lead];
+  if (p.rowmap) {  // a plan's group is one segment: its rows are consecutive in the row map
+    for (int q = lane; q < kTcRows; q += 32)
+      out[q] = p0 + q < p_hi ? __ldg(p.rowmap + starts[lead] + p0 + q) : -1;
+    __syncwarp();
+    return;
+  }
   for (int q = lane; q < kTcRows; q += 32) out[q] = -1;
   __syncwarp();
   int pos = 0;
@@ -275,11 +281,12 @@ struct TcRole {
       const int box_tok = my_box ? rt[8 * lane] : (pbox ? rt[prow] : 0);
       const int tile_tok = rt[0];
       const int k = c.adapters[lead];
+      const int rk = rank_of<R>(p, k);  // A / B hold rk columns / rows; the rest reads as zero
       const T* Ak = kDoShrink ? static_cast<const T*>(p.A_ptrs[k]) +
-                                    static_cast<size_t>(p.layer) * p.h_in * R
+                                    static_cast<size_t>(p.layer) * p.h_in * rk
                               : nullptr;
       const T* Bk = kDoExpand ? static_cast<const T*>(p.B_ptrs[k]) +
-                                    static_cast<size_t>(p.layer) * R * p.h_out
+                                    static_cast<size_t>(p.layer) * rk * p.h_out
                               : nullptr;
       // shrink slots: x rows [128 x 64] + A rows [64 x r]
       for (int kc = c.k_lo; kc < c.k_hi; ++kc, rg.next(c.slots)) {
@@ -316,8 +323,8 @@ struct TcRole {
         for (int u = lane; u < kTcK * kCpr; u += 32) {
           const int kr = u / kCpr, cc = u - kr * kCpr;
           const uint32_t d = dst + kASlotOff + sw128(kr, cc);
-          if (k0 + kr < p.h_in)
-            cp_async16(d, Ak + static_cast<size_t>(k0 + kr) * R + cc * 8);
+          if (k0 + kr < p.h_in && cc * 8 < rk)
+            cp_async16(d, Ak + static_cast<size_t>(k0 + kr) * rk + cc * 8);
           else
             cp_async16_zero(d, Ak);
         }
@@ -348,7 +355,9 @@ struct TcRole {
 #pragma unroll 4
         for (int u = lane; u < R * 8; u += 32) {
           const int kr = u >> 3, cc = u & 7;
-          if (cc < nvalid)
+          if (kr >= rk)  // past the adapter's rank: zeros (0 x stale data could be NaN)
+            cp_async16_zero(dst + sw128(kr, cc), Bk);
+          else if (cc < nvalid)
             cp_async16(dst + sw128(kr, cc), Bk + static_cast<size_t>(kr) * p.h_out + n0 + cc * 8);
         }
         if (!all_boxes) {
@@ -428,7 +437,8 @@ struct TcRole {
   // 16 columns [c0, c0 + 16) of this thread's v row (fp32): shrink only -> v_out; otherwise
   // scale -> 16-bit hi + lo -> TMEM.
   __device__ __forceinline__ static void finish16(const Params& p, uint32_t tq, int c0,
-                                                  const uint32_t (&v)[16], int tok_row) {
+                                                  const uint32_t (&v)[16], int tok_row,
+                                                  float sc) {
     if constexpr (MODE == kShrink) {
       if (tok_row >= 0) {
         float4* dst = reinterpret_cast<float4*>(p.v_out + static_cast<size_t>(tok_row) * R + c0);
@@ -441,7 +451,7 @@ struct TcRole {
       uint32_t hi[8], lo[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        split2(p.scale * __uint_as_float(v[2 * e]), p.scale * __uint_as_float(v[2 * e + 1]),
+        split2(sc * __uint_as_float(v[2 * e]), sc * __uint_as_float(v[2 * e + 1]),
                hi[e], lo[e]);
       tmem_st8(tq + kTmHi + c0 / 2, hi);
       tmem_st8(tq + kTmLo + c0 / 2, lo);
@@ -458,7 +468,7 @@ struct TcRole {
   // been read.
   __device__ __forceinline__ static bool exchange(const Params& p, const Ctx& c, const Waiter& w,
                                                   uint32_t tq, int q, int lane, int tok_row,
-                                                  uint32_t rnd, int* ctl) {
+                                                  uint32_t rnd, int* ctl, float sc) {
     const bool has_k = c.k_hi > c.k_lo;
     const uint32_t rs = c.xchg, ag = c.xchg + kTcHalfXchg;
     for (int j = 0; j < R / 16; ++j) {
@@ -520,12 +530,12 @@ struct TcRole {
         uint32_t v[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(sum[e]);
-        finish16(p, tq, 16 * j, v, tok_row);
+        finish16(p, tq, 16 * j, v, tok_row, sc);
         if constexpr (MODE == kFused) {
           uint32_t hi[8], lo[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            split2(p.scale * sum[2 * e], p.scale * sum[2 * e + 1], hi[e], lo[e]);
+            split2(sc * sum[2 * e], sc * sum[2 * e + 1], hi[e], lo[e]);
 #pragma unroll
           for (int pp = 0; pp < 4; ++pp) {
             if (pp == c.cr) continue;
@@ -589,6 +599,12 @@ struct TcRole {
         // is its expand fill.
         if (!__all_sync(0xffffffffu, w.until(tile_go, li))) return;
       }
+      float sc = p.scale;  // the scale of this m-tile's adapter
+      if (p.adapter_scale) {
+        int lead, p0, nrow;
+        c.tile(c.S, wk.mi, lead, p0, nrow);
+        sc = scale_of(p, c.adapters[lead]);
+      }
       if (g == 0) {  // the per-m-tile work: v into TMEM as hi / lo
         if constexpr (kDoShrink) {
           if (!wwait(w, c.fx(kTcVFull), li & 1)) return;
@@ -600,7 +616,7 @@ struct TcRole {
         tc_fence_after();
         if constexpr (kDoShrink) {
           if (c.split) {
-            if (!exchange(p, c, w, tq, q, lane, tok_row, rnd, ctl)) return;
+            if (!exchange(p, c, w, tq, q, lane, tok_row, rnd, ctl, sc)) return;
             rnd += R / 16;
           } else {
 #pragma unroll
@@ -608,7 +624,7 @@ struct TcRole {
               uint32_t v[16];
               tmem_ld16(tq + kTmV + c0, v);
               tmem_wait_ld();
-              finish16(p, tq, c0, v, tok_row);
+              finish16(p, tq, c0, v, tok_row, sc);
             }
           }
         } else {  // expand only: v rows from v_in
@@ -626,7 +642,7 @@ struct TcRole {
               v[4 * e + 2] = __float_as_uint(f.z);
               v[4 * e + 3] = __float_as_uint(f.w);
             }
-            finish16(p, tq, c0, v, tok_row);
+            finish16(p, tq, c0, v, tok_row, sc);
           }
         }
         if constexpr (kDoExpand) tmem_wait_st();
