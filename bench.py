@@ -334,6 +334,7 @@ class Setup:
 
 def capture_step(torch, fn, n, stream):
     """A CUDA graph of one step (n calls)."""
+    torch.cuda.synchronize()  # inputs made on other streams are complete before the first call
     with torch.cuda.stream(stream):
         for i in range(n):  # uncaptured first calls set the kernels' attributes
             fn(i, stream)
@@ -525,6 +526,102 @@ def measure_ranked(torch, device, stream, seconds):
     return out
 
 
+def measure_paging(torch, device, stream, seconds):
+    """Adapter paging (sgmv_pool_*): the decode_distinct shape (64 one-token segments, h = 4096,
+    r = 16, fp16, 32 layers) with 128 adapters in pinned host memory and a 64-slot device pool;
+    every step draws a new batch (64 distinct ids drawn by Zipf(1.2) weight over the 128, one
+    token each), acquires it (cold adapters are
+    copied on a copy stream while the previous step computes), replays the 32-layer graph and
+    releases it; no host wait between steps.  Beside it: the same steps with every adapter
+    resident (no pool)."""
+    from segmented_gather_gemm_sgmv_gb300 import AdapterPool, SgmvError, lora_apply
+    w = workloads.WORKLOADS["decode_distinct"]
+    n_adapters, slots, L, M = 128, 64, w.layers, 64
+    A, B = workloads.make_pool(w, device, seed=7, num_adapters=n_adapters)
+    hA = [A[k].cpu().contiguous().pin_memory() for k in range(n_adapters)]
+    hB = [B[k].cpu().contiguous().pin_memory() for k in range(n_adapters)]
+    pool = AdapterPool(slots, n_adapters, L, w.h_in, w.h_out, w.r, torch.float16, device=device)
+    for k in range(n_adapters):
+        pool.register(k, hA[k], hB[k])
+    rng = np.random.default_rng(11)
+    ss = np.arange(M + 1, dtype=np.int32)
+    d_ss = torch.as_tensor(ss, device=device)
+    # 64 requests per step, each with its own adapter: distinct ids drawn by Zipf(1.2) weight
+    # (hot adapters stay resident, cold ones stream in)
+    zw = np.arange(1, n_adapters + 1, dtype=np.float64) ** -1.2
+    batches = [rng.choice(n_adapters, size=M, replace=False, p=zw / zw.sum()).astype(np.int32)
+               for _ in range(64)]
+    host_sa = [torch.as_tensor(b).pin_memory() for b in batches]
+    d_sa = torch.as_tensor(batches[0], device=device)  # the table every step rewrites
+    acts = [workloads.make_activations(w, M, device, seed=500 + i) for i in range(L)]
+    res_A, res_B = workloads.pointer_table(A, device), workloads.pointer_table(B, device)
+    tables = {"pool": (pool.A_ptrs, pool.B_ptrs), "resident": (res_A, res_B)}
+    copy_s = torch.cuda.Stream(device)
+
+    def sweep(Ap, Bp):
+        def fn(i, stream=None):
+            x, y = acts[i]
+            lora_apply(y, x, Ap, Bp, d_ss, d_sa, i, w.r, w.scale, stream=stream,
+                       overlap_prior=True)
+        return fn
+
+    out = {"workload": "decode_distinct shape, 128 adapters on the host, 64-slot pool, 64 "
+                       "distinct ids per step drawn by Zipf(1.2) weight, 32-layer steps",
+           "slot_bytes": pool.slot_bytes}
+    nbytes_call, _ = algorithmic_bytes(w, ss, batches[0])
+    for label in ("resident", "pool"):
+        if label == "pool":  # the capture's first pass reads the pool's tables: fill them
+            pool.acquire(batches[0], copy_s, stream)
+            pool.release(batches[0], stream)
+        g = capture_step(torch, sweep(*tables[label]), L, stream)
+        copied = 0
+
+        def one(j):
+            nonlocal copied
+            b = batches[j % len(batches)]
+            if label == "pool":
+                while True:
+                    try:
+                        copied += pool.acquire(b, copy_s, stream)
+                        break
+                    except SgmvError as e:
+                        if e.status != -7:
+                            raise
+                        stream.synchronize()  # too few idle slots: let the last step finish
+            d_sa.copy_(host_sa[j % len(batches)], non_blocking=True)
+            g.replay()
+            if label == "pool":
+                pool.release(b, stream)
+
+        with torch.cuda.stream(stream):
+            for j in range(8):
+                one(j)
+            torch.cuda.synchronize()
+            copied = 0
+            n = 64
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for j in range(n):
+                one(8 + j)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        out[f"us_per_step_{label}"] = round(ms * 1e3, 2)
+        out[f"us_per_call_{label}"] = round(ms * 1e3 / L, 3)
+        if label == "pool":
+            out["adapters_copied_per_step"] = round(copied / n, 2)
+            out["copy_GB_per_step"] = round(copied / n * pool.slot_bytes / 1e9, 4)
+        del g
+    out["pool_stats"] = pool.stats()
+    out["launch"] = ("per step: sgmv_pool_acquire (copy stream), segment ids H2D, the 32-call "
+                     "lora_apply graph (SGMV_OVERLAP_PRIOR), sgmv_pool_release; no host waits")
+    pool.close()
+    del A, B, hA, hB, acts, pool
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_e2e(torch, setup, K, stream):
     """Public-API path with pinned host buffers.  Per call: ONE host->device copy of the call's
     inputs (x, y_in and the segment table packed in one pinned staging buffer), the lora_apply
@@ -652,6 +749,8 @@ def run_ours(args):
                                               args)
         per_config["qkv_multi"] = measure_multi(torch, device, stream, args.config_seconds)
         per_config["mixed_rank"] = measure_ranked(torch, device, stream, args.config_seconds)
+        if args.paging:
+            per_config["paging"] = measure_paging(torch, device, stream, args.config_seconds)
 
     w = workloads.WORKLOADS[args.workload]
     long_batch = {"auto": w.prefill, "on": True, "off": False}[args.long_batch]
@@ -821,6 +920,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per_config sweep of every named workload")
+    ap.add_argument("--paging", action="store_true",
+                    help="add the adapter-pool paging measurement to per_config")
     ap.add_argument("--config-seconds", type=float, default=0.4,
                     help="timed seconds per per_config measurement")
     ap.add_argument("--tensor-cores", choices=["auto", "never", "always"], default="auto",

@@ -76,7 +76,9 @@ typedef enum {
     SGMV_EUNSUPPORTED = -3,  /* rank not in {8,16,32,64}, sizes past the documented limits  */
     SGMV_ECUDA = -4,         /* a CUDA runtime call or launch failed                        */
     SGMV_ETIMEOUT = -5,      /* a bounded device-side wait ran out (see sgmv_get_error)     */
-    SGMV_EPLAN = -6          /* a planned call read an invalid plan (see sgmv_get_error)    */
+    SGMV_EPLAN = -6,         /* a planned call read an invalid plan (see sgmv_get_error)    */
+    SGMV_ENOSPACE = -7,      /* the adapter pool has too few free slots for the batch       */
+    SGMV_EBUSY = -8          /* the adapter's slot is read by a batch not yet released      */
 } sgmv_status_t;
 
 /* Largest num_segments one call accepts (the segment table is staged on chip). */
@@ -374,6 +376,73 @@ int lora_apply_ranked(void *y, int32_t ldy, const void *x, int32_t ldx,
                       const int32_t *seg_starts, const int32_t *seg_adapter, const void *plan,
                       int32_t num_segments, int32_t layer_idx, int32_t h_in, int32_t h_out,
                       int32_t r_max, sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream);
+
+/*
+ * ---- Adapter pool: device slots filled on demand from host copies ------------------------
+ * Source: section "Core Innovation 2: Decoupled Multi-Tenant Memory Architecture" (dynamic
+ * LoRA space allocation: adapter weights stream from host memory into a GPU pool
+ * asynchronously, so that loading a cold adapter overlaps the running batch) and the pointer
+ * arrays of section "Core Innovation 1".  The pool is host-side bookkeeping over device memory
+ * the caller owns: `slots` slots of sgmv_pool_slot_bytes() each in one slab, 256-byte aligned.
+ * Adapter k's host copy is its A block [L][h_in][r] and B block [L][r][h_out] (pinned host
+ * memory lets the copies overlap compute; pageable memory works but copies synchronously).
+ * Per batch: sgmv_pool_acquire (makes its adapters resident, pins their slots, writes the
+ * device pointer arrays the compute calls take), then the compute calls on compute_stream,
+ * then sgmv_pool_release (unpins; the slots may be refilled once the kernels enqueued before
+ * it have completed).  One pool serves one compute stream; calls on one pool are serialised
+ * by a mutex.  The pool allocates its host index and four pinned staging tables at creation
+ * and nothing afterwards.
+ */
+typedef struct sgmv_pool sgmv_pool_t;
+
+/* Bytes of one slot: the A and B blocks of one adapter, each rounded up to 256 bytes (0 for
+ * bad arguments). */
+size_t sgmv_pool_slot_bytes(int32_t layers, int32_t h_in, int32_t h_out, int32_t r,
+                            sgmv_dtype_t dtype);
+
+/*
+ * sgmv_pool_create -- a pool of `slots` slots in the caller's device slab (>= slots *
+ * sgmv_pool_slot_bytes(), 256-byte aligned, on the current device) for adapter ids
+ * [0, num_adapters).  *out receives the handle.  Returns SGMV_OK, SGMV_EINVAL, SGMV_EALIGN or
+ * SGMV_ECUDA.
+ */
+int sgmv_pool_create(sgmv_pool_t **out, void *slab, size_t slab_bytes, int32_t slots,
+                     int32_t num_adapters, int32_t layers, int32_t h_in, int32_t h_out,
+                     int32_t r, sgmv_dtype_t dtype);
+
+/* Waits for the pool's outstanding events and frees its host-side state (not the slab). */
+int sgmv_pool_destroy(sgmv_pool_t *pool);
+
+/* Where adapter k's host copy lives (host pointers, read by later acquires).  Re-registering
+ * a resident adapter drops its slot so that the next acquire copies the new weights
+ * (SGMV_EBUSY while an unreleased batch reads it). */
+int sgmv_pool_register(sgmv_pool_t *pool, int32_t adapter, const void *host_A,
+                       const void *host_B);
+
+/*
+ * sgmv_pool_acquire -- makes the adapters of ids[0..n) (a HOST array; negative ids are skipped,
+ * repeats count once) resident and pins their slots until sgmv_pool_release.  Each missing
+ * adapter takes the least-recently-used slot that is unpinned and whose last release has
+ * completed; its A and B blocks are copied on copy_stream.  compute_stream then waits for
+ * those copies, and d_A_ptrs / d_B_ptrs (device arrays of num_adapters pointers, as
+ * lora_apply takes them) are rewritten on compute_stream: entries of resident adapters point
+ * at their slots, the others are null.  *copied (may be null) receives the number of adapters
+ * copied.  Returns SGMV_OK, SGMV_EINVAL (an id past num_adapters or not registered),
+ * SGMV_ENOSPACE (more distinct adapters than free slots: nothing is changed), SGMV_EALIGN or
+ * SGMV_ECUDA.
+ */
+int sgmv_pool_acquire(sgmv_pool_t *pool, const int32_t *ids, int32_t n, void *d_A_ptrs,
+                      void *d_B_ptrs, sgmv_stream_t copy_stream, sgmv_stream_t compute_stream,
+                      int32_t *copied);
+
+/* Unpins the slots of ids[0..n) (host array) after the batch's kernels were enqueued on
+ * compute_stream; they become evictable once those kernels complete. */
+int sgmv_pool_release(sgmv_pool_t *pool, const int32_t *ids, int32_t n,
+                      sgmv_stream_t compute_stream);
+
+/* Counters: acquires that found an adapter resident / copied it, and the slots in use. */
+int sgmv_pool_stats(const sgmv_pool_t *pool, uint64_t *hits, uint64_t *misses,
+                    int32_t *resident);
 
 /*
  * sgmv_validate -- checks a segment table on the device and writes an OR of these bits to

@@ -3,7 +3,7 @@ shrink->expand, as a C-ABI CUDA library (libsgmv_gb300.so) with a thin Python bi
 
     from segmented_gather_gemm_sgmv_gb300 import lora_apply, sgmv_shrink, sgmv_expand
 """
-from .binding import (Plan, SgmvError, lora_apply, lora_apply_multi, lora_apply_planned,
+from .binding import (AdapterPool, Plan, SgmvError, lora_apply, lora_apply_multi, lora_apply_planned,
                       lora_apply_ranked,
                       sgmv_expand, sgmv_expand_planned, sgmv_get_error, sgmv_plan,
                       sgmv_plan_size, sgmv_set_wait_limit, sgmv_shrink, sgmv_shrink_planned,
@@ -11,5 +11,5 @@ from .binding import (Plan, SgmvError, lora_apply, lora_apply_multi, lora_apply_
 
 __all__ = ["lora_apply", "sgmv_shrink", "sgmv_expand", "sgmv_plan", "sgmv_plan_size",
            "lora_apply_planned", "sgmv_shrink_planned", "sgmv_expand_planned",
-           "lora_apply_multi", "lora_apply_ranked", "Plan", "sgmv_validate", "sgmv_validate_pointers",
+           "lora_apply_multi", "lora_apply_ranked", "AdapterPool", "Plan", "sgmv_validate", "sgmv_validate_pointers",
            "sgmv_get_error", "sgmv_set_wait_limit", "sgmv_version", "status_string", "SgmvError"]

@@ -18,6 +18,8 @@ _lib = None
 
 SGMV_OK, SGMV_EINVAL, SGMV_EALIGN, SGMV_EUNSUPPORTED, SGMV_ECUDA, SGMV_ETIMEOUT = 0, -1, -2, -3, -4, -5
 SGMV_EPLAN = -6
+SGMV_ENOSPACE = -7
+SGMV_EBUSY = -8
 SGMV_MAX_PROJECTIONS = 4
 PLAN_HEADER = 16  # int32 words before a plan's group table (include/sgmv.h)
 SGMV_MAX_SEGMENTS = 4096
@@ -32,7 +34,8 @@ SYMBOLS = ("lora_apply", "lora_apply_ex", "lora_apply_strided", "sgmv_shrink", "
            "sgmv_validate", "sgmv_validate_pointers", "sgmv_get_error", "sgmv_set_wait_limit",
            "sgmv_status_string", "sgmv_version", "sgmv_plan_size", "sgmv_plan",
            "lora_apply_planned", "sgmv_shrink_planned", "sgmv_expand_planned", "lora_apply_multi",
-           "lora_apply_ranked")
+           "lora_apply_ranked", "sgmv_pool_slot_bytes", "sgmv_pool_create", "sgmv_pool_destroy",
+           "sgmv_pool_register", "sgmv_pool_acquire", "sgmv_pool_release", "sgmv_pool_stats")
 
 
 class Projection(ctypes.Structure):
@@ -94,13 +97,23 @@ def lib(build_if_stale: bool = True) -> ctypes.CDLL:
                                        u32, vp]
         L.lora_apply_ranked.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32,
                                         i32, i32, i32, ci, u32, vp]
+        L.sgmv_pool_slot_bytes.argtypes = [i32, i32, i32, i32, ci]
+        L.sgmv_pool_slot_bytes.restype = ctypes.c_size_t
+        L.sgmv_pool_create.argtypes = [ctypes.POINTER(vp), vp, ctypes.c_size_t, i32, i32, i32,
+                                       i32, i32, i32, ci]
+        L.sgmv_pool_destroy.argtypes = [vp]
+        L.sgmv_pool_register.argtypes = [vp, i32, vp, vp]
+        L.sgmv_pool_acquire.argtypes = [vp, vp, i32, vp, vp, vp, vp, ctypes.POINTER(i32)]
+        L.sgmv_pool_release.argtypes = [vp, vp, i32, vp]
+        L.sgmv_pool_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64),
+                                      ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(i32)]
         L.sgmv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
         L.sgmv_set_wait_limit.argtypes = [ctypes.c_uint64, i32]
         L.sgmv_status_string.argtypes = [ctypes.c_int]
         L.sgmv_status_string.restype = ctypes.c_char_p
         L.sgmv_version.argtypes = []
         for name in SYMBOLS:
-            if name not in ("sgmv_status_string", "sgmv_plan_size"):
+            if name not in ("sgmv_status_string", "sgmv_plan_size", "sgmv_pool_slot_bytes"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
         return L
@@ -519,3 +532,86 @@ def lora_apply_ranked(y, x, A_ptrs, B_ptrs, adapter_rank, adapter_scale, layer_i
             x.shape[1], y.shape[1], int(r_max), _dtype_code(x), flags, _stream(stream, x.device))
     _check(rc, "lora_apply_ranked")
     return y
+
+
+# ----------------------------------------------------------------------- adapter pool ----
+class AdapterPool:
+    """sgmv_pool_*: `slots` device slots (one adapter's A and B blocks each) in a device slab the
+    binding allocates with torch, filled on demand from registered host copies (pinned CPU
+    tensors).  acquire() returns how many adapters it copied; the device pointer tables it
+    writes (A_ptrs / B_ptrs, int64 [num_adapters]) are what lora_apply takes."""
+
+    def __init__(self, slots, num_adapters, layers, h_in, h_out, r, dtype, device=None):
+        import torch
+        device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.code = _dtype_code(torch.empty(0, dtype=dtype))
+        self.slot_bytes = int(lib().sgmv_pool_slot_bytes(layers, h_in, h_out, r, self.code))
+        if self.slot_bytes == 0:
+            raise ValueError("bad pool shape")
+        self.slab = torch.empty(slots * self.slot_bytes + 256, dtype=torch.uint8, device=device)
+        off = (-self.slab.data_ptr()) % 256
+        self.num_adapters = int(num_adapters)
+        self.A_ptrs = torch.zeros(num_adapters, dtype=torch.int64, device=device)
+        self.B_ptrs = torch.zeros(num_adapters, dtype=torch.int64, device=device)
+        self._keep = {}
+        self.handle = ctypes.c_void_p()
+        with torch.cuda.device(device):
+            _check(lib().sgmv_pool_create(ctypes.byref(self.handle), self.slab.data_ptr() + off,
+                                          slots * self.slot_bytes, int(slots), int(num_adapters),
+                                          int(layers), int(h_in), int(h_out), int(r), self.code),
+                   "sgmv_pool_create")
+        self.device = device
+
+    def register(self, adapter, host_A, host_B):
+        for t in (host_A, host_B):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("host copies must be contiguous CPU tensors (pinned: async)")
+        _check(lib().sgmv_pool_register(self.handle, int(adapter), host_A.data_ptr(),
+                                        host_B.data_ptr()), "sgmv_pool_register")
+        self._keep[int(adapter)] = (host_A, host_B)
+
+    def _ids(self, ids):
+        import numpy as np
+        arr = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        return arr, arr.ctypes.data
+
+    def acquire(self, ids, copy_stream, compute_stream) -> int:
+        arr, ptr = self._ids(ids)
+        copied = ctypes.c_int32(0)
+        with torch_device(self.device):
+            _check(lib().sgmv_pool_acquire(self.handle, ptr, len(arr), self.A_ptrs.data_ptr(),
+                                           self.B_ptrs.data_ptr(),
+                                           ctypes.c_void_p(copy_stream.cuda_stream),
+                                           ctypes.c_void_p(compute_stream.cuda_stream),
+                                           ctypes.byref(copied)), "sgmv_pool_acquire")
+        return int(copied.value)
+
+    def release(self, ids, compute_stream):
+        arr, ptr = self._ids(ids)
+        with torch_device(self.device):
+            _check(lib().sgmv_pool_release(self.handle, ptr, len(arr),
+                                           ctypes.c_void_p(compute_stream.cuda_stream)),
+                   "sgmv_pool_release")
+
+    def stats(self):
+        h, m, r = ctypes.c_uint64(0), ctypes.c_uint64(0), ctypes.c_int32(0)
+        _check(lib().sgmv_pool_stats(self.handle, ctypes.byref(h), ctypes.byref(m),
+                                     ctypes.byref(r)), "sgmv_pool_stats")
+        return {"hits": int(h.value), "misses": int(m.value), "resident": int(r.value)}
+
+    def close(self):
+        if self.handle:
+            with torch_device(self.device):
+                lib().sgmv_pool_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def torch_device(device):
+    import torch
+    return torch.cuda.device(device)

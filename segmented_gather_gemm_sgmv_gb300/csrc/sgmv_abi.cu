@@ -960,6 +960,8 @@ const char* sgmv_status_string(int status) {
     case SGMV_ECUDA: return "SGMV_ECUDA: CUDA runtime error";
     case SGMV_ETIMEOUT: return "SGMV_ETIMEOUT: a device-side wait ran out";
     case SGMV_EPLAN: return "SGMV_EPLAN: a planned call was given an invalid plan";
+    case SGMV_ENOSPACE: return "SGMV_ENOSPACE: too few free adapter-pool slots for the batch";
+    case SGMV_EBUSY: return "SGMV_EBUSY: the adapter's slot is read by an unreleased batch";
     default: return "unknown status";
   }
 }

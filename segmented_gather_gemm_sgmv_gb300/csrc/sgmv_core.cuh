@@ -837,7 +837,9 @@ struct Kernel {
   }
 
   // --------------------------------------------------------------- consumer warps ----
-  template <int RB>
+  // kRanked: the call has per-adapter ranks (rk read from the descriptor); otherwise rk is the
+  // compile-time R, so that the hot loops keep constant strides.
+  template <int RB, bool kRanked>
   __device__ __forceinline__ static void consume_item(const Params& p, const Smem& sm,
                                                       const Waiter& w, const Group& grp,
                                                       const MemberPlan& mp, int li, bool last,
@@ -848,7 +850,7 @@ struct Kernel {
     // The item's adapter rank (R unless ranked) and the scale of its term.  Clamped like nrow:
     // a CTA that has given up no longer waits for the descriptor, and whatever it then reads
     // must still index inside its own stages.
-    const int rk = min(max(d[6], 0), R) & ~7;
+    const int rk = kRanked ? min(max(d[6], 0), R) & ~7 : R;
     const float sk = __int_as_float(d[7]);
     float acc[RB][kVec];
     float* vfull = sm.vfull_p;
@@ -1106,12 +1108,21 @@ struct Kernel {
       const int* d = sm.desc(li & 1);
       const int nrow = min(max(d[1], 0), kRowsMax);
       const bool last = li == n_my - 1;
-      if (nrow <= 1)
-        consume_item<1>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
-      else if (nrow <= 2)
-        consume_item<2>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
-      else
-        consume_item<kRowsMax>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
+      if (p.adapter_rank) {
+        if (nrow <= 1)
+          consume_item<1, true>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
+        else if (nrow <= 2)
+          consume_item<2, true>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
+        else
+          consume_item<kRowsMax, true>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
+      } else {
+        if (nrow <= 1)
+          consume_item<1, false>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
+        else if (nrow <= 2)
+          consume_item<2, false>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
+        else
+          consume_item<kRowsMax, false>(p, sm, w, grp, mp, li, last, rp, d, nrow, ctl);
+      }
     }
     // keep every thread's cluster barrier sequence: wait #1, arrive #2 (done per item above
     // when the group exchanges partial products)

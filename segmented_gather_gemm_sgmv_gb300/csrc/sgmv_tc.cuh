@@ -319,14 +319,26 @@ struct TcRole {
           }
         }
         constexpr int kCpr = R / 8;  // 16-byte chunks per A row
+        if (rk == R) {  // every unranked call: constant strides
 #pragma unroll 4
-        for (int u = lane; u < kTcK * kCpr; u += 32) {
-          const int kr = u / kCpr, cc = u - kr * kCpr;
-          const uint32_t d = dst + kASlotOff + sw128(kr, cc);
-          if (k0 + kr < p.h_in && cc * 8 < rk)
-            cp_async16(d, Ak + static_cast<size_t>(k0 + kr) * rk + cc * 8);
-          else
-            cp_async16_zero(d, Ak);
+          for (int u = lane; u < kTcK * kCpr; u += 32) {
+            const int kr = u / kCpr, cc = u - kr * kCpr;
+            const uint32_t d = dst + kASlotOff + sw128(kr, cc);
+            if (k0 + kr < p.h_in)
+              cp_async16(d, Ak + static_cast<size_t>(k0 + kr) * R + cc * 8);
+            else
+              cp_async16_zero(d, Ak);
+          }
+        } else {
+#pragma unroll 4
+          for (int u = lane; u < kTcK * kCpr; u += 32) {
+            const int kr = u / kCpr, cc = u - kr * kCpr;
+            const uint32_t d = dst + kASlotOff + sw128(kr, cc);
+            if (k0 + kr < p.h_in && cc * 8 < rk)
+              cp_async16(d, Ak + static_cast<size_t>(k0 + kr) * rk + cc * 8);
+            else
+              cp_async16_zero(d, Ak);
+          }
         }
         cp_async_arrive(bar);
         issued |= 1u << rg.s;
@@ -352,13 +364,24 @@ struct TcRole {
           else if (pbox == 16) tma_load_2d(d, &p.tmap_y16, n0, box_tok, bar);
           else tma_load_2d(d, &p.tmap_y8, n0, box_tok, bar);
         }
+        if (rk == R) {  // every unranked call
 #pragma unroll 4
-        for (int u = lane; u < R * 8; u += 32) {
-          const int kr = u >> 3, cc = u & 7;
-          if (kr >= rk)  // past the adapter's rank: zeros (0 x stale data could be NaN)
-            cp_async16_zero(dst + sw128(kr, cc), Bk);
-          else if (cc < nvalid)
-            cp_async16(dst + sw128(kr, cc), Bk + static_cast<size_t>(kr) * p.h_out + n0 + cc * 8);
+          for (int u = lane; u < R * 8; u += 32) {
+            const int kr = u >> 3, cc = u & 7;
+            if (cc < nvalid)
+              cp_async16(dst + sw128(kr, cc),
+                         Bk + static_cast<size_t>(kr) * p.h_out + n0 + cc * 8);
+          }
+        } else {
+#pragma unroll 4
+          for (int u = lane; u < R * 8; u += 32) {
+            const int kr = u >> 3, cc = u & 7;
+            if (kr >= rk)  // past the adapter's rank: zeros (0 x stale data could be NaN)
+              cp_async16_zero(dst + sw128(kr, cc), Bk);
+            else if (cc < nvalid)
+              cp_async16(dst + sw128(kr, cc),
+                         Bk + static_cast<size_t>(kr) * p.h_out + n0 + cc * 8);
+          }
         }
         if (!all_boxes) {
           for (int u = lane; u < kTcRows * 8; u += 32) {

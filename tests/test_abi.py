@@ -43,13 +43,14 @@ def test_header_constants_match_binding():
     assert "#define SGMV_MAX_LD (1 << 24)" in text and binding.SGMV_MAX_LD == 1 << 24
     assert f"#define SGMV_MAX_PROJECTIONS {binding.SGMV_MAX_PROJECTIONS}" in text
     for name, val in [("SGMV_EINVAL", -1), ("SGMV_EALIGN", -2), ("SGMV_EUNSUPPORTED", -3),
-                      ("SGMV_ECUDA", -4), ("SGMV_ETIMEOUT", -5), ("SGMV_EPLAN", -6)]:
+                      ("SGMV_ECUDA", -4), ("SGMV_ETIMEOUT", -5), ("SGMV_EPLAN", -6),
+                      ("SGMV_ENOSPACE", -7), ("SGMV_EBUSY", -8)]:
         assert re.search(rf"{name}\s*=\s*{val}\b", text), name
 
 
 def test_version_and_strings(L):
     assert L.sgmv_version() == 200
-    for s in (0, -1, -2, -3, -4, -5, -6):
+    for s in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert binding.status_string(s).startswith("SGMV_")
 
 
@@ -230,3 +231,24 @@ def test_multi_host_checks(L):
     assert multi([proj()], plan=None) == -1
     assert multi([proj()], r=24) == -3
     assert multi([proj()], flags=16) == -1
+
+
+def test_pool_host_checks(L):
+    """The adapter pool's size formula and the checks it makes before any CUDA call."""
+    import ctypes
+    assert L.sgmv_pool_slot_bytes(2, 4096, 4096, 16, 1) == 2 * (2 * 4096 * 16 * 2)
+    assert L.sgmv_pool_slot_bytes(1, 100, 60, 8, 0) == 3328 + 2048  # each block up to 256 B
+    assert L.sgmv_pool_slot_bytes(0, 4096, 4096, 16, 1) == 0
+    assert L.sgmv_pool_slot_bytes(1, 4096, 4096, 16, 9) == 0
+    h = ctypes.c_void_p()
+    sb = L.sgmv_pool_slot_bytes(1, 256, 256, 16, 1)
+    assert L.sgmv_pool_create(None, P, 4 * sb, 4, 8, 1, 256, 256, 16, 1) == -1
+    assert L.sgmv_pool_create(ctypes.byref(h), None, 4 * sb, 4, 8, 1, 256, 256, 16, 1) == -1
+    assert L.sgmv_pool_create(ctypes.byref(h), P, 4 * sb, 0, 8, 1, 256, 256, 16, 1) == -1
+    assert L.sgmv_pool_create(ctypes.byref(h), P, 3 * sb, 4, 8, 1, 256, 256, 16, 1) == -1
+    assert L.sgmv_pool_create(ctypes.byref(h), P + 16, 4 * sb, 4, 8, 1, 256, 256, 16, 1) == -2
+    assert L.sgmv_pool_destroy(None) == -1
+    assert L.sgmv_pool_register(None, 0, P, P) == -1
+    assert L.sgmv_pool_acquire(None, None, 0, P, P, None, None, None) == -1
+    assert L.sgmv_pool_release(None, None, 0, None) == -1
+    assert L.sgmv_pool_stats(None, None, None, None) == -1

@@ -37,6 +37,7 @@ def run_chain(c, layers, long_batch, seed=40):
     sets = [workloads.make_activations(c.w, c.M, "cuda", seed=seed + i) for i in range(len(layers))]
     ys = [y0.clone() for _, y0 in sets]
     stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())  # inputs made on the default stream
 
     def chain():
         for (x, _), y, layer in zip(sets, ys, layers):

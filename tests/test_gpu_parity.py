@@ -313,6 +313,7 @@ def test_overlap_prior_chain(use_graph):
     ys = [c.y0.clone() * 0.5 for _ in range(n)]
     x0 = c.x.clone()
     stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())  # inputs made on the default stream
 
     def chain():
         x = x0

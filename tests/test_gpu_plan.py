@@ -130,6 +130,7 @@ def test_planned_layer_sweep_decode_distinct():
     sets = [workloads.make_activations(w, c.M, "cuda", seed=70 + i) for i in range(w.layers)]
     ys = [y0.clone() for _, y0 in sets]
     stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())  # inputs made on the default stream
 
     def sweep():
         for i, ((x, _), y) in enumerate(zip(sets, ys)):
