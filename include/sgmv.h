@@ -89,6 +89,8 @@ typedef enum {
 #define SGMV_MAX_LD (1 << 24)
 /* Largest number of projections of one lora_apply_multi call. */
 #define SGMV_MAX_PROJECTIONS 4
+/* Largest row capacity (max_rows) of lora_apply_static_plan. */
+#define SGMV_STATIC_PLAN_MAX_ROWS 65536
 
 /*
  * lora_apply -- the fused path: y[t] += scale * (x[t] . A_k) . B_k for every segment row.
@@ -347,6 +349,37 @@ typedef struct {
 int lora_apply_multi(const sgmv_projection_t *proj, int32_t num_proj, const void *plan,
                      int32_t num_segments, int32_t layer_idx, int32_t r, sgmv_dtype_t dtype,
                      uint32_t flags, sgmv_stream_t stream);
+
+/*
+ * lora_apply_static_plan -- lora_apply_planned for callers that cannot allocate device memory:
+ * the library builds the plan itself (sgmv_plan) into a fixed array inside the library
+ * instead of a caller-provided buffer, then applies it; the caller passes only inputs and
+ * outputs.  The pages describe no counterpart: it is a deployment variant.  Callers in this
+ * position are, for example, an inference runtime that reserves all device memory at start-up
+ * through its own allocator and forbids cudaMalloc afterwards (a fixed memory budget, no
+ * fragmentation), or a plugin interface that gives an operator no way to request a workspace.
+ *   seg_starts, seg_adapter, num_segments  the device table, as for lora_apply
+ *   max_rows       the plan's row capacity (>= the rows of the table that have an adapter)
+ *   other arguments as for lora_apply_planned (ldx / ldy as for lora_apply_strided)
+ * Limits: num_segments <= SGMV_MAX_SEGMENTS and max_rows <= SGMV_STATIC_PLAN_MAX_ROWS, else
+ * SGMV_EUNSUPPORTED.  The array holds one plan of that size (about 295 KB), is created on every
+ * device that loads the library and stays there until the process exits.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, once per device); make
+ * that first call before any stream capture.  The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ * Sharing: every call, on every stream, uses the same array, which keeps the last call's plan
+ * (the plan kernel rewrites every word the apply kernel reads, so nothing needs clearing).
+ * Calls that overlap on the GPU -- on two streams, or two host threads -- race on it: order
+ * them.  SGMV_OVERLAP_PRIOR is rejected (SGMV_EINVAL): the apply kernel must wait for the
+ * plan kernel enqueued just before it.  Errors otherwise as for sgmv_plan and
+ * lora_apply_planned; nothing is enqueued on a host-checked error.
+ */
+int lora_apply_static_plan(void *y, int32_t ldy, const void *x, int32_t ldx,
+                           const void *const *A_ptrs, const void *const *B_ptrs,
+                           const int32_t *seg_starts, const int32_t *seg_adapter,
+                           int32_t num_segments, int32_t max_rows, int32_t layer_idx,
+                           int32_t h_in, int32_t h_out, int32_t r, float scale,
+                           sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream);
 
 /*
  * lora_apply_ranked -- the fused LoRA term with a rank and a scale of its own for every

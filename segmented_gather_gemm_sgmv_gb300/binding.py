@@ -21,6 +21,7 @@ SGMV_EPLAN = -6
 SGMV_ENOSPACE = -7
 SGMV_EBUSY = -8
 SGMV_MAX_PROJECTIONS = 4
+SGMV_STATIC_PLAN_MAX_ROWS = 65536
 PLAN_HEADER = 16  # int32 words before a plan's group table (include/sgmv.h)
 SGMV_MAX_SEGMENTS = 4096
 SGMV_MAX_HIDDEN = 65536
@@ -35,7 +36,8 @@ SYMBOLS = ("lora_apply", "lora_apply_ex", "lora_apply_strided", "sgmv_shrink", "
            "sgmv_status_string", "sgmv_version", "sgmv_plan_size", "sgmv_plan",
            "lora_apply_planned", "sgmv_shrink_planned", "sgmv_expand_planned", "lora_apply_multi",
            "lora_apply_ranked", "sgmv_pool_slot_bytes", "sgmv_pool_create", "sgmv_pool_destroy",
-           "sgmv_pool_register", "sgmv_pool_acquire", "sgmv_pool_release", "sgmv_pool_stats")
+           "sgmv_pool_register", "sgmv_pool_acquire", "sgmv_pool_release", "sgmv_pool_stats",
+           "lora_apply_static_plan")
 
 
 class Projection(ctypes.Structure):
@@ -107,6 +109,8 @@ def lib(build_if_stale: bool = True) -> ctypes.CDLL:
         L.sgmv_pool_release.argtypes = [vp, vp, i32, vp]
         L.sgmv_pool_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64),
                                       ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(i32)]
+        L.lora_apply_static_plan.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, i32, i32, i32,
+                                             i32, i32, i32, f32, ci, u32, vp]
         L.sgmv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
         L.sgmv_set_wait_limit.argtypes = [ctypes.c_uint64, i32]
         L.sgmv_status_string.argtypes = [ctypes.c_int]
@@ -436,6 +440,26 @@ def lora_apply_planned(y, x, A_ptrs, B_ptrs, plan: Plan, layer_idx, r, scale, st
             plan.buf.data_ptr(), plan.num_segments, int(layer_idx), x.shape[1], y.shape[1],
             int(r), float(scale), _dtype_code(x), flags, _stream(stream, x.device))
     _check(rc, "lora_apply_planned")
+    return y
+
+
+def lora_apply_static_plan(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, max_rows, layer_idx, r,
+                           scale, stream=None, tensor_cores="auto", long_batch=False):
+    """lora_apply_planned with the plan built inside the library's fixed device array: the call
+    allocates no device memory (for callers that may not).  Calls that overlap on the GPU
+    share that array and must be ordered; overlap_prior is not available here."""
+    ldy, ldx = _rows(y, "y"), _rows(x, "x")
+    if x.dtype != y.dtype or x.shape[0] != y.shape[0]:
+        raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
+    S = _table(seg_starts, seg_adapter)
+    flags = _flags(False, tensor_cores, long_batch)
+    with _on(x, y, A_ptrs, B_ptrs, seg_starts, seg_adapter):
+        rc = lib().lora_apply_static_plan(
+            y.data_ptr(), ldy, x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
+            seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(max_rows), int(layer_idx),
+            x.shape[1], y.shape[1], int(r), float(scale), _dtype_code(x), flags,
+            _stream(stream, x.device))
+    _check(rc, "lora_apply_static_plan")
     return y
 
 

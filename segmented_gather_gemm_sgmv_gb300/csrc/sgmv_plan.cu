@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "sgmv.h"
 #include "sgmv_core.cuh"
@@ -196,9 +197,74 @@ __global__ void __launch_bounds__(kPlanThreads)
   }
 }
 
+// ---- lora_apply_static_plan: the plan in a fixed device array instead of caller memory ----
+// Some callers cannot allocate device memory when they call the library (see the header): the
+// plan, the only scratch memory of the planned path, then lives in this file-scope array,
+// sized for SGMV_MAX_SEGMENTS segments and SGMV_STATIC_PLAN_MAX_ROWS rows.  Every device that
+// loads the library holds it until the process exits.  The plan kernel rewrites every word the
+// apply kernel reads, so nothing in it has to be cleared between calls.
+constexpr size_t kStaticPlanWords = static_cast<size_t>(sgmv::kPlanHeader) +
+                                    2 * static_cast<size_t>(SGMV_MAX_SEGMENTS) + 1 +
+                                    static_cast<size_t>(SGMV_STATIC_PLAN_MAX_ROWS);
+static __device__ __align__(256) int32_t g_static_plan[kStaticPlanWords];
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_static_once[kMaxDevices];
+int32_t* g_static_addr[kMaxDevices] = {};
+int g_static_rc[kMaxDevices] = {};
+
+// The array's device address on the current device, looked up once per device (with that
+// device current).  In host code the array's name is only a host-side stand-in.
+int static_plan_address(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SGMV_ECUDA;
+  std::call_once(g_static_once[dev], [dev] {
+    void* ptr = nullptr;
+    const cudaError_t rc = cudaGetSymbolAddress(&ptr, g_static_plan);
+    g_static_rc[dev] = rc == cudaSuccess && ptr ? SGMV_OK : SGMV_ECUDA;
+    g_static_addr[dev] = static_cast<int32_t*>(ptr);
+  });
+  if (g_static_rc[dev] != SGMV_OK) return g_static_rc[dev];
+  *out = g_static_addr[dev];
+  return SGMV_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int lora_apply_static_plan(void* y, int32_t ldy, const void* x, int32_t ldx,
+                           const void* const* A_ptrs, const void* const* B_ptrs,
+                           const int32_t* seg_starts, const int32_t* seg_adapter,
+                           int32_t num_segments, int32_t max_rows, int32_t layer_idx,
+                           int32_t h_in, int32_t h_out, int32_t r, float scale,
+                           sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream) {
+  if (num_segments < 0 || max_rows < 0 || !seg_starts || (num_segments > 0 && !seg_adapter))
+    return SGMV_EINVAL;
+  if (num_segments > SGMV_MAX_SEGMENTS || max_rows > SGMV_STATIC_PLAN_MAX_ROWS)
+    return SGMV_EUNSUPPORTED;
+  // The apply kernel reads the plan that the kernel just before it writes: it must wait for
+  // that kernel, so it cannot be launched as its programmatic dependent.
+  if (flags & SGMV_OVERLAP_PRIOR) return SGMV_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(seg_starts) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seg_adapter) & 3u))
+    return SGMV_EALIGN;
+  // Every argument of the apply call is checked before anything is enqueued: with no segments
+  // the planned call runs its host checks only and never reads the plan pointer (any non-null
+  // 16-byte-aligned value passes its own check).
+  const void* const kChecksOnly = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+  int rc = lora_apply_planned(y, ldy, x, ldx, A_ptrs, B_ptrs, kChecksOnly, 0, layer_idx, h_in,
+                              h_out, r, scale, dtype, flags, stream);
+  if (rc != SGMV_OK) return rc;
+  if (num_segments == 0) return SGMV_OK;
+  int32_t* plan = nullptr;
+  if ((rc = static_plan_address(&plan)) != SGMV_OK) return rc;
+  if ((rc = sgmv_plan(seg_starts, seg_adapter, num_segments, max_rows, plan,
+                      sizeof(int32_t) * kStaticPlanWords, stream)) != SGMV_OK)
+    return rc;
+  return lora_apply_planned(y, ldy, x, ldx, A_ptrs, B_ptrs, plan, num_segments, layer_idx, h_in,
+                            h_out, r, scale, dtype, flags, stream);
+}
 
 size_t sgmv_plan_size(int32_t num_segments, int32_t max_rows) {
   if (num_segments < 0 || max_rows < 0 || num_segments > SGMV_MAX_SEGMENTS) return 0;

@@ -42,6 +42,7 @@ def test_header_constants_match_binding():
     assert f"#define SGMV_LONG_BATCH {binding.SGMV_LONG_BATCH}u" in text
     assert "#define SGMV_MAX_LD (1 << 24)" in text and binding.SGMV_MAX_LD == 1 << 24
     assert f"#define SGMV_MAX_PROJECTIONS {binding.SGMV_MAX_PROJECTIONS}" in text
+    assert f"#define SGMV_STATIC_PLAN_MAX_ROWS {binding.SGMV_STATIC_PLAN_MAX_ROWS}" in text
     for name, val in [("SGMV_EINVAL", -1), ("SGMV_EALIGN", -2), ("SGMV_EUNSUPPORTED", -3),
                       ("SGMV_ECUDA", -4), ("SGMV_ETIMEOUT", -5), ("SGMV_EPLAN", -6),
                       ("SGMV_ENOSPACE", -7), ("SGMV_EBUSY", -8)]:
