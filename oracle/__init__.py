@@ -121,6 +121,9 @@ class OracleLib:
                                                  i32]
         lib.oracle_lora_apply_ranked.restype = ctypes.c_int
         lib.oracle_plan.restype = ctypes.c_int32
+        lib.oracle_base_lora.argtypes = [dp, dp, dp, dp, dp, dp, dp, i32, i32, i32, i32, i32,
+                                         i32, ctypes.c_double]
+        lib.oracle_base_lora.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -222,6 +225,31 @@ class OracleLib:
             raise MemoryError("oracle_lora_apply_ranked failed")
         return y
 
+    def base_lora(self, x, W0, A_blocks, B_blocks, seg_starts, seg_adapter, layer_idx, scale):
+        """Return y = x W0^T + scale * (x A_k) B_k per segment row (fp64, a new array).
+
+        x: (M, h_in); W0: (h_out, h_in), one row per output feature; A_blocks / B_blocks as for
+        lora_apply.  Rows outside every segment, or of a segment without an adapter, get the
+        base projection only.
+        """
+        x = _f64(x)
+        W0 = _f64(W0)
+        M, h_in = x.shape
+        h_out = W0.shape[0]
+        if W0.shape[1] != h_in:
+            raise ValueError("W0 must be (h_out, h_in)")
+        ss, sa = _i32(seg_starts), _i32(seg_adapter)
+        _check_segments(ss, sa, len(A_blocks), M)
+        y = np.full((M, h_out), np.nan)  # every element is written
+        At, Bt = _PtrTable(A_blocks), _PtrTable(B_blocks)
+        rc = self.lib.oracle_base_lora(y.ctypes.data, x.ctypes.data, W0.ctypes.data, At.ptr,
+                                       Bt.ptr, ss.ctypes.data, sa.ctypes.data, len(sa), M,
+                                       int(layer_idx), h_in, h_out, _rank(A_blocks),
+                                       float(scale))
+        if rc != 0:
+            raise MemoryError("oracle_base_lora failed")
+        return y
+
     def plan(self, seg_starts, seg_adapter, max_rows):
         """The adapter grouping of a table: (g_starts[G+1], g_adapter[G], rows[n]) as int32
         arrays, or None when more than max_rows rows would be listed."""
@@ -275,6 +303,10 @@ def lora_apply_ranked(*args, **kw):
     return _load().lora_apply_ranked(*args, **kw)
 
 
+def base_lora(*args, **kw):
+    return _load().base_lora(*args, **kw)
+
+
 lora_apply.__doc__ = OracleLib.lora_apply.__doc__
 sgmv_shrink.__doc__ = OracleLib.sgmv_shrink.__doc__
 sgmv_expand.__doc__ = OracleLib.sgmv_expand.__doc__
@@ -282,6 +314,7 @@ validate.__doc__ = OracleLib.validate.__doc__
 validate_pointers.__doc__ = OracleLib.validate_pointers.__doc__
 plan.__doc__ = OracleLib.plan.__doc__
 lora_apply_ranked.__doc__ = OracleLib.lora_apply_ranked.__doc__
+base_lora.__doc__ = OracleLib.base_lora.__doc__
 
 
 class PreparedApply:

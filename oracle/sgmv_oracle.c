@@ -244,3 +244,32 @@ int oracle_lora_apply_ranked(double *y, const double *x, const double *const *A,
     free(v);
     return 0;
 }
+
+/* y[t] = x[t] W0 + scale * (x[t] A_k) B_k -- both terms of the per-request equation
+ * ("Punica Guide: Multi-Tenant LoRA Serving with SGMV", section "The Heterogeneous Batching
+ * Bottleneck", y_i = x_i W0 + (alpha/r) x_i A B, and the figure of the same section in which
+ * the base GEMM feeds the fused SGMV kernel; section "Step-by-Step Implementation", the
+ * dispatcher's base output plus its delta).  The base weight is stored as a linear layer
+ * keeps it, one row per output feature: W0 is [h_out][h_in] row-major, so the equation's
+ * x_i W0 is sum_j x[t][j] * W0[n][j].  y is written, not accumulated: every row t < M gets
+ * its base projection, and the rows of segments with an adapter (id >= 0) get the LoRA term
+ * on top (by oracle_lora_apply, the same per-row loop). */
+int oracle_base_lora(double *y, const double *x, const double *W0, const double *const *A,
+                     const double *const *B, const int32_t *seg_starts,
+                     const int32_t *seg_adapter, int32_t num_segments, int32_t M,
+                     int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, double scale)
+{
+    for (int32_t t = 0; t < M; ++t) {
+        const double *xt = x + (size_t)t * (size_t)h_in;
+        double *yt = y + (size_t)t * (size_t)h_out;
+        for (int32_t n = 0; n < h_out; ++n) {
+            const double *wn = W0 + (size_t)n * (size_t)h_in;
+            double s = 0.0;
+            for (int32_t j = 0; j < h_in; ++j)
+                s += xt[j] * wn[j];
+            yt[n] = s;
+        }
+    }
+    return oracle_lora_apply(y, x, A, B, seg_starts, seg_adapter, num_segments, layer_idx, h_in,
+                             h_out, r, scale);
+}

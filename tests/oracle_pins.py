@@ -326,8 +326,42 @@ def check_ranked(o):
         assert np.allclose(one, pad, rtol=1e-12, atol=1e-12)
 
 
+def check_base_lora(o):
+    """The base projection plus the LoRA term, written into y, pinned four ways: the
+    hand-worked case in tests/golden/base_lora_hand.json; merged weights through numpy (each
+    row times W0^T + s A_k B_k of its own adapter, base only for rows without one); W0 = 0
+    reduces it to the already pinned lora_apply on a zero y; and zero adapters reduce it to a
+    numpy matmul x W0^T."""
+    g = json.load(open(os.path.join(GOLDEN, "base_lora_hand.json")))
+    A = [np.asarray(a, np.float64)[None] for a in g["A"]]
+    B = [np.asarray(b, np.float64)[None] for b in g["B"]]
+    y = o.base_lora(g["x"], g["W0"], A, B, g["seg_starts"], g["seg_adapter"], 0, g["scale"])
+    assert np.array_equal(y, np.asarray(g["y_expected"], np.float64)), y
+    rng = np.random.default_rng(23)
+    p = random_problem(29, S=6, h_in=20, h_out=28, r=3, n_adapters=3)
+    M = p["M"] + 3  # three rows after the last segment
+    x = rng.standard_normal((M, p["h_in"]))
+    W0 = rng.standard_normal((p["h_out"], p["h_in"]))
+    sa = p["sa"].copy()
+    sa[1] = -1
+    s, layer = 0.6, 1
+    got = o.base_lora(x, W0, p["A"], p["B"], p["ss"], sa, layer, s)
+    want = x @ W0.T
+    for i, k in enumerate(sa):
+        lo, hi = p["ss"][i], p["ss"][i + 1]
+        if k >= 0:
+            want[lo:hi] = x[lo:hi] @ (W0.T + s * (p["A"][k][layer] @ p["B"][k][layer]))
+    _close(got, want, what="base + LoRA, merged weights")
+    zero_w = o.base_lora(x, np.zeros_like(W0), p["A"], p["B"], p["ss"], sa, layer, s)
+    _close(zero_w, o.lora_apply(np.zeros((M, p["h_out"])), x, p["A"], p["B"], p["ss"], sa,
+                                layer, s), what="W0 = 0")
+    zero_a = o.base_lora(x, W0, [np.zeros_like(a) for a in p["A"]], p["B"], p["ss"], sa, layer,
+                         s)
+    _close(zero_a, x @ W0.T, what="zero adapters")
+
+
 ALL_CHECKS = [check_hand_example, check_merged_weights, check_per_request_gemv,
               check_single_adapter_dense, check_zero_adapter, check_permutation,
               check_brute_force, check_layer_selection, check_shrink_expand,
               check_untouched_rows, check_validate, check_validate_pointers, check_plan,
-              check_ranked]
+              check_ranked, check_base_lora]

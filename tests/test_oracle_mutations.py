@@ -43,6 +43,15 @@ MUTATIONS = [
      None),
     ("ranked_transposed_B", "(size_t)layer_idx * (size_t)h_in * (size_t)r;\n        const double *Bk = B[k] + (size_t)layer_idx * (size_t)r * (size_t)h_out;\n        for (int32_t t = seg_starts[i]; t < seg_starts[i + 1]; ++t) {\n            const double *xt = x + (size_t)t * (size_t)h_in;\n            double *yt = y + (size_t)t * (size_t)h_out;\n            for (int32_t c = 0; c < r; ++c) {\n                double s = 0.0;\n                for (int32_t j = 0; j < h_in; ++j)\n                    s += xt[j] * Ak[(size_t)j * (size_t)r + (size_t)c];\n                v[c] = s;\n            }\n            for (int32_t n = 0; n < h_out; ++n) {\n                double s = 0.0;\n                for (int32_t c = 0; c < r; ++c)\n                    s += v[c] * Bk[(size_t)c * (size_t)h_out + (size_t)n];\n                yt[n] += scale[k] * s;",
      "(size_t)layer_idx * (size_t)h_in * (size_t)r;\n        const double *Bk = B[k] + (size_t)layer_idx * (size_t)r * (size_t)h_out;\n        for (int32_t t = seg_starts[i]; t < seg_starts[i + 1]; ++t) {\n            const double *xt = x + (size_t)t * (size_t)h_in;\n            double *yt = y + (size_t)t * (size_t)h_out;\n            for (int32_t c = 0; c < r; ++c) {\n                double s = 0.0;\n                for (int32_t j = 0; j < h_in; ++j)\n                    s += xt[j] * Ak[(size_t)j * (size_t)r + (size_t)c];\n                v[c] = s;\n            }\n            for (int32_t n = 0; n < h_out; ++n) {\n                double s = 0.0;\n                for (int32_t c = 0; c < r; ++c)\n                    s += v[c] * Bk[(size_t)n * (size_t)r + (size_t)c];\n                yt[n] += scale[k] * s;", None),
+    ("base_W0_transposed", "s += xt[j] * wn[j];",
+     "s += xt[j] * W0[(size_t)j * (size_t)h_out + (size_t)n];", None),
+    ("base_accumulated", "            yt[n] = s;\n", "            yt[n] += s;\n", None),
+    ("base_last_row_dropped", "for (int32_t t = 0; t < M; ++t) {",
+     "for (int32_t t = 0; t < M - 1; ++t) {", None),
+    ("base_lora_term_dropped",
+     "return oracle_lora_apply(y, x, A, B, seg_starts, seg_adapter, num_segments, layer_idx, h_in,",
+     "return 0 * oracle_lora_apply(y, x, A, B, seg_starts, seg_adapter, 0, layer_idx, h_in,",
+     None),
     ("plan_rows_reversed", "rows[n++] = t;",
      "rows[n++] = seg_starts[j + 1] - 1 - (t - seg_starts[j]);", None),
 ]
