@@ -351,6 +351,40 @@ int lora_apply_multi(const sgmv_projection_t *proj, int32_t num_proj, const void
                      uint32_t flags, sgmv_stream_t stream);
 
 /*
+ * lora_apply_base -- the base projection and the LoRA term in one output pass:
+ *     y[t] = x[t] . W0^T + scale * (x[t] . A_k) . B_k   rows t of segments with adapter k >= 0
+ *     y[t] = x[t] . W0^T                                 every other row t < M
+ * Source: "Punica Guide: Multi-Tenant LoRA Serving with SGMV", section "The Heterogeneous
+ * Batching Bottleneck": the y_i equation's two terms, and that section's figure in which the
+ * base GEMM feeds the fused SGMV kernel; here the LoRA term is added in the base GEMM's
+ * epilogue, so y is written once (no read-modify-write of a base output).
+ *   y        [M][ldy] output, written (not accumulated) for every row < M, columns < h_out
+ *   x        [M][ldx] input rows
+ *   M        rows of x and y (segment rows must lie in [0, M))
+ *   W0       [h_out][ldw] base weight, one row per output feature (a linear layer's weight:
+ *            the equation's x_i W0 is sum_j x[t][j] * W0[n][j])
+ *   A_ptrs, B_ptrs, seg_starts, seg_adapter, num_segments, layer_idx, h_in, h_out, r, scale
+ *            as for lora_apply (num_segments = 0: y = x . W0^T only)
+ *   v_work   caller-owned fp32 workspace of M * r floats, 16-byte aligned (the shrink writes
+ *            v = x . A_k there for the rows of segments with an adapter); may be NULL when
+ *            num_segments == 0
+ *   flags    passed to the shrink (SGMV_OVERLAP_PRIOR also makes the GEMM wait for the
+ *            previous kernel of the stream before reading x)
+ * Enqueues two kernels: sgmv_shrink_strided into v_work, then the GEMM (tcgen05, 128 x 256
+ * output tiles, one CTA per SM), which starts its main loop while the shrink runs and waits
+ * for it only before reading v.  Types: SGMV_F16 and SGMV_BF16 (SGMV_F32 -> SGMV_EUNSUPPORTED).
+ * Layout rules as for lora_apply_strided (h_in, h_out, ldx, ldy, ldw multiples of 8; y, x, W0,
+ * v_work 16-byte aligned).  Errors as for lora_apply; nothing is enqueued on a host-checked
+ * error.  The device error word reports SGMV_ETIMEOUT if a bounded wait of either kernel
+ * runs out.
+ */
+int lora_apply_base(void *y, int32_t ldy, const void *x, int32_t ldx, int32_t M, const void *W0,
+                    int32_t ldw, const void *const *A_ptrs, const void *const *B_ptrs,
+                    const int32_t *seg_starts, const int32_t *seg_adapter, int32_t num_segments,
+                    int32_t layer_idx, int32_t h_in, int32_t h_out, int32_t r, float scale,
+                    float *v_work, sgmv_dtype_t dtype, uint32_t flags, sgmv_stream_t stream);
+
+/*
  * lora_apply_static_plan -- lora_apply_planned for callers that cannot allocate device memory:
  * the library builds the plan itself (sgmv_plan) into a fixed array inside the library
  * instead of a caller-provided buffer, then applies it; the caller passes only inputs and

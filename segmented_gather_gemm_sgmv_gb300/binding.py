@@ -37,7 +37,7 @@ SYMBOLS = ("lora_apply", "lora_apply_ex", "lora_apply_strided", "sgmv_shrink", "
            "lora_apply_planned", "sgmv_shrink_planned", "sgmv_expand_planned", "lora_apply_multi",
            "lora_apply_ranked", "sgmv_pool_slot_bytes", "sgmv_pool_create", "sgmv_pool_destroy",
            "sgmv_pool_register", "sgmv_pool_acquire", "sgmv_pool_release", "sgmv_pool_stats",
-           "lora_apply_static_plan")
+           "lora_apply_static_plan", "lora_apply_base")
 
 
 class Projection(ctypes.Structure):
@@ -109,6 +109,8 @@ def lib(build_if_stale: bool = True) -> ctypes.CDLL:
         L.sgmv_pool_release.argtypes = [vp, vp, i32, vp]
         L.sgmv_pool_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64),
                                       ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(i32)]
+        L.lora_apply_base.argtypes = [vp, i32, vp, i32, i32, vp, i32, vp, vp, vp, vp, i32, i32,
+                                      i32, i32, i32, f32, vp, ci, u32, vp]
         L.lora_apply_static_plan.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, i32, i32, i32,
                                              i32, i32, i32, f32, ci, u32, vp]
         L.sgmv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
@@ -460,6 +462,40 @@ def lora_apply_static_plan(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, max_ro
             x.shape[1], y.shape[1], int(r), float(scale), _dtype_code(x), flags,
             _stream(stream, x.device))
     _check(rc, "lora_apply_static_plan")
+    return y
+
+
+def lora_apply_base(y, x, W0, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale,
+                    v_work=None, stream=None, overlap_prior=False, tensor_cores="auto",
+                    long_batch=False):
+    """y = x W0^T + scale * (x A_k) B_k per segment row (x W0^T alone on other rows), written
+    into y (fp16 / bf16).  W0 is [h_out, h_in] (a linear layer's weight).  v_work: fp32
+    [M, r] workspace (made here with torch when not given).  Flags as for lora_apply; they
+    apply to the shrink."""
+    import torch
+    ldy, ldx = _rows(y, "y"), _rows(x, "x")
+    ldw = _rows(W0, "W0")
+    if x.dtype != y.dtype or W0.dtype != x.dtype or x.shape[0] != y.shape[0]:
+        raise ValueError("x [M, h_in], W0 [h_out, h_in] and y [M, h_out] share a dtype and M")
+    if W0.shape[0] != y.shape[1] or W0.shape[1] != x.shape[1]:
+        raise ValueError("W0 must be [h_out, h_in]")
+    S = _table(seg_starts, seg_adapter)
+    M = x.shape[0]
+    if v_work is None and S > 0:
+        v_work = torch.empty((M, int(r)), dtype=torch.float32, device=x.device)
+    if v_work is not None:
+        _cuda(v_work, "v_work")
+        if v_work.dtype != torch.float32 or v_work.numel() < M * int(r):
+            raise ValueError("v_work must hold M * r fp32 values")
+    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    with _on(x, y, W0, seg_starts, seg_adapter):
+        rc = lib().lora_apply_base(
+            y.data_ptr(), ldy, x.data_ptr(), ldx, M, W0.data_ptr(), ldw,
+            _ptrs(A_ptrs, "A_ptrs") if S else None, _ptrs(B_ptrs, "B_ptrs") if S else None,
+            seg_starts.data_ptr(), seg_adapter.data_ptr(), S, int(layer_idx), x.shape[1],
+            y.shape[1], int(r), float(scale), v_work.data_ptr() if v_work is not None else None,
+            _dtype_code(x), flags, _stream(stream, x.device))
+    _check(rc, "lora_apply_base")
     return y
 
 

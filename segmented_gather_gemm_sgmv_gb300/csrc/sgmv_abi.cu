@@ -533,6 +533,19 @@ __global__ void validate_ptrs_kernel(const void* const* A_ptrs, const void* cons
 
 }  // namespace
 
+namespace sgmv {
+int device_context(int** err, int* sms, uint64_t* wait_ns, int* inject_stall) {
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != SGMV_OK) return rc;
+  *err = st->err;
+  *sms = st->sms;
+  *wait_ns = st->wait_ns.load(std::memory_order_relaxed);
+  *inject_stall = st->inject.load(std::memory_order_relaxed);
+  return SGMV_OK;
+}
+}  // namespace sgmv
+
 extern "C" {
 
 int lora_apply(void* y, const void* x, const void* const* A_ptrs, const void* const* B_ptrs,

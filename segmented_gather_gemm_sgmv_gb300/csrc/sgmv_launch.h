@@ -17,4 +17,8 @@ const void* kernel_multi_f32(int r, bool wide);
 const void* kernel_multi_f16(int r, bool wide);
 const void* kernel_multi_bf16(int r, bool wide);
 
+// The current device's library context for kernels launched outside sgmv_abi.cu: the device
+// error word, the SM count and the bounded-wait settings (sgmv_set_wait_limit).
+int device_context(int** err, int* sms, uint64_t* wait_ns, int* inject_stall);
+
 }  // namespace sgmv

@@ -253,3 +253,28 @@ def test_pool_host_checks(L):
     assert L.sgmv_pool_acquire(None, None, 0, P, P, None, None, None) == -1
     assert L.sgmv_pool_release(None, None, 0, None) == -1
     assert L.sgmv_pool_stats(None, None, None, None) == -1
+
+
+def test_base_host_checks(L):
+    """lora_apply_base: argument checks that need no device (M = 0 returns OK, no launch)."""
+    a = OK_ARGS
+    W0, v = P + 0x70000, P + 0x80000
+
+    def base(M=0, S=4, dt=1, r=16, h_in=4096, h_out=4096, ldx=4096, ldy=4096, ldw=4096,
+             x=a["x"], w=W0, vw=v, flags=0):
+        return L.lora_apply_base(a["y"], ldy, x, ldx, M, w, ldw, a["A"], a["B"], a["ss"],
+                                 a["sa"], S, 0, h_in, h_out, r, 1.0, vw, dt, flags, None)
+    assert base() == 0
+    assert base(S=0, vw=None) == 0
+    assert base(dt=0) == -3          # fp32: the tensor cores take 16-bit operands
+    assert base(r=24) == -3
+    assert base(M=-1) == -1
+    assert base(w=None) == -1
+    assert base(vw=None) == -1       # segments need the workspace
+    assert base(ldw=4090) == -1
+    assert base(ldw=4100) == -2
+    assert base(h_out=4092, ldy=4092) == -2
+    assert base(x=P + 0x10008) == -2
+    assert base(vw=v + 8) == -2
+    assert base(flags=16) == -1
+    assert base(S=5000) == -3
