@@ -526,6 +526,84 @@ def measure_ranked(torch, device, stream, seconds):
     return out
 
 
+def measure_base(torch, device, stream, seconds):
+    """The base projection with the LoRA term in its epilogue (lora_apply_base) at the
+    prefill_mixed shape (4096 -> 11008, r = 64, bf16, 8 segments of 128-1024 rows), against
+    the same output made unfused: a cuBLAS GEMM (torch.matmul) writing x W0^T, then lora_apply
+    reading and rewriting y; and against the cuBLAS GEMM alone (no LoRA term: the floor).  Two
+    sets of (x, W0, y) alternate, so a call's footprint (~195 MB) is not in L2 from the call
+    before."""
+    from segmented_gather_gemm_sgmv_gb300 import lora_apply, lora_apply_base
+    w = workloads.WORKLOADS["prefill_mixed"]
+    ss, sa = workloads.make_segments(w.name, 0)
+    M = int(ss[-1])
+    A, B = workloads.make_pool(w, device, seed=41)
+    A_ptrs, B_ptrs = workloads.pointer_table(A, device), workloads.pointer_table(B, device)
+    d_ss, d_sa = torch.as_tensor(ss, device=device), torch.as_tensor(sa, device=device)
+    g = torch.Generator(device=device).manual_seed(43)
+    bound = 1.0 / np.sqrt(w.h_in)
+    sets = []
+    for i in range(2):
+        x, y = workloads.make_activations(w, M, device, seed=600 + i)
+        W0 = ((torch.rand((w.h_out, w.h_in), generator=g, device=device) * 2 - 1) *
+              bound).to(torch.bfloat16)
+        sets.append((x, W0, y))
+    v_work = torch.empty((M, w.r), dtype=torch.float32, device=device)
+
+    def fused(i, stream=None):
+        x, W0, y = sets[i % 2]
+        lora_apply_base(y, x, W0, A_ptrs, B_ptrs, d_ss, d_sa, 0, w.r, w.scale, v_work=v_work,
+                        stream=stream, long_batch=True)
+
+    def unfused(i, stream=None):
+        x, W0, y = sets[i % 2]
+        torch.matmul(x, W0.t(), out=y)
+        lora_apply(y, x, A_ptrs, B_ptrs, d_ss, d_sa, 0, w.r, w.scale, stream=stream,
+                   long_batch=True)
+
+    def cublas(i, stream=None):
+        x, W0, y = sets[i % 2]
+        torch.matmul(x, W0.t(), out=y)
+
+    _, tc_peak, kind = measured_peaks()
+    hbm = measured_peaks()[0]
+    f_base = 2.0 * M * w.h_in * w.h_out
+    f_lora = 2.0 * M * w.r * (w.h_in + w.h_out)
+    eb = 2
+    nbytes = (M * w.h_in + w.h_out * w.h_in + M * w.h_out) * eb + \
+        len(set(sa.tolist())) * w.r * (w.h_in + w.h_out) * eb
+    out = {"workload": "prefill_mixed shape: x [%d, 4096] . W0^T [4096, 11008] + LoRA r=64, bf16"
+                       % M, "flops_base": f_base, "flops_lora": f_lora, "bytes_min": nbytes}
+    n = 8
+    for label, fn in (("fused", fused), ("unfused", unfused), ("cublas_gemm_only", cublas)):
+        gr = capture_step(torch, fn, n, stream)
+        K = steps_for(torch, gr, stream, seconds)
+        clocks = ClockSampler(torch.cuda.current_device()).start() if label == "fused" else None
+        ms = time_steps(torch, gr, K, 3, stream)
+        if clocks is not None:
+            out["clocks"] = clocks.stop()
+        us = ms * 1e3 / (K * n)
+        out[f"us_per_call_{label}"] = round(us, 2)
+        out[f"TFLOP_per_s_{label}"] = round((f_base + (f_lora if label != "cublas_gemm_only"
+                                                       else 0.0)) / us / 1e6, 1)
+        del gr
+    us = out["us_per_call_fused"]
+    t_flop = (f_base + f_lora) / (tc_peak * 1e12)
+    t_mem = nbytes / (hbm * 1e9)
+    out["roofline"] = {"bound": "tensor" if t_flop >= t_mem else "hbm",
+                       "achieved": out["TFLOP_per_s_fused"], "peak": tc_peak, "unit": "TFLOP/s",
+                       "frac": round(max(t_flop, t_mem) / (us * 1e-6), 4),
+                       "peak_source": kind + " (bf16 sustained)",
+                       "t_flop_us": round(t_flop * 1e6, 2), "t_mem_us": round(t_mem * 1e6, 2)}
+    out["launch"] = ("lora_apply_base (sgmv_shrink_strided + the tcgen05 GEMM whose epilogue adds "
+                     "the LoRA term; y written once) vs torch.matmul + lora_apply (y written, "
+                     "then read and rewritten) vs torch.matmul alone")
+    del sets, A, B, v_work
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_paging(torch, device, stream, seconds):
     """Adapter paging (sgmv_pool_*): the decode_distinct shape (64 one-token segments, h = 4096,
     r = 16, fp16, 32 layers) with 128 adapters in pinned host memory and a 64-slot device pool;
@@ -788,6 +866,10 @@ def run_ours(args):
     us_call = per_step / n * 1e6
     e2e_s, h2d, d2h = time_e2e(torch, setup, max(3, min(K, 200)), stream)
     e2e_s = reduce_max(e2e_s, world, device)
+    if world == 1 and not args.no_per_config:
+        # the GEMM leg runs the GPU at its power cap: after the headline's timed region, so
+        # that the lower clocks it leaves behind do not carry into it
+        per_config["base_fused"] = measure_base(torch, device, stream, args.config_seconds)
     if rank != 0:
         dist_finish(world)
         return

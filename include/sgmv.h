@@ -368,8 +368,9 @@ int lora_apply_multi(const sgmv_projection_t *proj, int32_t num_proj, const void
  *   v_work   caller-owned fp32 workspace of M * r floats, 16-byte aligned (the shrink writes
  *            v = x . A_k there for the rows of segments with an adapter); may be NULL when
  *            num_segments == 0
- *   flags    passed to the shrink (SGMV_OVERLAP_PRIOR also makes the GEMM wait for the
- *            previous kernel of the stream before reading x)
+ *   flags    passed to the shrink, which sends adapter groups of 64 rows or more to its
+ *            tensor role unless SGMV_NO_TENSOR_CORES is set (SGMV_OVERLAP_PRIOR also makes the
+ *            GEMM wait for the previous kernel of the stream before reading x)
  * Enqueues two kernels: sgmv_shrink_strided into v_work, then the GEMM (tcgen05, 128 x 256
  * output tiles, one CTA per SM), which starts its main loop while the shrink runs and waits
  * for it only before reading v.  Types: SGMV_F16 and SGMV_BF16 (SGMV_F32 -> SGMV_EUNSUPPORTED).

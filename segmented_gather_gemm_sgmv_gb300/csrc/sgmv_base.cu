@@ -591,9 +591,15 @@ int lora_apply_base(void* y, int32_t ldy, const void* x, int32_t ldx, int32_t M,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // v = x . A_k into the workspace (rows of segments with an adapter); the GEMM below waits
   // for it (programmatic dependent launch) only before its epilogue reads v.
+  // The shrink alone streams only x and A: groups of 64 rows and more go to its tensor role
+  // (measured at the prefill shape, 4096 -> r = 64, 3450 rows in 8 groups of 142-891 rows:
+  // 25 us there against 65 us under the fused call's cost rule, which keeps groups under
+  // 256 rows on the CUDA cores), unless the caller turned the tensor cores off.
+  const uint32_t shrink_flags =
+      (flags & SGMV_NO_TENSOR_CORES) ? flags : (flags | SGMV_TENSOR_CORES_ALWAYS);
   if (num_segments > 0) {
     rc = sgmv_shrink_strided(v_work, x, ldx, A_ptrs, seg_starts, seg_adapter, num_segments,
-                             layer_idx, h_in, r, dtype, flags, stream);
+                             layer_idx, h_in, r, dtype, shrink_flags, stream);
     if (rc != SGMV_OK) return rc;
   }
   // The loads of x may start before the previous kernel has finished only when it is our own
