@@ -32,6 +32,7 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import dataclasses
 import glob
 import hashlib
 import json
@@ -831,6 +832,8 @@ def run_ours(args):
             per_config["paging"] = measure_paging(torch, device, stream, args.config_seconds)
 
     w = workloads.WORKLOADS[args.workload]
+    if args.pool_layers > 0:
+        w = dataclasses.replace(w, layers=args.pool_layers)
     long_batch = {"auto": w.prefill, "on": True, "off": False}[args.long_batch]
     setup = Setup(w, device, tensor_cores=args.tensor_cores, long_batch=long_batch,
                   strided=args.strided)
@@ -1016,6 +1019,13 @@ def main(argv=None):
                          "(lora_apply_strided; the e2e figure stays on dense copies)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain lora_apply launches (no programmatic dependent launch)")
+    ap.add_argument("--pool-layers", type=int, default=0,
+                    help="pool layers of the workload (default: its own); a smaller pool for "
+                         "profiling captures of the same kernel, whose work per call does not "
+                         "depend on the layer count")
+    ap.add_argument("--only-base", action="store_true",
+                    help="run only the base_fused measurement (lora_apply_base at the "
+                         "prefill_mixed shape) and print it; for profiling that kernel")
     argv = sys.argv[1:] if argv is None else argv
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -1029,6 +1039,12 @@ def main(argv=None):
         sys.exit(subprocess.call(relaunch_cmd(argv, args.gpus)))
     if args.impl == "reference":
         run_reference(args)
+    elif args.only_base:
+        import torch
+        device = torch.device("cuda", 0)
+        torch.cuda.set_device(device)
+        print(json.dumps({"base_fused": measure_base(torch, device, torch.cuda.Stream(device),
+                                                     args.config_seconds)}), flush=True)
     else:
         run_ours(args)
 
