@@ -13,8 +13,9 @@ Prints one JSON line (rank 0):
   value         algorithmic HBM GB/s, whole job (bytes per call: each distinct adapter's A
                 and B once, x once, y read + written once), inputs resident in HBM, CUDA events
                 on the launching stream around exactly K steps;
-  e2e           the same metric through the public API with pinned HOST buffers: every call of
-                a step copies its x, y_in and segment table host->device and reads y back;
+  e2e           the same metric through the public API with pinned HOST buffers: every step
+                copies all its calls' x and y_in and the segment table host->device (one copy)
+                and reads every call's y back (one copy);
   roofline      achieved / measured HBM copy bandwidth (and the FLOP term beside it);
   per_config    every named workload (decode_distinct, decode_zipf, decode_uniform,
                 decode_same, prefill_mixed, mixed_70b): us per call chained and isolated, the
@@ -702,65 +703,80 @@ def measure_paging(torch, device, stream, seconds):
 
 
 def time_e2e(torch, setup, K, stream):
-    """Public-API path with pinned host buffers.  Per call: ONE host->device copy of the call's
-    inputs (x, y_in and the segment table packed in one pinned staging buffer), the lora_apply
-    call on views of the device copy, ONE device->host copy of y.  Calls alternate between two
-    streams and two device / host buffer sets, so that one call's copies overlap the other
-    stream's kernel; each stream runs its calls in order.  Returns seconds per step (one step =
-    the same number of calls as a device-timed step)."""
+    """Public-API path with pinned host buffers, one host->device copy and one device->host copy
+    per step: the step's inputs (every call's x and y_in, then the segment table, packed in one
+    pinned staging buffer) go in with ONE copy, the step's calls run on views of the device
+    copy (the same lora_apply calls and flags as the device-timed step), and every call's y
+    comes back with ONE copy (measured: one copy per direction per step doubled the figure
+    against one per call; cutting each copy into four chunks on streams of their own lowered
+    it again).  Steps alternate between two streams and two device / host buffer
+    sets, so that one step's copies overlap the other step's kernels; a CUDA graph holds four
+    steps.  Returns seconds per step and the bytes copied in and out per step."""
     w = setup.w
     dt = workloads.torch_dtype(w.dtype)
     x0, y0 = setup.x[0], setup.y[0]
     eb = x0.element_size()
+    n = setup.calls
 
     def up16(v):
         return (v + 15) // 16 * 16
 
-    nx, ny = x0.numel() * eb, y0.numel() * eb
+    nx, ny = up16(x0.numel() * eb), up16(y0.numel() * eb)
     nss, nsa = 4 * len(setup.ss), 4 * len(setup.sa)
-    off_y = up16(nx)
-    off_ss = off_y + up16(ny)
+    off_y = n * nx
+    off_ss = off_y + n * ny
     off_sa = off_ss + up16(nss)
     total = off_sa + up16(nsa)
     host = torch.empty(total, dtype=torch.uint8).pin_memory()
-    host[0:nx].copy_(x0.cpu().contiguous().view(torch.uint8).view(-1))
-    host[off_y:off_y + ny].copy_(y0.cpu().contiguous().view(torch.uint8).view(-1))
+    for i in range(n):
+        host[i * nx:i * nx + x0.numel() * eb].copy_(
+            setup.x[i].cpu().contiguous().view(torch.uint8).view(-1))
+        host[off_y + i * ny:off_y + i * ny + y0.numel() * eb].copy_(
+            setup.y[i].cpu().contiguous().view(torch.uint8).view(-1))
     host[off_ss:off_ss + nss].copy_(torch.as_tensor(setup.ss).view(torch.uint8))
     host[off_sa:off_sa + nsa].copy_(torch.as_tensor(setup.sa).view(torch.uint8))
     streams = [stream, torch.cuda.Stream(x0.device)]
     sets = []
     for _ in range(2):
         dev = torch.empty(total, dtype=torch.uint8, device=x0.device)
-        sets.append(dict(dev=dev, x=dev[0:nx].view(dt).view(x0.shape),
-                         y=dev[off_y:off_y + ny].view(dt).view(y0.shape),
-                         ss=dev[off_ss:off_ss + nss].view(torch.int32),
-                         sa=dev[off_sa:off_sa + nsa].view(torch.int32),
-                         out=torch.empty(y0.shape, dtype=dt).pin_memory()))
+        sets.append(dict(
+            dev=dev,
+            x=[dev[i * nx:i * nx + x0.numel() * eb].view(dt).view(x0.shape) for i in range(n)],
+            y=[dev[off_y + i * ny:off_y + i * ny + y0.numel() * eb].view(dt).view(y0.shape)
+               for i in range(n)],
+            ys=dev[off_y:off_ss],
+            ss=dev[off_ss:off_ss + nss].view(torch.int32),
+            sa=dev[off_sa:off_sa + nsa].view(torch.int32),
+            out=torch.empty(off_ss - off_y, dtype=torch.uint8).pin_memory()))
     from segmented_gather_gemm_sgmv_gb300 import lora_apply
 
-    def one(s):
-        st, b = streams[s % 2], sets[s % 2]
+    def one_step(j):
+        st, b = streams[j % 2], sets[j % 2]
         with torch.cuda.stream(st):
             b["dev"].copy_(host, non_blocking=True)
-            lora_apply(b["y"], b["x"], setup.A_ptrs, setup.B_ptrs, b["ss"], b["sa"],
-                       s % w.layers, w.r, w.scale, stream=st, overlap_prior=setup.overlap,
-                       tensor_cores=setup.tensor_cores, long_batch=setup.long_batch)
-            b["out"].copy_(b["y"], non_blocking=True)
+            for i in range(n):
+                lora_apply(b["y"][i], b["x"][i], setup.A_ptrs, setup.B_ptrs, b["ss"], b["sa"],
+                           i % w.layers, w.r, w.scale, stream=st, overlap_prior=setup.overlap,
+                           tensor_cores=setup.tensor_cores, long_batch=setup.long_batch)
+            b["out"].copy_(b["ys"], non_blocking=True)
 
-    def step():
+    per_graph = 4
+
+    def steps():
         streams[1].wait_stream(streams[0])  # fork
-        for s in range(setup.calls):
-            one(s)
+        for j in range(per_graph):
+            one_step(j)
         streams[0].wait_stream(streams[1])  # join
 
     with torch.cuda.stream(stream):
-        step()
+        steps()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        step()
-    ms = time_steps(torch, g, K, 3, stream)
-    return ms / 1e3 / K, total * setup.calls, ny * setup.calls
+        steps()
+    reps = max(2, (K + per_graph - 1) // per_graph)
+    ms = time_steps(torch, g, reps, 3, stream)
+    return ms / 1e3 / (reps * per_graph), total, off_ss - off_y
 
 
 def cpu_baseline(w, setup, seconds=10.0):
