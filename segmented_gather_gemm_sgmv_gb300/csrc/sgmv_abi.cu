@@ -297,6 +297,7 @@ int setup_problem(const DeviceState* st, const Problem& pb, sgmv::Params& p, uin
   p.scale = pb.scale;
   p.wait_limit_ns = st->wait_ns.load(std::memory_order_relaxed);
   p.inject_stall = st->inject.load(std::memory_order_relaxed);
+  p.dependent = (flags & SGMV_OVERLAP_PRIOR) ? 1 : 0;
   // Tensor role (16-bit types, r >= 16; every mode): it uses none of the CUDA-core scratch
   // areas, so its row table sits at off_vpart and its ring of 24 KB slots right after it, up to
   // the end of the budget (the launch then always takes the whole budget).

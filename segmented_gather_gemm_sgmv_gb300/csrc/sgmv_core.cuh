@@ -108,6 +108,10 @@ struct Params {
   int32_t desc_ints;
   uint64_t wait_limit_ns;
   int32_t inject_stall;
+  // Launched as a programmatic dependent of the previous kernel (SGMV_OVERLAP_PRIOR): the
+  // activations may only be read after griddepcontrol.wait.  Otherwise the previous kernel has
+  // completed before this one started and they are copied with the weights from the start.
+  int32_t dependent;
   int32_t tc_min_rows;  // groups with at least this many rows go to the tensor role (INT32_MAX: none)
   int32_t tc_slots;     // tensor-role ring slots (24 KB each)
   uint32_t tc_base;     // tensor-role ring offset (1024-aligned; after its row table at off_vpart)
@@ -781,7 +785,7 @@ struct Kernel {
     const int total = mp.total;
     RingPos rp;
     rp.init();
-    bool prior_done = false;
+    bool prior_done = !p.dependent;  // nothing to wait for: activations go with their stages
     for (int li = 0; li < n_my; ++li) {
       const int b = li & 1;
       if (li >= 2 && lane == 0) w.wait<false>(sm.fixed(kDescFree0 + b), ((li >> 1) - 1) & 1);
