@@ -122,3 +122,61 @@ def test_random_unfused_case_matches_oracle(i):
     y_ref = oracle.sgmv_expand(c.y0.double().cpu().numpy(), v.double().cpu().numpy(), B, ss, sa,
                                0, w.scale)
     harness.assert_close(y.float().cpu().numpy(), y_ref, what + " expand")
+
+
+@pytest.mark.parametrize("i", range(N_CASES // 3))
+def test_random_planned_case_matches_oracle(i):
+    """The same draws through a plan (sgmv_plan, then lora_apply_planned with the draw's
+    options): the row capacity is the row count exactly, and every row is checked."""
+    from segmented_gather_gemm_sgmv_gb300 import lora_apply_planned, sgmv_plan
+    dtype, r, h_in, h_out, n_adapters, lens, ids, opts, strided = _draw(9000 + i)
+    ss = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    sa = np.asarray(ids, np.int32)
+    w = workloads.Workload("fuzz_planned", h_in, h_out, r, dtype, n_adapters, 2)
+    c = harness.make_case(w, ss, sa, M=int(ss[-1]) + 2, seed=i)
+    layer = i % 2
+    what = f"planned case {i}: {dtype} r{r} {h_in}->{h_out} lens={lens} ids={ids} {opts}"
+    plan = sgmv_plan(c.d_ss, c.d_sa, max(1, int(ss[-1])))
+    y = c.y0.clone()
+    lora_apply_planned(y, c.x, c.A_ptrs, c.B_ptrs, plan, layer, r, w.scale, **opts)
+    torch.cuda.synchronize()
+    harness.assert_close(y.float().cpu().numpy(), harness.oracle_apply(c, layer), what)
+    keep = harness.row_adapters(c.ss, c.sa, c.M) < 0
+    idx = torch.as_tensor(np.nonzero(keep)[0], device="cuda")
+    assert torch.equal(y[idx], c.y0[idx]), f"{what}: rows without an adapter were modified"
+
+
+@pytest.mark.parametrize("i", range(N_CASES // 4))
+def test_random_base_case_matches_oracle(i):
+    """lora_apply_base (base projection + LoRA term, written) on the draws' tables, 16-bit
+    types and hidden sizes up to 640, against oracle.base_lora on every row."""
+    import oracle
+    from segmented_gather_gemm_sgmv_gb300 import lora_apply_base
+    dtype, r, h_in, h_out, n_adapters, lens, ids, opts, strided = _draw(12000 + i)
+    rng = np.random.default_rng(77 + i)
+    dtype = "bf16" if dtype == "f32" else dtype
+    h_in, h_out = int(8 * rng.integers(4, 81)), int(8 * rng.integers(4, 81))
+    ss = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    sa = np.asarray(ids, np.int32)
+    w = workloads.Workload("fuzz_base", h_in, h_out, r, dtype, n_adapters, 2)
+    M = int(ss[-1]) + int(rng.integers(0, 40))  # rows after the last segment: base only
+    c = harness.make_case(w, ss, sa, M=max(M, 1), seed=i)
+    layer = i % 2
+    g = torch.Generator(device="cuda")
+    g.manual_seed(300 + i)
+    W0 = ((torch.rand((h_out, h_in), generator=g, device="cuda") * 2 - 1) /
+          np.sqrt(h_in)).to(c.x.dtype)
+    y = torch.full((c.M, h_out), float("nan"), dtype=c.x.dtype, device="cuda")
+    tc = "never" if opts["tensor_cores"] == "never" else "auto"
+    lora_apply_base(y, c.x, W0, c.A_ptrs, c.B_ptrs, c.d_ss, c.d_sa, layer, r, w.scale,
+                    tensor_cores=tc, overlap_prior=opts["overlap_prior"],
+                    long_batch=opts["long_batch"])
+    torch.cuda.synchronize()
+    keys = harness.touched(sa, ss)
+    A = harness.oracle_blocks(c.A, keys, layer)
+    B = harness.oracle_blocks(c.B, keys, layer)
+    ref = oracle.base_lora(c.x.double().cpu().numpy(), W0.double().cpu().numpy(), A, B, ss, sa,
+                           0, w.scale)
+    harness.assert_close(y.float().cpu().numpy(), ref,
+                         f"base case {i}: {dtype} r{r} {h_in}->{h_out} M={c.M} lens={lens} "
+                         f"ids={ids} {opts}")
