@@ -253,6 +253,17 @@ def relaunch_cmd(argv, n):
 
 
 # ----------------------------------------------------------------- our arm ----
+def dense_grid_rule(w, ss, sa):
+    """The caller-side rule for SGMV_DENSE_GRID, as a serving layer that built the table would
+    apply it: a decode batch (no prefill segments) of at least 128 rows spread over at least 32
+    adapter groups, i.e. many work items for each SM (measured: decode_zipf and decode_uniform
+    gain; a batch of one row per adapter, or one adapter for every row, loses)."""
+    if w.prefill:
+        return False
+    groups = group_rows(ss, sa)
+    return sum(groups.values()) >= 128 and len(groups) >= 32
+
+
 def sweep_len(w):
     """Calls per step: every layer of the pool once (a single-layer pool: 20 repeats)."""
     return w.layers if w.layers > 1 else 20
@@ -262,12 +273,13 @@ class Setup:
     """Device-resident inputs of the workload: pool, one x/y set per call of a step, table."""
 
     def __init__(self, w, device, seed=0, overlap=True, tensor_cores="auto", long_batch=False,
-                 strided=False):
+                 strided=False, dense_grid=False):
         import torch
         self.w = w
         self.overlap = overlap
         self.tensor_cores = tensor_cores
         self.long_batch = long_batch
+        self.dense_grid = dense_grid
         self.ss, self.sa = workloads.make_segments(w.name, seed)
         self.M = int(self.ss[-1])
         self.A, self.B = workloads.make_pool(w, device, seed=seed + 1)
@@ -303,14 +315,14 @@ class Setup:
         lora_apply_planned(self.y[i], self.x[i], self.A_ptrs, self.B_ptrs, self.plan,
                            i % self.w.layers, self.w.r, self.w.scale, stream=stream,
                            overlap_prior=self.overlap, tensor_cores=self.tensor_cores,
-                           long_batch=self.long_batch)
+                           long_batch=self.long_batch, dense_grid=self.dense_grid)
 
     def call(self, i, stream=None):
         from segmented_gather_gemm_sgmv_gb300 import lora_apply
         lora_apply(self.y[i], self.x[i], self.A_ptrs, self.B_ptrs, self.d_ss, self.d_sa,
                    i % self.w.layers, self.w.r, self.w.scale, stream=stream,
                    overlap_prior=self.overlap, tensor_cores=self.tensor_cores,
-                   long_batch=self.long_batch)
+                   long_batch=self.long_batch, dense_grid=self.dense_grid)
 
     def call_unfused(self, i, stream=None):
         """The pages' two launches per layer: sgmv_shrink into v, then sgmv_expand."""
@@ -319,7 +331,7 @@ class Setup:
         if self.v is None:
             self.v = torch.zeros((self.M, self.w.r), dtype=torch.float32, device=self.x[0].device)
         kw = dict(stream=stream, tensor_cores=self.tensor_cores, long_batch=self.long_batch,
-                  overlap_prior=self.overlap)
+                  overlap_prior=self.overlap, dense_grid=self.dense_grid)
         sgmv_shrink(self.v, self.x[i], self.A_ptrs, self.d_ss, self.d_sa, i % self.w.layers,
                     self.w.r, **kw)
         sgmv_expand(self.y[i], self.v, self.B_ptrs, self.d_ss, self.d_sa, i % self.w.layers,
@@ -331,6 +343,9 @@ class Setup:
              "lora_apply: each call starts after the previous one completes")
         if self.long_batch:
             t += "; SGMV_LONG_BATCH (a prefill batch: one CTA per SM, whole shared memory)"
+        if self.dense_grid and not self.long_batch:
+            t += ("; SGMV_DENSE_GRID (a decode batch of many work items: two CTAs of the call "
+                  "per SM)")
         return t
 
 
@@ -379,7 +394,11 @@ def measure_config(torch, name, device, stream, seconds, args):
     """One per_config entry: chained, isolated and unfused us per call, with clocks."""
     w = workloads.WORKLOADS[name]
     long_batch = {"auto": w.prefill, "on": True, "off": False}[args.long_batch]
-    setup = Setup(w, device, tensor_cores=args.tensor_cores, long_batch=long_batch)
+    ss0, sa0 = workloads.make_segments(w.name, 0)
+    dense = {"auto": dense_grid_rule(w, ss0, sa0), "on": True,
+             "off": False}[args.dense_grid]
+    setup = Setup(w, device, tensor_cores=args.tensor_cores, long_batch=long_batch,
+                  dense_grid=dense)
     n = setup.calls
     out = {"calls_per_step": n, "layers": w.layers}
     nbytes, M = algorithmic_bytes(w, setup.ss, setup.sa)
@@ -757,7 +776,8 @@ def time_e2e(torch, setup, K, stream):
             for i in range(n):
                 lora_apply(b["y"][i], b["x"][i], setup.A_ptrs, setup.B_ptrs, b["ss"], b["sa"],
                            i % w.layers, w.r, w.scale, stream=st, overlap_prior=setup.overlap,
-                           tensor_cores=setup.tensor_cores, long_batch=setup.long_batch)
+                           tensor_cores=setup.tensor_cores, long_batch=setup.long_batch,
+                           dense_grid=setup.dense_grid)
             b["out"].copy_(b["ys"], non_blocking=True)
 
     per_graph = 4
@@ -851,8 +871,10 @@ def run_ours(args):
     if args.pool_layers > 0:
         w = dataclasses.replace(w, layers=args.pool_layers)
     long_batch = {"auto": w.prefill, "on": True, "off": False}[args.long_batch]
+    ss0, sa0 = workloads.make_segments(w.name, 0)
+    dense = {"auto": dense_grid_rule(w, ss0, sa0), "on": True, "off": False}[args.dense_grid]
     setup = Setup(w, device, tensor_cores=args.tensor_cores, long_batch=long_batch,
-                  strided=args.strided)
+                  strided=args.strided, dense_grid=dense)
     nbytes, M = algorithmic_bytes(w, setup.ss, setup.sa)
     n = setup.calls
 
@@ -1030,6 +1052,10 @@ def main(argv=None):
     ap.add_argument("--long-batch", choices=["auto", "on", "off"], default="auto",
                     help="SGMV_LONG_BATCH launches; auto: for workloads that hold prefill "
                          "segments (prefill_mixed, mixed_70b)")
+    ap.add_argument("--dense-grid", choices=["auto", "on", "off"], default="auto",
+                    help="SGMV_DENSE_GRID launches (two CTAs of a call per SM); auto: decode "
+                         "batches of >= 128 rows over >= 32 adapter groups (decode_zipf, "
+                         "decode_uniform)")
     ap.add_argument("--strided", action="store_true",
                     help="x and y are the middle column third of 3x-wide activations "
                          "(lora_apply_strided; the e2e figure stays on dense copies)")

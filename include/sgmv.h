@@ -132,6 +132,7 @@ int lora_apply(void *y, const void *x, const void *const *A_ptrs, const void *co
 #define SGMV_NO_TENSOR_CORES 2u
 #define SGMV_TENSOR_CORES_ALWAYS 4u
 #define SGMV_LONG_BATCH 8u
+#define SGMV_DENSE_GRID 16u
 
 /*
  * lora_apply_ex -- lora_apply with launch flags.
@@ -159,6 +160,16 @@ int lora_apply(void *y, const void *x, const void *const *A_ptrs, const void *co
  *     of h_in are the same; the grid, and with it the split of work over CTAs, may differ).
  *     With SGMV_OVERLAP_PRIOR the next call's CTAs can only start where this call's CTAs have
  *     left, so the overlap of short calls is lost: do not use it for decode batches.
+ *   flags |= SGMV_DENSE_GRID: the caller declares a decode batch with many work items (many
+ *     rows spread over many adapter groups, for example 256 tokens over 60 or more adapters).
+ *     The kernel then runs two CTAs of this call per SM in the default geometry instead of
+ *     one, so that each SM streams two items at once; the next kernel of the stream can start
+ *     only as this call's CTAs finish, so the overlap that hides a short call's start-up is
+ *     lost.  Measured on GB300 (256 tokens, h = 4096, r = 16): 256 ids over 1024 adapters
+ *     25.7 -> 17.3 us per chained call, Zipf-drawn ids 16.0 -> 12.0 us; 64 one-token segments
+ *     of 64 adapters 6.0 -> 9.2 us (do not use it there).  Ignored with SGMV_LONG_BATCH (whose
+ *     CTAs take a whole SM).  The results agree with a launch without the flag within
+ *     rounding (the split of work over CTAs differs).
  * Other arguments, layout and errors: as for lora_apply (SGMV_EINVAL for unknown flags).
  */
 int lora_apply_ex(void *y, const void *x, const void *const *A_ptrs, const void *const *B_ptrs,

@@ -29,6 +29,7 @@ SGMV_OVERLAP_PRIOR = 1
 SGMV_NO_TENSOR_CORES = 2
 SGMV_TENSOR_CORES_ALWAYS = 4
 SGMV_LONG_BATCH = 8
+SGMV_DENSE_GRID = 16
 SGMV_MAX_LD = 1 << 24
 SYMBOLS = ("lora_apply", "lora_apply_ex", "lora_apply_strided", "sgmv_shrink", "sgmv_shrink_ex",
            "sgmv_shrink_strided", "sgmv_expand", "sgmv_expand_ex", "sgmv_expand_strided",
@@ -193,11 +194,12 @@ def _ptrs(t, name):
     return t.data_ptr()
 
 
-def _flags(overlap_prior, tensor_cores, long_batch=False) -> int:
+def _flags(overlap_prior, tensor_cores, long_batch=False, dense_grid=False) -> int:
     mode = {True: "auto", False: "never"}.get(tensor_cores, tensor_cores)
     if mode not in ("auto", "never", "always"):
         raise ValueError(f"tensor_cores must be 'auto', 'never' or 'always', not {tensor_cores!r}")
     return ((SGMV_OVERLAP_PRIOR if overlap_prior else 0) | (SGMV_LONG_BATCH if long_batch else 0) |
+            (SGMV_DENSE_GRID if dense_grid else 0) |
             {"auto": 0, "never": SGMV_NO_TENSOR_CORES, "always": SGMV_TENSOR_CORES_ALWAYS}[mode])
 
 
@@ -207,7 +209,7 @@ def _check(rc: int, where: str):
 
 
 def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None,
-               overlap_prior=False, tensor_cores="auto", long_batch=False):
+               overlap_prior=False, tensor_cores="auto", long_batch=False, dense_grid=False):
     """y[t] += scale * (x[t] A_k) B_k for every segment row (in place on y).
 
     overlap_prior=True calls lora_apply_ex with SGMV_OVERLAP_PRIOR: the kernel may stream
@@ -215,7 +217,8 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
     tensor_cores: "auto" (the library's cost rule), "never" (SGMV_NO_TENSOR_CORES) or "always"
     (SGMV_TENSOR_CORES_ALWAYS); True / False mean "auto" / "never".
     long_batch=True adds SGMV_LONG_BATCH: one CTA per SM with the whole shared memory, for
-    prefill-sized calls (see include/sgmv.h).
+    prefill-sized calls (see include/sgmv.h).  dense_grid=True adds SGMV_DENSE_GRID: two CTAs
+    of the call per SM, for decode batches with many work items (see include/sgmv.h).
     x and y may be column slices of wider matrices (unit column stride, row stride a multiple
     of 8 elements): they then go through lora_apply_strided.
     """
@@ -223,7 +226,7 @@ def lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scal
     if x.dtype != y.dtype or x.shape[0] != y.shape[0]:
         raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
     S = _table(seg_starts, seg_adapter)
-    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch, dense_grid)
     with _on(x, y, A_ptrs, B_ptrs, seg_starts, seg_adapter):
         return _lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale,
                            stream, flags, ldx, ldy, S)
@@ -251,7 +254,7 @@ def _lora_apply(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, sca
 
 
 def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None,
-                tensor_cores="auto", long_batch=False, overlap_prior=False):
+                tensor_cores="auto", long_batch=False, overlap_prior=False, dense_grid=False):
     """v[t] = x[t] A_k (fp32) for every segment row (tensor_cores, long_batch, overlap_prior as
     for lora_apply)."""
     import torch
@@ -260,7 +263,7 @@ def sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream=None
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != x.shape[0]:
         raise ValueError("v must be float32 [M, r]")
     S = _table(seg_starts, seg_adapter)
-    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch, dense_grid)
     with _on(x, v, A_ptrs, seg_starts, seg_adapter):
         return _sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream, flags,
                             ldx, S)
@@ -283,7 +286,7 @@ def _sgmv_shrink(v, x, A_ptrs, seg_starts, seg_adapter, layer_idx, r, stream, fl
 
 
 def sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream=None,
-                tensor_cores="auto", long_batch=False, overlap_prior=False):
+                tensor_cores="auto", long_batch=False, overlap_prior=False, dense_grid=False):
     """y[t] += scale * v[t] B_k for every segment row (in place on y; tensor_cores, long_batch,
     overlap_prior as for lora_apply)."""
     import torch
@@ -292,7 +295,7 @@ def sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stre
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != y.shape[0]:
         raise ValueError("v must be float32 [M, r]")
     S = _table(seg_starts, seg_adapter)
-    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch, dense_grid)
     with _on(y, v, B_ptrs, seg_starts, seg_adapter):
         return _sgmv_expand(y, v, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale, stream,
                             flags, ldy, S)
@@ -430,12 +433,12 @@ def sgmv_plan(seg_starts, seg_adapter, max_rows, stream=None, out=None) -> Plan:
 
 
 def lora_apply_planned(y, x, A_ptrs, B_ptrs, plan: Plan, layer_idx, r, scale, stream=None,
-                       overlap_prior=False, tensor_cores="auto", long_batch=False):
+                       overlap_prior=False, tensor_cores="auto", long_batch=False, dense_grid=False):
     """lora_apply with a plan instead of the segment table (x, y may be column slices)."""
     ldy, ldx = _rows(y, "y"), _rows(x, "x")
     if x.dtype != y.dtype or x.shape[0] != y.shape[0]:
         raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
-    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch, dense_grid)
     with _on(x, y, A_ptrs, B_ptrs, plan.buf):
         rc = lib().lora_apply_planned(
             y.data_ptr(), ldy, x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
@@ -446,7 +449,7 @@ def lora_apply_planned(y, x, A_ptrs, B_ptrs, plan: Plan, layer_idx, r, scale, st
 
 
 def lora_apply_static_plan(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, max_rows, layer_idx, r,
-                           scale, stream=None, tensor_cores="auto", long_batch=False):
+                           scale, stream=None, tensor_cores="auto", long_batch=False, dense_grid=False):
     """lora_apply_planned with the plan built inside the library's fixed device array: the call
     allocates no device memory (for callers that may not).  Calls that overlap on the GPU
     share that array and must be ordered; overlap_prior is not available here."""
@@ -454,7 +457,7 @@ def lora_apply_static_plan(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, max_ro
     if x.dtype != y.dtype or x.shape[0] != y.shape[0]:
         raise ValueError("x [M, h_in] and y [M, h_out] must share M and dtype")
     S = _table(seg_starts, seg_adapter)
-    flags = _flags(False, tensor_cores, long_batch)
+    flags = _flags(False, tensor_cores, long_batch, dense_grid)
     with _on(x, y, A_ptrs, B_ptrs, seg_starts, seg_adapter):
         rc = lib().lora_apply_static_plan(
             y.data_ptr(), ldy, x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),
@@ -467,7 +470,7 @@ def lora_apply_static_plan(y, x, A_ptrs, B_ptrs, seg_starts, seg_adapter, max_ro
 
 def lora_apply_base(y, x, W0, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx, r, scale,
                     v_work=None, stream=None, overlap_prior=False, tensor_cores="auto",
-                    long_batch=False):
+                    long_batch=False, dense_grid=False):
     """y = x W0^T + scale * (x A_k) B_k per segment row (x W0^T alone on other rows), written
     into y (fp16 / bf16).  W0 is [h_out, h_in] (a linear layer's weight).  v_work: fp32
     [M, r] workspace (made here with torch when not given).  Flags as for lora_apply; they
@@ -487,7 +490,7 @@ def lora_apply_base(y, x, W0, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx
         _cuda(v_work, "v_work")
         if v_work.dtype != torch.float32 or v_work.numel() < M * int(r):
             raise ValueError("v_work must hold M * r fp32 values")
-    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch, dense_grid)
     with _on(x, y, W0, seg_starts, seg_adapter):
         rc = lib().lora_apply_base(
             y.data_ptr(), ldy, x.data_ptr(), ldx, M, W0.data_ptr(), ldw,
@@ -500,13 +503,13 @@ def lora_apply_base(y, x, W0, A_ptrs, B_ptrs, seg_starts, seg_adapter, layer_idx
 
 
 def sgmv_shrink_planned(v, x, A_ptrs, plan: Plan, layer_idx, r, stream=None,
-                        tensor_cores="auto", long_batch=False, overlap_prior=False):
+                        tensor_cores="auto", long_batch=False, overlap_prior=False, dense_grid=False):
     import torch
     _cuda(v, "v")
     ldx = _rows(x, "x")
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != x.shape[0]:
         raise ValueError("v must be float32 [M, r]")
-    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch, dense_grid)
     with _on(x, v, A_ptrs, plan.buf):
         rc = lib().sgmv_shrink_planned(v.data_ptr(), x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"),
                                        plan.buf.data_ptr(), plan.num_segments, int(layer_idx),
@@ -517,13 +520,13 @@ def sgmv_shrink_planned(v, x, A_ptrs, plan: Plan, layer_idx, r, stream=None,
 
 
 def sgmv_expand_planned(y, v, B_ptrs, plan: Plan, layer_idx, r, scale, stream=None,
-                        tensor_cores="auto", long_batch=False, overlap_prior=False):
+                        tensor_cores="auto", long_batch=False, overlap_prior=False, dense_grid=False):
     import torch
     _cuda(v, "v")
     ldy = _rows(y, "y")
     if v.dtype != torch.float32 or v.dim() != 2 or v.shape[1] != r or v.shape[0] != y.shape[0]:
         raise ValueError("v must be float32 [M, r]")
-    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch, dense_grid)
     with _on(y, v, B_ptrs, plan.buf):
         rc = lib().sgmv_expand_planned(y.data_ptr(), ldy, v.data_ptr(), _ptrs(B_ptrs, "B_ptrs"),
                                        plan.buf.data_ptr(), plan.num_segments, int(layer_idx),
@@ -534,7 +537,7 @@ def sgmv_expand_planned(y, v, B_ptrs, plan: Plan, layer_idx, r, scale, stream=No
 
 
 def lora_apply_multi(projections, plan: Plan, layer_idx, r, stream=None, overlap_prior=False,
-                     tensor_cores="auto", long_batch=False):
+                     tensor_cores="auto", long_batch=False, dense_grid=False):
     """One launch over several projections: projections is a list of
     (y, x, A_ptrs, B_ptrs, scale) tuples sharing the plan, layer, rank and dtype."""
     if not 1 <= len(projections) <= SGMV_MAX_PROJECTIONS:
@@ -554,7 +557,7 @@ def lora_apply_multi(projections, plan: Plan, layer_idx, r, stream=None, overlap
                             float(scale), 0)
         tensors += [y, x, A_ptrs, B_ptrs]
     x0 = projections[0][1]
-    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch, dense_grid)
     with _on(x0, plan.buf, *tensors):
         rc = lib().lora_apply_multi(arr, len(projections), plan.buf.data_ptr(), plan.num_segments,
                                     int(layer_idx), int(r), _dtype_code(x0), flags,
@@ -564,7 +567,7 @@ def lora_apply_multi(projections, plan: Plan, layer_idx, r, stream=None, overlap
 
 def lora_apply_ranked(y, x, A_ptrs, B_ptrs, adapter_rank, adapter_scale, layer_idx, r_max,
                       seg_starts=None, seg_adapter=None, plan: Plan = None, stream=None,
-                      overlap_prior=False, tensor_cores="auto", long_batch=False):
+                      overlap_prior=False, tensor_cores="auto", long_batch=False, dense_grid=False):
     """y[t] += adapter_scale[k] (x[t] A_k) B_k with adapter k of rank adapter_rank[k] (device
     int32 and float32 tensors, one entry per adapter); the table, or a plan."""
     import torch
@@ -584,7 +587,7 @@ def lora_apply_ranked(y, x, A_ptrs, B_ptrs, adapter_rank, adapter_scale, layer_i
     else:
         S, ss, sa, pl = plan.num_segments, None, None, plan.buf.data_ptr()
         extra = (plan.buf,)
-    flags = _flags(overlap_prior, tensor_cores, long_batch)
+    flags = _flags(overlap_prior, tensor_cores, long_batch, dense_grid)
     with _on(x, y, A_ptrs, B_ptrs, adapter_rank, adapter_scale, *extra):
         rc = lib().lora_apply_ranked(
             y.data_ptr(), ldy, x.data_ptr(), ldx, _ptrs(A_ptrs, "A_ptrs"), _ptrs(B_ptrs, "B_ptrs"),

@@ -311,7 +311,7 @@ int setup_problem(const DeviceState* st, const Problem& pb, sgmv::Params& p, uin
 // Clusters of C CTAs that fit at once for this kernel and shared-memory size (one CTA per SM
 // per kernel), cached per instantiation.  Also sets the kernel's attributes.
 int grid_for(DeviceState* st, KernelCache& kc, const void* fn, int threads, size_t smem,
-             bool clustered, int C, int* grid) {
+             bool clustered, int C, int* grid, bool dense = false) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (kc.smem_set < smem) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -352,6 +352,11 @@ int grid_for(DeviceState* st, KernelCache& kc, const void* fn, int threads, size
     kc.max_clusters = n;
   }
   *grid = kc.max_clusters * C;
+  // SGMV_DENSE_GRID: two CTAs of the call per SM.  Two default-geometry CTAs fit on an SM (that
+  // is what lets the next kernel of the stream start beside this one); the occupancy query
+  // answers one cluster slot per SM for this size, so the count is set directly.  No CTA waits
+  // on a CTA of another cluster, so a grid that did not fit would only run in two waves.
+  if (dense && smem <= kPairSmem) *grid = std::max(*grid, 2 * (st->sms / C) * C);
   return SGMV_OK;
 }
 
@@ -453,7 +458,7 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
   const bool clustered = pb.mode != sgmv::kExpand;
   int grid = 0;
   rc = grid_for(st, st->cache[pb.dtype][pb.mode][rank_index(pb.r)][wide_kernel ? 1 : 0], fn,
-                threads, smem, clustered, p.C, &grid);
+                threads, smem, clustered, p.C, &grid, (flags & SGMV_DENSE_GRID) != 0);
   if (rc != SGMV_OK) return rc;
   if ((rc = finish_problem(pb, p, flags, smem, 0, grid, wide_kernel)) != SGMV_OK) return rc;
   return launch_kernel(fn, grid, threads, smem, clustered, p.C, flags, &p, stream);
@@ -461,7 +466,8 @@ int launch(const Problem& pb, sgmv::Params& p, uint32_t flags, cudaStream_t stre
 
 bool flags_ok(uint32_t flags) {
   if (flags & ~static_cast<uint32_t>(SGMV_OVERLAP_PRIOR | SGMV_NO_TENSOR_CORES |
-                                     SGMV_TENSOR_CORES_ALWAYS | SGMV_LONG_BATCH))
+                                     SGMV_TENSOR_CORES_ALWAYS | SGMV_LONG_BATCH |
+                                     SGMV_DENSE_GRID))
     return false;
   return !((flags & SGMV_NO_TENSOR_CORES) && (flags & SGMV_TENSOR_CORES_ALWAYS));
 }
@@ -821,7 +827,7 @@ int lora_apply_multi(const sgmv_projection_t* proj, int32_t num_proj, const void
   const int C = mp.prob[0].C;
   int grid = 0;
   rc = grid_for(st, st->cache[dtype][3][rank_index(r)][wide_kernel ? 1 : 0], fn, threads, smem,
-                true, C, &grid);
+                true, C, &grid, (flags & SGMV_DENSE_GRID) != 0);
   if (rc != SGMV_OK) return rc;
   // Clusters per projection, in proportion to an estimate of its bytes: the weights of an
   // adapter ((h_in + h_out) r) plus the activations of its rows (h_in + 2 h_out per row; ~4 rows

@@ -534,7 +534,8 @@ int lora_apply_base(void* y, int32_t ldy, const void* x, int32_t ldx, int32_t M,
   using namespace sgmv_base;
   if (M < 0 || num_segments < 0 || layer_idx < 0 || !y || !x || !W0) return SGMV_EINVAL;
   if (flags & ~static_cast<uint32_t>(SGMV_OVERLAP_PRIOR | SGMV_NO_TENSOR_CORES |
-                                     SGMV_TENSOR_CORES_ALWAYS | SGMV_LONG_BATCH))
+                                     SGMV_TENSOR_CORES_ALWAYS | SGMV_LONG_BATCH |
+                                     SGMV_DENSE_GRID))
     return SGMV_EINVAL;
   if (dtype != SGMV_F32 && dtype != SGMV_F16 && dtype != SGMV_BF16) return SGMV_EINVAL;
   if (dtype == SGMV_F32) return SGMV_EUNSUPPORTED;  // the tensor cores take 16-bit operands

@@ -40,6 +40,7 @@ def test_header_constants_match_binding():
     assert f"#define SGMV_NO_TENSOR_CORES {binding.SGMV_NO_TENSOR_CORES}u" in text
     assert f"#define SGMV_TENSOR_CORES_ALWAYS {binding.SGMV_TENSOR_CORES_ALWAYS}u" in text
     assert f"#define SGMV_LONG_BATCH {binding.SGMV_LONG_BATCH}u" in text
+    assert f"#define SGMV_DENSE_GRID {binding.SGMV_DENSE_GRID}u" in text
     assert "#define SGMV_MAX_LD (1 << 24)" in text and binding.SGMV_MAX_LD == 1 << 24
     assert f"#define SGMV_MAX_PROJECTIONS {binding.SGMV_MAX_PROJECTIONS}" in text
     assert f"#define SGMV_STATIC_PLAN_MAX_ROWS {binding.SGMV_STATIC_PLAN_MAX_ROWS}" in text
@@ -83,11 +84,11 @@ def test_lora_apply_ex_flags(L):
     a = OK_ARGS
     args = (a["y"], a["x"], a["A"], a["B"], a["ss"], a["sa"], 0, a["layer"], a["h_in"],
             a["h_out"], a["r"], a["scale"], a["dt"])
-    for flags in (0, 1, 2, 3, 4, 5, 8, 9, 10, 13):  # num_segments = 0: checks only, no launch
+    for flags in (0, 1, 2, 3, 4, 5, 8, 9, 10, 13, 16, 17, 25):  # num_segments = 0: no launch
         assert L.lora_apply_ex(*args, flags, None) == 0
     assert L.lora_apply_ex(*args, 6, None) == -1  # never + always
     assert L.lora_apply_ex(*args, 14, None) == -1
-    assert L.lora_apply_ex(*args, 16, None) == -1  # unknown bit
+    assert L.lora_apply_ex(*args, 32, None) == -1  # unknown bit
 
 
 def test_strided_host_checks(L):
@@ -231,7 +232,7 @@ def test_multi_host_checks(L):
     assert multi([proj(x=P + 0x10008)]) == -2
     assert multi([proj()], plan=None) == -1
     assert multi([proj()], r=24) == -3
-    assert multi([proj()], flags=16) == -1
+    assert multi([proj()], flags=32) == -1
 
 
 def test_pool_host_checks(L):
@@ -276,5 +277,5 @@ def test_base_host_checks(L):
     assert base(h_out=4092, ldy=4092) == -2
     assert base(x=P + 0x10008) == -2
     assert base(vw=v + 8) == -2
-    assert base(flags=16) == -1
+    assert base(flags=32) == -1
     assert base(S=5000) == -3

@@ -29,7 +29,7 @@ def _gpu():
     torch.cuda.empty_cache()
 
 
-def run_chain(c, layers, long_batch, seed=40):
+def run_chain(c, layers, long_batch, seed=40, dense_grid=False):
     """Back-to-back calls in one CUDA graph, as bench.py times them: call i works on its own
     (x_i, y_i) at layers[i], with SGMV_OVERLAP_PRIOR (+ SGMV_LONG_BATCH).  Returns the inputs and
     outputs of every call."""
@@ -42,7 +42,8 @@ def run_chain(c, layers, long_batch, seed=40):
     def chain():
         for (x, _), y, layer in zip(sets, ys, layers):
             lora_apply(y, x, c.A_ptrs, c.B_ptrs, c.d_ss, c.d_sa, layer, c.w.r, c.w.scale,
-                       stream=stream, overlap_prior=True, long_batch=long_batch)
+                       stream=stream, overlap_prior=True, long_batch=long_batch,
+                       dense_grid=dense_grid)
 
     with torch.cuda.stream(stream):
         chain()  # uncaptured first calls set the kernels' attributes
@@ -80,14 +81,17 @@ def test_decode_distinct_overlap_chain_full_size():
     check_chain(c, layers, sets, ys, w.name)
 
 
+# decode_zipf and decode_uniform are timed with SGMV_DENSE_GRID (two CTAs of a call per SM: many
+# rows over many adapter groups); decode_same without it.  Both forms are checked for all three.
+@pytest.mark.parametrize("dense", [False, True])
 @pytest.mark.parametrize("name", ["decode_zipf", "decode_uniform", "decode_same"])
-def test_decode_skewed_overlap_chain_full_size(name):
+def test_decode_skewed_overlap_chain_full_size(name, dense):
     w = workloads.WORKLOADS[name]
     ss, sa = workloads.make_segments(name, 0)
     c = harness.make_case(w, ss, sa)
     layers = [0, 15, 7]
-    sets, ys = run_chain(c, layers, long_batch=False)
-    check_chain(c, layers, sets, ys, name)
+    sets, ys = run_chain(c, layers, long_batch=False, dense_grid=dense)
+    check_chain(c, layers, sets, ys, f"{name} dense={dense}")
 
 
 def test_prefill_mixed_long_batch_every_row():

@@ -3,8 +3,8 @@
 Each case draws a dtype, a rank, hidden sizes (multiples of 8, often not of 64), a segment
 table mixing one-row decode segments, empty segments, segments with no adapter (-1) and long
 segments whose adapters repeat across non-adjacent segments (tensor-core groups), and the
-launch options (tensor-core routing, long-batch geometry, programmatic overlap, column-slice
-views).  Every output row is compared with the fp64 oracle
+launch options (tensor-core routing, long-batch geometry, two CTAs per SM, programmatic
+overlap, column-slice views).  Every output row is compared with the fp64 oracle
 (|y - y_ref| <= 1e-2 + 1e-2 |y_ref|); rows without an adapter and the elements outside a
 slice must be bit-for-bit unchanged.  The draws are fixed by the seed, so a failure is
 reproducible by its case index.  SGMV_FUZZ_CASES sets the number of cases (default 100).
@@ -84,6 +84,10 @@ def test_random_case_matches_oracle(i):
         x, y = X[:, 8:8 + h_in], Y[:, 16:16 + h_out]
     else:
         x, y = c.x, c.y0.clone()
+    # SGMV_DENSE_GRID (two CTAs of the call per SM) on a third of the cases, drawn apart so
+    # that the other draws stay as they were
+    opts = dict(opts, dense_grid=bool(np.random.default_rng(777 + i).random() < 0.3))
+    what += f" dense={opts['dense_grid']}"
     lora_apply(y, x, c.A_ptrs, c.B_ptrs, c.d_ss, c.d_sa, layer, r, w.scale, **opts)
     torch.cuda.synchronize()
     harness.assert_close(y.float().cpu().numpy(), harness.oracle_apply(c, layer), what)
@@ -138,6 +142,8 @@ def test_random_planned_case_matches_oracle(i):
     what = f"planned case {i}: {dtype} r{r} {h_in}->{h_out} lens={lens} ids={ids} {opts}"
     plan = sgmv_plan(c.d_ss, c.d_sa, max(1, int(ss[-1])))
     y = c.y0.clone()
+    opts = dict(opts, dense_grid=bool(np.random.default_rng(888 + i).random() < 0.5))
+    what += f" dense={opts['dense_grid']}"
     lora_apply_planned(y, c.x, c.A_ptrs, c.B_ptrs, plan, layer, r, w.scale, **opts)
     torch.cuda.synchronize()
     harness.assert_close(y.float().cpu().numpy(), harness.oracle_apply(c, layer), what)
