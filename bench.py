@@ -457,9 +457,12 @@ def measure_multi(torch, device, stream, seconds):
     plan = setups[0].plan
     n = setups[0].calls
 
+    # one launch carries three projections' work items (192 of them): the many-item geometry
+    # (SGMV_DENSE_GRID, two CTAs per SM), as a caller batching projections would declare it
     def multi(i, stream=None):
         lora_apply_multi([(st.y[i], st.x[i], st.A_ptrs, st.B_ptrs, w.scale) for st in setups],
-                         plan, i % w.layers, w.r, stream=stream, overlap_prior=True)
+                         plan, i % w.layers, w.r, stream=stream, overlap_prior=True,
+                         dense_grid=True)
 
     def three(i, stream=None):
         for st in setups:
@@ -477,8 +480,8 @@ def measure_multi(torch, device, stream, seconds):
         out[f"us_per_layer_{label}"] = round(us, 3)
         out[f"GB_per_s_{label}"] = round(3 * nbytes / us / 1e3, 2)
         del g
-    out["launch"] = ("lora_apply_multi (one launch per layer for q, k, v) vs three "
-                     "lora_apply_planned launches, SGMV_OVERLAP_PRIOR")
+    out["launch"] = ("lora_apply_multi (one launch per layer for q, k, v; SGMV_OVERLAP_PRIOR | "
+                     "SGMV_DENSE_GRID) vs three lora_apply_planned launches (SGMV_OVERLAP_PRIOR)")
     del setups
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

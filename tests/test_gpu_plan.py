@@ -174,9 +174,12 @@ def test_planned_prefill_and_70b():
         torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("dtype,r,long_batch", [("f16", 16, False), ("bf16", 64, True),
-                                                ("f32", 8, False)])
-def test_multi_projection_one_launch(dtype, r, long_batch):
+@pytest.mark.parametrize("dtype,r,long_batch,dense", [("f16", 16, False, False),
+                                                      ("bf16", 64, True, False),
+                                                      ("f32", 8, False, False),
+                                                      ("f16", 16, False, True),
+                                                      ("bf16", 32, False, True)])
+def test_multi_projection_one_launch(dtype, r, long_batch, dense):
     """q / k / v-like projections (h_out 1024, 256, 256; k and v on column slices of one fused
     output) and a gate-like one (h_out 2048) in one lora_apply_multi launch, each against the
     oracle.  (Each projection runs on a share of the grid, so the CUDA-core role may split its
@@ -199,7 +202,7 @@ def test_multi_projection_one_launch(dtype, r, long_batch):
     ys[2].copy_(cases[2].y0)
     plan = _plan(cases[0], M)
     lora_apply_multi([(y, x, c.A_ptrs, c.B_ptrs, c.w.scale) for y, c in zip(ys, cases)], plan, 1,
-                     r, long_batch=long_batch)
+                     r, long_batch=long_batch, dense_grid=dense)
     for q, (y, c) in enumerate(zip(ys, cases)):
         harness.assert_close(y.float().cpu().numpy(), harness.oracle_apply(c, 1, x=x),
                              f"multi projection {q}")
