@@ -59,6 +59,11 @@ constexpr int kTcMinRows = 64;
 // ... when their CUDA-core items would re-read at least this many MB of weights (ceil(rows / 4)
 // items x the adapter's A and B bytes).
 constexpr int kTcMinMB = 32;
+// The shrink-only launch streams A alone, half the bytes of a fused item at the same rank: it
+// takes the tensor cores from a lower volume (measured on the prefill mix, rank 64, groups of
+// 142-195 rows: on the CUDA cores those groups made sgmv_shrink 60 us; rank-16 decode groups
+// of up to 256 rows (8 MB) stay faster on the CUDA cores).
+constexpr int kTcMinMBShrink = 16;
 // Cost of one partial-sum exchange through distributed shared memory, in streamed KB (the
 // group-size rule of the CUDA-core role).
 constexpr int kXchgKB = 64;
@@ -398,7 +403,8 @@ int finish_problem(const Problem& pb, sgmv::Params& p, uint32_t flags, size_t sm
       const double w = static_cast<double>(pb.r) * 2.0 *
                        ((pb.mode != sgmv::kExpand ? pb.h_in : 0) +
                         (pb.mode != sgmv::kShrink ? pb.h_out : 0));
-      const double items = std::ceil(kTcMinMB * 1048576.0 / w);
+      const double min_mb = pb.mode == sgmv::kShrink ? kTcMinMBShrink : kTcMinMB;
+      const double items = std::ceil(min_mb * 1048576.0 / w);
       p.tc_min_rows = (flags & SGMV_TENSOR_CORES_ALWAYS)
                           ? 64
                           : static_cast<int>(std::min(

@@ -205,7 +205,19 @@ struct TcRole {
     const int warp = lt >> 5, lane = lt & 31;
     const T* x = static_cast<const T*>(p.x);
     const T* y = static_cast<const T*>(p.y);
-    pdl_wait_prior();  // x and y may be written by the previous kernel of the stream
+    // x and y may be written by the previous kernel of the stream; the segment table, the row
+    // map, the pointer arrays and the weights may not (the launch contract of a programmatic
+    // dependent).  So the first m-tile's row table and the weight part of each warp's first
+    // slot (never used before: no wait on a consumer) are issued at once, and the activation
+    // parts of those slots right after the wait on the previous kernel, which comes before the
+    // warp's next slot or at the end of the first m-tile.  One slot per warp: a second one's
+    // weight copies would hold back the first one's x copy whenever the previous kernel has
+    // already completed (measured on GB300, 8-slot ring: 0.5-0.9 us per call slower; 4-slot
+    // ring, 256 rows of one adapter on the tensor cores: 16.7 -> 11.6 us per chained call).
+    constexpr int kDefer = 4;  // loader warps
+    bool prior_done = !p.dependent;
+    uint32_t deferred = 0;  // first-round slots of this warp whose activation part is pending
+    int seq = 0;            // position in the slot sequence (every warp counts every slot)
     Ring rg{0, 0};
     bool ok = true;
     for (int li = 0; ok && wk.next(); ++li) {
@@ -249,7 +261,8 @@ struct TcRole {
       // no warp can run ahead of, or fall two phases behind, the table barriers -- even a warp
       // that fills no slot of this m-tile.
       if (!wwait(w, c.fx(kTcRtFull0 + par), (li >> 1) & 1)) break;
-      const int n_sl = (c.k_hi - c.k_lo) + (kDoExpand ? wk.b - wk.a : 0);
+      const int nsh = c.k_hi - c.k_lo;  // shrink slots of the m-tile (they come first)
+      const int n_sl = nsh + (kDoExpand ? wk.b - wk.a : 0);
       bool mine = false;
       for (int i = 0, sl = rg.s; i < min(n_sl, c.slots); ++i) {
         mine = mine || (sl & 3) == warp;
@@ -257,6 +270,7 @@ struct TcRole {
       }
       if (!mine) {
         for (int i = 0; i < n_sl; ++i) rg.next(c.slots);
+        seq += n_sl;
         __syncwarp();
         if (lane == 0) mbar_arrive(c.fx(kTcRtFree0 + par));
         continue;
@@ -288,12 +302,10 @@ struct TcRole {
       const T* Bk = kDoExpand ? static_cast<const T*>(p.B_ptrs[k]) +
                                     static_cast<size_t>(p.layer) * rk * p.h_out
                               : nullptr;
-      // shrink slots: x rows [128 x 64] + A rows [64 x r]
-      for (int kc = c.k_lo; kc < c.k_hi; ++kc, rg.next(c.slots)) {
-        if ((rg.s & 3) != warp) continue;
-        if (!wwait(w, c.empty(rg.s), rg.par ^ 1u)) { ok = false; break; }
-        const uint32_t dst = c.slot(rg.s), bar = c.full(rg.s);
-        const int k0 = kc * kTcK;
+      // Activation part of a shrink slot (the x rows [128 x 64] of h_in chunk k0) and of an
+      // expand slot (the y rows [128 x 64] of h_out chunk n0): the slot's TMA bytes, and each
+      // lane's arrival, which covers every cp.async the lane issued before it (weights too).
+      auto acts_x = [&](uint32_t dst, uint32_t bar, int k0) {
         if (lane == 0) {
           mbar_arrive_expect_tx(bar, tx);
           if (whole) tma_load_2d(dst, &p.tmap_x128, k0, tile_tok, bar);
@@ -318,6 +330,55 @@ struct TcRole {
               cp_async16_zero(d, x);
           }
         }
+        cp_async_arrive(bar);
+      };
+      auto acts_y = [&](uint32_t dst, uint32_t bar, int n0) {
+        const int nvalid = min(kTcN, p.h_out - n0) >> 3;  // 16-byte chunks in range
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, tx);
+          if (whole) tma_load_2d(dst + kYSlotOff, &p.tmap_y128, n0, tile_tok, bar);
+        }
+        if (my_box) tma_load_2d(dst + kYSlotOff + 1024u * lane, &p.tmap_y8, n0, box_tok, bar);
+        if (pbox) {
+          const uint32_t d = dst + kYSlotOff + 128u * prow;
+          if (pbox == 64) tma_load_2d(d, &p.tmap_y64, n0, box_tok, bar);
+          else if (pbox == 32) tma_load_2d(d, &p.tmap_y32, n0, box_tok, bar);
+          else if (pbox == 16) tma_load_2d(d, &p.tmap_y16, n0, box_tok, bar);
+          else tma_load_2d(d, &p.tmap_y8, n0, box_tok, bar);
+        }
+        if (!all_boxes) {
+          for (int u = lane; u < kTcRows * 8; u += 32) {
+            const int m = u >> 3, ch = u & 7;
+            const int tok = rt[m];
+            if (tok < 0 || ch >= nvalid || ((mask >> (m >> 3)) & 1u)) continue;
+            cp_async16(dst + kYSlotOff + sw128(m, ch),
+                       y + static_cast<size_t>(tok) * p.ldy + n0 + ch * 8);
+          }
+        }
+        cp_async_arrive(bar);
+      };
+      // The wait on the previous kernel, then the pending activation parts.  Deferred slots
+      // belong to the first round of the first m-tile, where slot s holds sequence position s.
+      auto release = [&]() {
+        pdl_wait_prior();
+        prior_done = true;
+        for (int s = 0; s < c.slots; ++s) {
+          if (!((deferred >> s) & 1u)) continue;
+          if (s < nsh) acts_x(c.slot(s), c.full(s), (c.k_lo + s) * kTcK);
+          else acts_y(c.slot(s), c.full(s), (wk.a + s - nsh) * kTcN);
+          issued |= 1u << s;
+          parity &= ~(1u << s);
+        }
+        deferred = 0;
+      };
+      // shrink slots: x rows [128 x 64] + A rows [64 x r]
+      for (int kc = c.k_lo; kc < c.k_hi; ++kc, rg.next(c.slots), ++seq) {
+        if ((rg.s & 3) != warp) continue;
+        const bool defer = !prior_done && li == 0 && seq < min(kDefer, c.slots);
+        if (!prior_done && !defer) release();
+        if (!wwait(w, c.empty(rg.s), rg.par ^ 1u)) { ok = false; break; }
+        const uint32_t dst = c.slot(rg.s), bar = c.full(rg.s);
+        const int k0 = kc * kTcK;
         constexpr int kCpr = R / 8;  // 16-byte chunks per A row
         if (rk == R) {  // every unranked call: constant strides
 #pragma unroll 4
@@ -340,30 +401,24 @@ struct TcRole {
               cp_async16_zero(d, Ak);
           }
         }
-        cp_async_arrive(bar);
+        if (defer) {
+          deferred |= 1u << rg.s;
+          continue;
+        }
+        acts_x(dst, bar, k0);
         issued |= 1u << rg.s;
         parity = (parity & ~(1u << rg.s)) | (rg.par << rg.s);
       }
       if (!ok) break;
       // expand slots: B rows [r x 64] + y rows [128 x 64]
-      for (int nt = wk.a; kDoExpand && nt < wk.b; ++nt, rg.next(c.slots)) {
+      for (int nt = wk.a; kDoExpand && nt < wk.b; ++nt, rg.next(c.slots), ++seq) {
         if ((rg.s & 3) != warp) continue;
+        const bool defer = !prior_done && li == 0 && seq < min(kDefer, c.slots);
+        if (!prior_done && !defer) release();
         if (!wwait(w, c.empty(rg.s), rg.par ^ 1u)) { ok = false; break; }
         const uint32_t dst = c.slot(rg.s), bar = c.full(rg.s);
         const int n0 = nt * kTcN;
         const int nvalid = min(kTcN, p.h_out - n0) >> 3;  // 16-byte chunks in range
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar, tx);
-          if (whole) tma_load_2d(dst + kYSlotOff, &p.tmap_y128, n0, tile_tok, bar);
-        }
-        if (my_box) tma_load_2d(dst + kYSlotOff + 1024u * lane, &p.tmap_y8, n0, box_tok, bar);
-        if (pbox) {
-          const uint32_t d = dst + kYSlotOff + 128u * prow;
-          if (pbox == 64) tma_load_2d(d, &p.tmap_y64, n0, box_tok, bar);
-          else if (pbox == 32) tma_load_2d(d, &p.tmap_y32, n0, box_tok, bar);
-          else if (pbox == 16) tma_load_2d(d, &p.tmap_y16, n0, box_tok, bar);
-          else tma_load_2d(d, &p.tmap_y8, n0, box_tok, bar);
-        }
         if (rk == R) {  // every unranked call
 #pragma unroll 4
           for (int u = lane; u < R * 8; u += 32) {
@@ -383,19 +438,17 @@ struct TcRole {
                          Bk + static_cast<size_t>(kr) * p.h_out + n0 + cc * 8);
           }
         }
-        if (!all_boxes) {
-          for (int u = lane; u < kTcRows * 8; u += 32) {
-            const int m = u >> 3, ch = u & 7;
-            const int tok = rt[m];
-            if (tok < 0 || ch >= nvalid || ((mask >> (m >> 3)) & 1u)) continue;
-            cp_async16(dst + kYSlotOff + sw128(m, ch),
-                       y + static_cast<size_t>(tok) * p.ldy + n0 + ch * 8);
-          }
+        if (defer) {
+          deferred |= 1u << rg.s;
+          continue;
         }
-        cp_async_arrive(bar);
+        acts_y(dst, bar, n0);
         issued |= 1u << rg.s;
         parity = (parity & ~(1u << rg.s)) | (rg.par << rg.s);
       }
+      // the activation parts still pending (the m-tile ended within the first round): issued
+      // before the table is released, since they read it
+      if (ok && deferred) release();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.fx(kTcRtFree0 + par));
     }
@@ -877,9 +930,12 @@ struct TcRole {
     // single CTAs otherwise.
     const int unit = c.split ? rank >> 2 : rank;
     const int n_units = c.split ? n_tc >> 2 : n_tc;
-    if (n_mt <= n_units) {
+    if (n_mt <= n_units && c.split) {
       // Fewer m-tiles than units: every m-tile gets its own floor / ceil(n_units / n_mt)
-      // units, which split its n-tiles, so that no unit repeats a second shrink.
+      // units, which split its n-tiles, so that no unit repeats a second shrink.  (Without a
+      // shrink, a range that crosses m-tiles costs one more read of v rows, so the expand-only
+      // form always takes the equal contiguous ranges below: measured on the prefill mix,
+      // whole m-tiles per unit left 12 of 152 CTAs with 43 n-tiles against 34-35.)
       const int mi = static_cast<int>(static_cast<long long>(unit) * n_mt / n_units);
       const int first =
           static_cast<int>((static_cast<long long>(mi) * n_units + n_mt - 1) / n_mt);
