@@ -931,19 +931,19 @@ struct TcRole {
     const int unit = c.split ? rank >> 2 : rank;
     const int n_units = c.split ? n_tc >> 2 : n_tc;
     if (n_mt <= n_units && c.split) {
-      // Fewer m-tiles than units: every m-tile gets its own floor / ceil(n_units / n_mt)
-      // units, which split its n-tiles, so that no unit repeats a second shrink.  (Without a
-      // shrink, a range that crosses m-tiles costs one more read of v rows, so the expand-only
-      // form always takes the equal contiguous ranges below: measured on the prefill mix,
-      // whole m-tiles per unit left 12 of 152 CTAs with 43 n-tiles against 34-35.)
-      const int mi = static_cast<int>(static_cast<long long>(unit) * n_mt / n_units);
-      const int first =
-          static_cast<int>((static_cast<long long>(mi) * n_units + n_mt - 1) / n_mt);
-      const int next =
-          static_cast<int>((static_cast<long long>(mi + 1) * n_units + n_mt - 1) / n_mt);
-      const int j = unit - first, cnt = next - first;
-      wk.u = mi * wk.ntile + j * wk.ntile / cnt;
-      wk.u1 = mi * wk.ntile + (j + 1) * wk.ntile / cnt;
+      // Fewer m-tiles than units: every m-tile gets the same k = floor(n_units / n_mt) units,
+      // which split its n-tiles, so that no unit repeats a second shrink; the other units
+      // idle.  Giving the remainder to some m-tiles cannot shorten the launch (the m-tiles
+      // with k units still take as long) and adds their shrinks to the HBM traffic: measured
+      // on the prefill mix (31 m-tiles, 36 clusters), 60.3 us with 5 m-tiles shared by two
+      // clusters, 57.2 us with those 5 clusters idle.  (Without a shrink, a range that crosses
+      // m-tiles costs one more read of v rows, so the expand-only form always takes the equal
+      // contiguous ranges below: whole m-tiles per unit left 12 of 152 CTAs with 43 n-tiles
+      // against 34-35 there.)
+      const int k = n_units / n_mt;
+      const int mi = unit / k, j = unit - mi * k;
+      wk.u = mi < n_mt ? mi * wk.ntile + j * wk.ntile / k : 0;
+      wk.u1 = mi < n_mt ? mi * wk.ntile + (j + 1) * wk.ntile / k : 0;
     } else {  // contiguous equal ranges of the (m-tile, n-tile) sequence
       const long long U = static_cast<long long>(n_mt) * wk.ntile;
       wk.u = static_cast<int>(U * unit / n_units);
