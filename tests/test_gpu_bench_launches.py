@@ -127,3 +127,34 @@ def test_mixed_70b_long_batch_layers():
     check_chain(c, layers, sets, ys, w.name + " long batch")
     del c, sets, ys
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("long_batch", [True, False])
+def test_prefill_mixed_unfused_pair_every_row(long_batch):
+    """The bench's unfused leg at full size: sgmv_shrink into v, then sgmv_expand from it, both
+    with SGMV_OVERLAP_PRIOR on one stream (the expand reads the v the shrink just wrote).  The
+    shrink-only routing sends every prefill group (142-891 rows, rank 64) to the tensor role.
+    v is compared with the oracle's shrink, y with the oracle's expand of the library's v."""
+    import oracle
+    from segmented_gather_gemm_sgmv_gb300 import sgmv_expand, sgmv_shrink
+    w = workloads.WORKLOADS["prefill_mixed"]
+    ss, sa = workloads.make_segments(w.name, 0)
+    c = harness.make_case(w, ss, sa, seed=5)
+    v = torch.full((c.M, w.r), float("nan"), dtype=torch.float32, device="cuda")
+    y = c.y0.clone()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    kw = dict(stream=stream, overlap_prior=True, long_batch=long_batch)
+    with torch.cuda.stream(stream):
+        sgmv_shrink(v, c.x, c.A_ptrs, c.d_ss, c.d_sa, 0, w.r, **kw)
+        sgmv_expand(y, v, c.B_ptrs, c.d_ss, c.d_sa, 0, w.r, w.scale, **kw)
+    torch.cuda.synchronize()
+    keys = harness.touched(c.sa, c.ss)
+    rows = harness.row_adapters(c.ss, c.sa, c.M) >= 0
+    v_gpu = v.double().cpu().numpy()
+    v_ref = oracle.sgmv_shrink(np.zeros((c.M, w.r)), c.x.double().cpu().numpy(),
+                               harness.oracle_blocks(c.A, keys, 0), c.ss, c.sa, 0)
+    harness.assert_close(v_gpu[rows], v_ref[rows], "v")
+    y_ref = oracle.sgmv_expand(c.y0.double().cpu().numpy(), np.where(rows[:, None], v_gpu, 0.0),
+                               harness.oracle_blocks(c.B, keys, 0), c.ss, c.sa, 0, w.scale)
+    harness.assert_close(y.float().cpu().numpy(), y_ref, "y")
